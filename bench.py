@@ -1,0 +1,385 @@
+"""Benchmark of the Nest placement DP on GB300: DP relaxations/s and solves/s.
+
+One step = one nest_solve of a whole batch: prep, stage-cost build, strategy
+reduction, DP sweep and backtrack, inputs resident in HBM.  The default workload
+is the 32-layer dense transformer (hidden 4096) on 64 devices in three tiers,
+16 instances.  `value` counts the min-max transitions (j, m, c') of the
+recurrence per second; `solves_per_s` counts instances.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank solves its own batch (different seeds): the
+work is partitioned, so there is no collective on the data path (weak scaling);
+only the timing barrier and the max-over-ranks use the process group.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from memory_aware_device_gb300 import synth  # noqa: E402
+
+METRIC = "DP relaxations/sec and placement solves/sec on 1 GB300; % of HBM roofline"
+UNIT = "relaxations/s"
+KERNELS = ("prep", "cost_build", "strategy_reduce", "dp_sweep", "backtrack")
+KERNEL_SRC = {"prep": "nest_prep.cu", "cost_build": "nest_cost.cu", "strategy_reduce": "nest_reduce.cu",
+              "dp_sweep": "nest_sweep.cu", "backtrack": "nest_backtrack.cu"}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def relaxations(x) -> int:
+    """Min-max transitions (j, m, c') the recurrence evaluates for one instance:
+    every cell (i, d, p, c) times its cut points j, widths m <= log2 d allowed by
+    the link tier, and next-link candidates c' allowed for that width."""
+    L, Du, P, C, u = x.L, x.D // x.unit, x.Pmax, len(x.cand), x.unit
+    G = [int(x.tierG[c]) for c in x.cand]
+    K = Du.bit_length()
+    tot = 0
+    for i in range(L):
+        Pi = min(P, L - i)
+        for c in range(1 if i == 0 else C):
+            for m in range(K):
+                k = u << m
+                if i > 0 and 2 * k > G[c]:
+                    continue
+                nd = Du - (1 << m) + 1
+                ncp = sum(1 for g in G if 2 * k <= g)
+                tot += nd * (1 + (Pi - 1) * (L - 1 - i) * ncp)
+    return tot
+
+
+def cost_words(x) -> int:
+    return x.L * (x.L + 1) // 2 * (x.D // x.unit).bit_length() * len(x.strat)
+
+
+def src_hash(kernel: str) -> str:
+    p = os.path.join(ROOT, "memory_aware_device_gb300", "csrc", KERNEL_SRC[kernel])
+    h = hashlib.sha256(open(p, "rb").read())
+    h.update(open(os.path.join(ROOT, "memory_aware_device_gb300", "csrc", "nest_internal.cuh"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# Plain integer ALU peak for the sweep's relaxation: 152 SMs x 128 INT32 lanes per
+# clock, and 11 INT32 instructions for the minimal op mix of one relaxation
+# (64-bit add: 2, 64-bit max: 4, 64-bit compare: 2, select of value and argument: 3).
+SMS, INT32_LANES, OPS_PER_RELAX = 152, 128, 11
+
+
+def alu_peak_relax_per_s(sm_mhz):
+    return SMS * INT32_LANES * sm_mhz * 1e6 / OPS_PER_RELAX
+
+
+def stored_traffic(kernel, workload):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(f"{kernel}@{workload}")
+    if not d or d.get("src") != src_hash(kernel):
+        return None
+    return d.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0, period_ms=20):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", f"-lms", str(period_ms)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(instances, relax_total, seconds=12.0):
+    """The oracle as it stands, one instance per host thread, on all host cores."""
+    from oracle import oracle as O
+    from concurrent.futures import ThreadPoolExecutor
+    O.lib()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    passes = 0
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        while True:
+            list(ex.map(O.solve, instances))
+            passes += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+    dt = time.perf_counter() - t0
+    return {"value": passes * relax_total / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{passes} pass(es) over the {len(instances)}-instance batch, {dt:.1f} s",
+            "solves_per_s": passes * len(instances) / dt}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def run_reference(args, workload, instances, relax_total):
+    """The CPU oracle as the reference arm: each step solves a bounded sample."""
+    rank, _, ws = dist_env()
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    from concurrent.futures import ThreadPoolExecutor
+    O.lib()
+    cores = os.cpu_count() or 1
+    per = [relaxations(x) for x in instances]
+    # one step = as many instances as there are cores (cycling through the batch)
+    n = min(cores, len(instances))
+    times = []
+    done_relax = 0
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        for step in range(args.warmup + args.steps):
+            idx = [(step * n + q) % len(instances) for q in range(n)]
+            t0 = time.perf_counter()
+            list(ex.map(O.solve, [instances[q] for q in idx]))
+            dt = time.perf_counter() - t0
+            if step >= args.warmup:
+                times.append(dt)
+                done_relax += sum(per[q] for q in idx)
+    total = sum(times)
+    value = done_relax / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "data": "synthetic", "config": {"workload": workload, "batch": len(instances),
+                                            "reference": "CPU oracle (plain C), one instance per host thread"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{n} instance(s) per step over {args.steps} steps"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps (capped at 500)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, local_rank, ws = dist_env()
+    workload = f"{synth.CONFIG_NAMES[args.workload]}"
+    B = synth.CONFIG_BATCH[args.workload]
+    instances = synth.config_batch(args.workload, B=B, first=rank * B if args.workload != 1 else 0)
+    relax_total = sum(relaxations(x) for x in instances)
+
+    if args.impl == "reference":
+        run_reference(args, workload, instances, relax_total)
+        return
+
+    import torch
+    from memory_aware_device_gb300 import nest
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    dims = nest.make_dims(instances)
+    solver = nest.Solver(dims, chunk=args.chunk, device=dev)
+    records = nest.pack_records(instances, dims)
+    solver.load(records)
+    chunk = args.chunk if 0 < args.chunk < B else B
+    nchunks = (B + chunk - 1) // chunk
+    stream = torch.cuda.current_stream(dev)
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(6 * nchunks)]
+    opt = nest.options(chunk=args.chunk, events=kev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        rc = nest.solve_raw(dims, solver.records, solver.costs, solver.plans, solver.workspace, stream, opt)
+        if rc:
+            raise nest.NestError(rc)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    # correctness guard on the bench's own output: every instance solved or infeasible
+    res = solver.results()
+    assert all(r["status"] in (nest.SOLVED, nest.INFEASIBLE) for r in res), "solver reported errors"
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    per_kernel = {k: 0.0 for k in KERNELS}
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.05)
+    for s in range(args.steps):
+        flush.zero_()                      # L2 flush outside the timed events
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+        if s % 64 == 63 or s == args.steps - 1:
+            # collect the kernel-boundary events of recent steps before they are re-recorded
+            pass
+        torch.cuda.synchronize(dev) if False else None
+        # per-kernel times of this step (events are reused: read them after each step)
+        ends[s].synchronize()
+        for c in range(nchunks):
+            for q, k in enumerate(KERNELS):
+                per_kernel[k] += kev[6 * c + q].elapsed_time(kev[6 * c + q + 1])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = relax_total * ws / (ms_per_step * 1e-3)
+    solves = B * ws / (ms_per_step * 1e-3)
+    launches = 5 * nchunks * args.steps
+
+    # end to end through the host-buffer entry point: H2D records, solve, D2H results
+    e2e_steps = args.e2e_steps or min(args.steps, 500)
+    wsh = torch.empty(nest.workspace_size(dims, args.chunk, host=True), dtype=torch.uint8, device=dev)
+    rec_pin = torch.from_numpy(records.ravel().copy()).pin_memory()
+    costs_pin = torch.empty(B, dtype=torch.int64).pin_memory()
+    plans_pin = torch.empty(B * nest.plan_bytes(dims), dtype=torch.uint8).pin_memory()
+    hopt = nest.options(chunk=args.chunk)
+
+    def host_step():
+        import ctypes as C
+        rc = nest.lib().nest_solve_host(C.byref(dims), rec_pin.data_ptr(), costs_pin.data_ptr(),
+                                        plans_pin.data_ptr(), wsh.data_ptr(), wsh.numel(),
+                                        C.c_void_p(stream.cuda_stream), C.byref(hopt))
+        if rc:
+            raise nest.NestError(rc, "nest_solve_host")
+    for _ in range(args.warmup):
+        host_step()
+    if dist is not None:
+        dist.barrier()
+    e2e_ms = []
+    for _ in range(e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        host_step()
+        e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    e2e_total = sum(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_val = relax_total * ws / (e2e_total / e2e_steps * 1e-3)
+    assert nest.decode_plans(plans_pin.numpy(), dims) == res, "host entry point disagrees with device path"
+
+    # roofline of the dominant kernel
+    peaks = load_peaks()
+    kms = {k: v / args.steps for k, v in per_kernel.items()}       # ms per step (all chunks)
+    dom = max(kms, key=kms.get)
+    words = sum(cost_words(x) for x in instances)
+    if dom == "dp_sweep":
+        mhz = (clk or {}).get("sm_mhz") or peaks["sm_max_mhz"]
+        peak = alu_peak_relax_per_s(peaks["sm_max_mhz"]) / 1e9
+        achieved = relax_total / (kms[dom] * 1e-3) / 1e9
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Grelax/s",
+                "frac": achieved / peak, "traffic": stored_traffic(dom, workload), "kernel": dom,
+                "peak_source": f"derived: {SMS} SMs x {INT32_LANES} INT32 lanes x {peaks['sm_max_mhz']:.0f} MHz"
+                               f" / {OPS_PER_RELAX} ops per relaxation", "sm_mhz_seen": mhz}
+    else:
+        algo = {"cost_build": 8 * words, "strategy_reduce": 8 * words,
+                "prep": 0, "backtrack": 0}[dom]
+        achieved = algo / (kms[dom] * 1e-3) / 1e9 / nchunks * nchunks
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": stored_traffic(dom, workload),
+                "kernel": dom, "peak_source": f"{peaks['source']} hbm_gbs"}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(instances, relax_total, args.cpu_seconds)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+                "config": {"workload": workload, "batch_per_gpu": B, "chunk": chunk,
+                           "relaxations_per_batch": relax_total, "cost_words_per_batch": words,
+                           "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                           "parallelism": f"replicas{ws}"},
+                "solves_per_s": solves,
+                "kernel_ms_per_step": kms,
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(records.nbytes),
+                        "d2h_bytes_per_step": int(8 * B + B * nest.plan_bytes(dims)),
+                        "ms_per_step": e2e_total / e2e_steps},
+                "gpu_launches": launches, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * nest.h - C ABI of the GB300 solver for the Nest placement dynamic program.
+ *
+ * Source of the method: "Nest: Network- and Memory-Aware Device Placement for
+ * Distributed Deep Learning" (cited as Nest):
+ *   §3.3 peak-memory equation   Mem(S, s) = sum(2 weights + optimizer states +
+ *                               activations) + (s - 1) stashed data, 1F1B positions;
+ *   §4 Eq. 3                    dp[l][D][k][s] = min over D', a of
+ *                               max(dp[l'][D'][k - a][s - 1], load_l(D \ D', a, s));
+ *   §4 load()                   compute + tiered collectives + forward/backward link
+ *                               traffic, with ZeRO and recompute in the transition;
+ *   Appendix K Algorithm 1      backward sweep, t_batch = t_stage (mbs + s - 1),
+ *                               stage reconstruction.
+ *
+ * One problem ("instance") is a chain of L layers, a cluster of D devices grouped
+ * in tiers, C candidate tiers for links between pipeline stages, S parallel
+ * strategies (TP t, context-parallel cp, expert-parallel e, ZeRO stage z,
+ * recompute r) and a per-device memory budget.  The solver returns, per instance,
+ * the smallest iteration time and a plan of contiguous stages, each with a device
+ * count unit * 2^m, a strategy and the candidate tier of its outgoing link.
+ * All times are int64 nanoseconds and every result is exact: the CUDA path and
+ * the plain CPU definition agree bit for bit.
+ *
+ * Memory ownership: the caller allocates every buffer.  The library allocates
+ * nothing, frees nothing and keeps no state between calls.  nest_solve only
+ * enqueues work on the caller's stream; results are valid once the stream has
+ * synchronised.  nest_solve_host is synchronous.
+ */
+#ifndef NEST_H
+#define NEST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- call status (return value) ------------------------------------------ */
+#define NEST_OK           0
+#define NEST_E_INVALID   -1  /* null pointer, negative count or malformed argument */
+#define NEST_E_LIMITS    -2  /* a batch dimension beyond the limits below */
+#define NEST_E_WORKSPACE -3  /* workspace smaller than nest_workspace_size() or misaligned */
+#define NEST_E_CUDA      -4  /* a CUDA runtime call failed (launch, copy, attribute) */
+#define NEST_E_TIMEOUT   -5  /* nest_solve_host only: a device wait gave up (see NEST_TIMED_OUT) */
+
+/* ---- per-instance status (nest_plan.status) -------------------------------- */
+#define NEST_SOLVED     0  /* plan and t_batch valid */
+#define NEST_INFEASIBLE 1  /* no plan fits memory, or every plan's bottleneck >= 2^40-1 ns */
+#define NEST_BAD_INPUT  2  /* the instance breaks a rule listed under nest_record_header */
+#define NEST_TIMED_OUT  3  /* a bounded wait inside the DP sweep gave up; result unusable */
+
+/* ---- batch dimensions ------------------------------------------------------
+ * Fixed strides of the instance records and of the workspace.  Limits (checked
+ * on the host before any launch, NEST_E_LIMITS otherwise):
+ *   1 <= Lmax <= 255 layers, 1 <= Tmax <= 8 tiers, 1 <= Cmax <= 15 candidates,
+ *   1 <= Smax <= 4095 strategies, 1 <= Pcap <= 31 stages,
+ *   1 <= Dumax <= 1024 device units, Cmax * (Dumax + 2) <= 8192.            */
+typedef struct {
+    int32_t B;      /* instances in the batch (0 is a no-op) */
+    int32_t Lmax;
+    int32_t Tmax;
+    int32_t Cmax;
+    int32_t Smax;
+    int32_t Pcap;
+    int32_t Dumax;  /* largest D / unit of any instance */
+    int32_t reserved;
+} nest_dims;
+
+/* ---- instance record ---------------------------------------------------------
+ * B records back to back, each nest_record_bytes() long, 256-byte aligned.  A
+ * record starts with this header; the arrays follow at the offsets returned by
+ * nest_record_layout().  Units: flops, bytes, bytes per microsecond,
+ * nanoseconds, flop per nanosecond.
+ * Rules (else the instance gets NEST_BAD_INPUT):
+ *   1 <= L <= Lmax; unit a power of two; unit <= D <= 8192; D % unit == 0;
+ *   D / unit <= Dumax; 1 <= T <= Tmax; tier sizes G strictly increasing powers of
+ *   two with G[T-1] >= D; 1000 <= bw <= 2^40; 0 <= lat <= 2^24; 1 <= C <= Cmax;
+ *   candidate tiers strictly increasing in [0, T); 1 <= S <= Smax; t, cp, e powers
+ *   of two <= 8192; z in 0..3; r in 0..1; 1 <= Pmax <= Pcap; Pmax <= M <= 2^20;
+ *   1 <= R <= 2^40; 0 <= budget <= 2^62; 0 <= opt_factor <= 16; per layer
+ *   0 <= fl <= 2^48, 0 <= pd, pe, ao, aw, a2a <= 2^38, moe in {0, 1}.       */
+typedef struct {
+    int32_t L;          /* layers */
+    int32_t D;          /* devices */
+    int32_t unit;       /* device counts are unit * 2^m */
+    int32_t T;          /* tiers */
+    int32_t C;          /* candidate tiers for inter-stage links */
+    int32_t S;          /* strategies */
+    int32_t Pmax;       /* largest number of pipeline stages */
+    int32_t reserved;
+    int64_t R;          /* device compute rate, flop per ns */
+    int64_t M;          /* microbatches per iteration */
+    int64_t budget;     /* bytes per device */
+    int64_t opt_factor; /* optimizer-state bytes per bf16 weight byte */
+} nest_record_header;
+
+/* Byte offsets inside one record (from its start). */
+typedef struct {
+    int64_t record_bytes; /* stride between records (multiple of 256) */
+    int64_t fl, pd, pe, ao, aw, a2a; /* int64 [Lmax] each */
+    int64_t moe;                     /* uint8 [Lmax] */
+    int64_t G, bw, lat;              /* int64 [Tmax] each */
+    int64_t cand;                    /* int32 [Cmax] */
+    int64_t strat;                   /* int16 [Smax][8]: t, cp, e, z, r, 0, 0, 0 */
+} nest_layout;
+
+/* ---- output plan --------------------------------------------------------------
+ * B plan records back to back, each nest_plan_bytes() long: a nest_plan_header
+ * followed by Pcap nest_stage entries (n_stages of them used).               */
+typedef struct {
+    int16_t i, j;    /* the stage holds layers [i, j) */
+    int16_t s;       /* strategy index into the instance's strategy table */
+    int8_t c_next;   /* candidate of the link to the next stage, -1 for the last stage */
+    int8_t reserved;
+    int32_t k;       /* devices of the stage */
+} nest_stage;
+
+typedef struct {
+    int32_t status;     /* NEST_SOLVED .. NEST_TIMED_OUT */
+    int32_t n_stages;
+    int64_t t_batch;    /* iteration time in ns, -1 unless solved */
+    int64_t bottleneck; /* largest stage time per microbatch in ns, -1 unless solved */
+} nest_plan_header;
+
+/* ---- options -------------------------------------------------------------------
+ * Zero-initialised options (or a NULL pointer) select the defaults.            */
+typedef struct {
+    int32_t chunk;          /* instances per pass through the kernels; 0 = all, at most 65535 (the
+                               workspace must be sized for the same chunk) */
+    int32_t sweep_cluster;  /* CTAs per instance in the DP sweep: 0 = auto, or 1, 2, 4, 8 */
+    int32_t sweep_jsplit;   /* threads sharing one DP cell: 0 = auto, or 1, 2, 4, 8 */
+    int32_t reserved;
+    int64_t spin_limit;     /* polls before a device wait gives up: 0 = default (2^26);
+                               a negative value makes every wait give up at once, which
+                               exercises the timeout path (instances end NEST_TIMED_OUT) */
+    void **events;          /* optional cudaEvent_t[6 * chunks]; for chunk n, events
+                               [6n .. 6n+5] are recorded on the stream before prep, cost
+                               build, strategy reduction, DP sweep, backtrack, and after
+                               backtrack.  NULL = no events. */
+} nest_options;
+
+/* Fills *out with the record layout for dims.  Returns NEST_OK or NEST_E_LIMITS. */
+int nest_record_layout(const nest_dims *dims, nest_layout *out);
+
+/* Stride of one plan record in bytes (0 when dims break the limits). */
+size_t nest_plan_bytes(const nest_dims *dims);
+
+/* Device workspace bytes that nest_solve needs for passes of `chunk` instances
+ * (chunk <= 0 means dims->B).  0 when dims break the limits.  The workspace holds,
+ * per instance of a chunk, the stage-cost tensor cost[pair(i, j)][m][s] (8 bytes
+ * per word), the per-position strategy loads, and the DP value and argument tables. */
+size_t nest_workspace_size(const nest_dims *dims, int32_t chunk);
+
+/* Solve a batch on the GPU.
+ *   records    DEVICE, B instance records (layout above), read only
+ *   costs_out  DEVICE int64 [B]: t_batch per instance, -1 unless NEST_SOLVED
+ *   plans_out  DEVICE, B plan records of nest_plan_bytes() each
+ *   workspace  DEVICE, >= nest_workspace_size(dims, opt->chunk) bytes, 256-byte aligned;
+ *              contents on entry are ignored, on return undefined
+ *   stream     a cudaStream_t (NULL = legacy default stream)
+ * Instances are independent; a bad instance only sets its own status.  Returns
+ * NEST_OK once every kernel is enqueued; NEST_E_* (nothing enqueued) on bad
+ * arguments; NEST_E_CUDA if a launch fails. */
+int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, void *plans_out,
+               void *workspace, size_t ws_bytes, void *stream, const nest_options *opt);
+
+/* Device workspace bytes for nest_solve_host: nest_workspace_size plus room for
+ * the records and the results. */
+size_t nest_workspace_size_host(const nest_dims *dims, int32_t chunk);
+
+/* Solve a batch held in HOST memory: copies the records to the device workspace,
+ * solves, copies costs and plans back and synchronises the stream.
+ *   records_host, costs_host, plans_host   HOST buffers (pinned memory is faster)
+ *   workspace    DEVICE, >= nest_workspace_size_host(dims, opt->chunk) bytes
+ * Returns NEST_OK, NEST_E_TIMEOUT if some instance timed out, or NEST_E_*. */
+int nest_solve_host(const nest_dims *dims, const void *records_host, int64_t *costs_host,
+                    void *plans_host, void *workspace, size_t ws_bytes, void *stream,
+                    const nest_options *opt);
+
+/* Offsets (bytes from the workspace start) of the intermediate tables of the
+ * LAST chunk a nest_solve call processed, for inspection after the stream syncs:
+ *   cost  uint64 [chunk][NP][Kmax][Spad]  (tau << 8) | pmax, all ones = not applicable
+ *   loads uint64 [chunk][Pcap][NP][Kpad]  (tau* << 16) | s* per position p (index p-1)
+ *   dpv   int64  [chunk][Pcap][Lmax][Cmax][Dpad]  DP value per (p, i, c, d), 2^40-1 = none
+ *   dpa   uint32 [chunk][Pcap][Lmax][Cmax][Dpad]  (j << 8) | (m << 4) | c'
+ * where NP = Lmax (Lmax + 1) / 2 pairs (i, j) ordered by i then j, Kmax =
+ * floor(log2 Dumax) + 1, Kpad = Kmax rounded up to even, Spad = Smax rounded up
+ * to even, Dpad = Dumax + 1 rounded up to even. */
+typedef struct {
+    int64_t cost, loads, dpv, dpa, total;
+    int32_t NP, Kmax, Kpad, Spad, Dpad, chunk;
+} nest_ws_layout;
+int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NEST_H */

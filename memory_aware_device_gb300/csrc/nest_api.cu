@@ -1,0 +1,200 @@
+// C ABI of the placement-DP solver (declared in include/nest.h).
+//
+// A call validates the batch dimensions on the host, then, for each chunk of
+// instances, enqueues five kernels on the caller's stream: prep (validation,
+// prefix sums, link costs), cost build, strategy reduction, DP sweep and
+// backtrack.  Nothing is allocated and no state survives the call.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "nest_internal.cuh"
+
+using namespace nest;
+
+namespace {
+
+constexpr int64_t kSweepSmemBudget = 200 * 1024;
+
+struct Config {
+    int cluster, jsplit, jc, threads;
+};
+
+int pick_config(const Geo &g, int n, const nest_options *opt, Config &cfg) {
+    const int NTd = (g.Dumax + 31) / 32 * 32;
+    int jsplit = opt ? opt->sweep_jsplit : 0;
+    if (jsplit == 0) {
+        jsplit = 1;
+        while (jsplit < 8 && NTd * jsplit * 2 <= 512) jsplit *= 2;
+    }
+    if (jsplit != 1 && jsplit != 2 && jsplit != 4 && jsplit != 8) return NEST_E_INVALID;
+    if (NTd * jsplit > 1024) return NEST_E_LIMITS;
+    int cluster = opt ? opt->sweep_cluster : 0;
+    if (cluster == 0) {
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cluster = 1;
+        while (cluster < 8 && cluster * 2 <= g.Pcap && int64_t(n) * cluster * 2 <= sms) cluster *= 2;
+    }
+    if (cluster != 1 && cluster != 2 && cluster != 4 && cluster != 8) return NEST_E_INVALID;
+    int dev = 0, optin = 227 * 1024;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const int64_t budget = kSweepSmemBudget < optin - 1024 ? kSweepSmemBudget : optin - 1024;
+    const int threads = NTd * jsplit;
+    int jc = g.Lmax > 1 ? g.Lmax - 1 : 1;
+    while (jc > 1 && sweep_smem_bytes(g, jc, jsplit, threads) > budget) jc--;
+    if (sweep_smem_bytes(g, jc, jsplit, threads) > budget) return NEST_E_LIMITS;
+    cfg = {cluster, jsplit, jc, threads};
+    return NEST_OK;
+}
+
+// Instances per pass: the whole batch by default, at most 65535 (the cost and
+// reduction kernels index instances with blockIdx.y).
+int32_t chunk_of(const nest_dims *dims, int32_t chunk) {
+    if (chunk <= 0 || chunk > dims->B) chunk = dims->B;
+    return chunk < 65535 ? chunk : 65535;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nest_record_layout(const nest_dims *dims, nest_layout *out) {
+    Geo g;
+    if (!dims || !out) return NEST_E_INVALID;
+    if (!make_geo(*dims, g)) return NEST_E_LIMITS;
+    record_layout(g, *out);
+    return NEST_OK;
+}
+
+size_t nest_plan_bytes(const nest_dims *dims) {
+    Geo g;
+    if (!dims || !make_geo(*dims, g)) return 0;
+    return size_t(plan_bytes(g));
+}
+
+size_t nest_workspace_size(const nest_dims *dims, int32_t chunk) {
+    Geo g;
+    if (!dims || !make_geo(*dims, g)) return 0;
+    const int32_t ch = chunk_of(dims, chunk);
+    return size_t(ws_layout(g, ch < 1 ? 1 : ch).total);
+}
+
+int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out) {
+    Geo g;
+    if (!dims || !out) return NEST_E_INVALID;
+    if (!make_geo(*dims, g)) return NEST_E_LIMITS;
+    const int32_t ch = chunk_of(dims, chunk);
+    const WsLayout w = ws_layout(g, ch < 1 ? 1 : ch);
+    out->cost = w.cost;
+    out->loads = w.loads;
+    out->dpv = w.dpv;
+    out->dpa = w.dpa;
+    out->total = w.total;
+    out->NP = g.NP;
+    out->Kmax = g.Kmax;
+    out->Kpad = g.Kpad;
+    out->Spad = g.Spad;
+    out->Dpad = g.Dpad;
+    out->chunk = ch;
+    return NEST_OK;
+}
+
+int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, void *plans_out,
+               void *workspace, size_t ws_bytes, void *stream, const nest_options *opt) {
+    if (!dims) return NEST_E_INVALID;
+    Geo g;
+    if (dims->B < 0) return NEST_E_INVALID;
+    if (!make_geo(*dims, g)) return NEST_E_LIMITS;
+    if (dims->B == 0) return NEST_OK;
+    if (!records || !costs_out || !plans_out || !workspace) return NEST_E_INVALID;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 || reinterpret_cast<uintptr_t>(records) % 256)
+        return NEST_E_WORKSPACE;
+    const int32_t chunk = chunk_of(dims, opt ? opt->chunk : 0);
+    const WsLayout w = ws_layout(g, chunk);
+    if (ws_bytes < size_t(w.total)) return NEST_E_WORKSPACE;
+    Config cfg;
+    int rc = pick_config(g, chunk, opt, cfg);
+    if (rc != NEST_OK) return rc;
+
+    PassArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.g = g;
+    a.w = w;
+    a.pl = prep_layout(g);
+    record_layout(g, a.rl);
+    a.ws = static_cast<unsigned char *>(workspace);
+    a.plan_stride = plan_bytes(g);
+    a.cluster = cfg.cluster;
+    a.jsplit = cfg.jsplit;
+    a.jc = cfg.jc;
+    a.threads = cfg.threads;
+    a.spin_limit = opt ? opt->spin_limit : 0;
+    cudaEvent_t *ev = opt ? reinterpret_cast<cudaEvent_t *>(opt->events) : nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto mark = [&](int chunk_idx, int k) {
+        if (ev && cudaEventRecord(ev[6 * chunk_idx + k], st) != cudaSuccess) return NEST_E_CUDA;
+        return NEST_OK;
+    };
+    int ci = 0;
+    for (int32_t first = 0; first < dims->B; first += chunk, ci++) {
+        a.n = dims->B - first < chunk ? dims->B - first : chunk;
+        a.records = static_cast<const unsigned char *>(records) + int64_t(first) * a.rl.record_bytes;
+        a.costs_out = costs_out + first;
+        a.plans_out = static_cast<unsigned char *>(plans_out) + int64_t(first) * a.plan_stride;
+        if ((rc = mark(ci, 0)) || (rc = launch_prep(a, st)) || (rc = mark(ci, 1)) || (rc = launch_cost(a, st)) ||
+            (rc = mark(ci, 2)) || (rc = launch_reduce(a, st)) || (rc = mark(ci, 3)) ||
+            (rc = launch_sweep(a, st)) || (rc = mark(ci, 4)) || (rc = launch_backtrack(a, st)) ||
+            (rc = mark(ci, 5)))
+            return rc;
+    }
+    return NEST_OK;
+}
+
+size_t nest_workspace_size_host(const nest_dims *dims, int32_t chunk) {
+    Geo g;
+    if (!dims || !make_geo(*dims, g)) return 0;
+    nest_layout rl;
+    record_layout(g, rl);
+    const int64_t B = dims->B;
+    return size_t(align_up(B * rl.record_bytes, 256) + align_up(8 * B, 256) + align_up(B * plan_bytes(g), 256) +
+                  int64_t(nest_workspace_size(dims, chunk)));
+}
+
+int nest_solve_host(const nest_dims *dims, const void *records_host, int64_t *costs_host, void *plans_host,
+                    void *workspace, size_t ws_bytes, void *stream, const nest_options *opt) {
+    if (!dims) return NEST_E_INVALID;
+    Geo g;
+    if (dims->B < 0) return NEST_E_INVALID;
+    if (!make_geo(*dims, g)) return NEST_E_LIMITS;
+    if (dims->B == 0) return NEST_OK;
+    if (!records_host || !costs_host || !plans_host || !workspace) return NEST_E_INVALID;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return NEST_E_WORKSPACE;
+    if (ws_bytes < nest_workspace_size_host(dims, opt ? opt->chunk : 0)) return NEST_E_WORKSPACE;
+    nest_layout rl;
+    record_layout(g, rl);
+    const int64_t B = dims->B;
+    unsigned char *base = static_cast<unsigned char *>(workspace);
+    unsigned char *rec_d = base;
+    int64_t *costs_d = reinterpret_cast<int64_t *>(base + align_up(B * rl.record_bytes, 256));
+    unsigned char *plans_d = reinterpret_cast<unsigned char *>(costs_d) + align_up(8 * B, 256);
+    unsigned char *ws = plans_d + align_up(B * plan_bytes(g), 256);
+    const size_t ws_left = ws_bytes - size_t(ws - base);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(rec_d, records_host, size_t(B * rl.record_bytes), cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return NEST_E_CUDA;
+    int rc = nest_solve(dims, rec_d, costs_d, plans_d, ws, ws_left, stream, opt);
+    if (rc != NEST_OK) return rc;
+    if (cudaMemcpyAsync(costs_host, costs_d, size_t(8 * B), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(plans_host, plans_d, size_t(B * plan_bytes(g)), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return NEST_E_CUDA;
+    const unsigned char *ph = static_cast<const unsigned char *>(plans_host);
+    for (int64_t b = 0; b < B; b++)
+        if (reinterpret_cast<const nest_plan_header *>(ph + b * plan_bytes(g))->status == NEST_TIMED_OUT)
+            return NEST_E_TIMEOUT;
+    return NEST_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// Internal layouts and helpers of the GB300 placement-DP solver.
+//
+// Method: "Nest: Network- and Memory-Aware Device Placement for Distributed Deep
+// Learning" (Nest), §3.3 memory model, §4 Eq. 3 and load(), Appendix K Algorithm 1.
+// The public ABI is include/nest.h; everything here is private to the library.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/nest.h"
+
+namespace nest {
+
+constexpr int64_t kCap = (int64_t(1) << 40) - 1;   // stage times >= kCap are infeasible
+constexpr uint64_t kInf = ~uint64_t(0);             // "no value" word / key
+constexpr uint32_t kNoArg = 0xFFFFFFu;              // argument field of an empty DP cell
+constexpr int kLogL = 8;                            // sparse-table levels: 2^8 > 255 layers
+
+__host__ __device__ inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// Batch geometry derived from nest_dims.
+struct Geo {
+    int32_t B, Lmax, Tmax, Cmax, Smax, Pcap, Dumax;
+    int32_t NP;    // pairs (i, j), 0 <= i < j <= Lmax
+    int32_t Kmax;  // widths unit * 2^m, m < Kmax
+    int32_t Kpad;  // Kmax rounded up to even (16-byte rows)
+    int32_t Spad;  // Smax rounded up to even
+    int32_t Dpad;  // Dumax + 1 rounded up to even
+};
+
+inline bool make_geo(const nest_dims &d, Geo &g) {
+    if (d.B < 0 || d.Lmax < 1 || d.Lmax > 255 || d.Tmax < 1 || d.Tmax > 8 || d.Cmax < 1 ||
+        d.Cmax > 15 || d.Smax < 1 || d.Smax > 4095 || d.Pcap < 1 || d.Pcap > 31 || d.Dumax < 1 ||
+        d.Dumax > 1024 || int64_t(d.Cmax) * (d.Dumax + 2) > 8192)
+        return false;
+    g.B = d.B;
+    g.Lmax = d.Lmax;
+    g.Tmax = d.Tmax;
+    g.Cmax = d.Cmax;
+    g.Smax = d.Smax;
+    g.Pcap = d.Pcap;
+    g.Dumax = d.Dumax;
+    g.NP = d.Lmax * (d.Lmax + 1) / 2;
+    int K = 0;
+    while ((1 << K) <= d.Dumax) K++;
+    g.Kmax = K;
+    g.Kpad = (K + 1) & ~1;
+    g.Spad = (d.Smax + 1) & ~1;
+    g.Dpad = (d.Dumax + 2) & ~1;
+    return true;
+}
+
+// Offsets inside one instance record (public layout, see nest.h).
+inline void record_layout(const Geo &g, nest_layout &o) {
+    int64_t off = sizeof(nest_record_header);
+    auto take = [&](int64_t bytes) {
+        int64_t at = off;
+        off = align_up(off + bytes, 16);
+        return at;
+    };
+    o.fl = take(8 * g.Lmax);
+    o.pd = take(8 * g.Lmax);
+    o.pe = take(8 * g.Lmax);
+    o.ao = take(8 * g.Lmax);
+    o.aw = take(8 * g.Lmax);
+    o.a2a = take(8 * g.Lmax);
+    o.moe = take(g.Lmax);
+    o.G = take(8 * g.Tmax);
+    o.bw = take(8 * g.Tmax);
+    o.lat = take(8 * g.Tmax);
+    o.cand = take(4 * g.Cmax);
+    o.strat = take(16 * g.Smax);
+    o.record_bytes = align_up(off, 256);
+}
+
+// Per-instance preparation record written by the prep kernel.
+struct PrepHdr {
+    int32_t status;  // NEST_SOLVED (0) when the instance is valid, NEST_BAD_INPUT otherwise;
+                     // the sweep raises it to NEST_TIMED_OUT when a wait gives up
+    int32_t L, D, unit, lu, Du, K, T, C, S, P, pad0;
+    int64_t R, M, budget, opt;
+    int64_t G[8], bw[8], lat[8];
+    int32_t cand[16];
+    int32_t mlim[16];  // largest m with 2 * unit * 2^m <= G[cand c], -1 if none
+    int64_t pad1[2];
+};
+static_assert(sizeof(PrepHdr) % 16 == 0, "PrepHdr alignment");
+
+enum { kFl = 0, kPd, kPe, kAo, kAw, kA2, kNm, kNumPfx };
+
+struct PrepLayout {
+    int64_t pfx;    // int64 [kNumPfx][Lmax + 1] prefix sums
+    int64_t ao;     // int64 [Lmax] raw output activation bytes
+    int64_t awst;   // int64 [kLogL][Lmax] sparse table of max(aw)
+    int64_t X;      // int64 [Lmax + 1][Cmax] link cost per boundary and candidate
+    int64_t strat;  // uint32 [Smax] packed log2 t | log2 cp << 4 | log2 e << 8 | z << 12 | r << 14
+    int64_t bytes;
+};
+
+__host__ __device__ inline PrepLayout prep_layout(const Geo &g) {
+    PrepLayout p;
+    int64_t off = sizeof(PrepHdr);
+    p.pfx = off;
+    off += 8 * int64_t(kNumPfx) * (g.Lmax + 1);
+    p.ao = off;
+    off += 8 * int64_t(g.Lmax);
+    p.awst = off;
+    off += 8 * int64_t(kLogL) * g.Lmax;
+    p.X = off;
+    off += 8 * int64_t(g.Lmax + 1) * g.Cmax;
+    p.strat = off;
+    off += 4 * int64_t(g.Smax);
+    p.bytes = align_up(off, 256);
+    return p;
+}
+
+// Workspace regions for passes of `ch` instances.
+struct WsLayout {
+    int64_t prep, cost, loads, dpv, dpa, total;
+    int64_t prep_stride, cost_stride, loads_stride, dp_stride;  // per instance (elements for tables)
+};
+
+__host__ __device__ inline WsLayout ws_layout(const Geo &g, int64_t ch) {
+    WsLayout w;
+    PrepLayout p = prep_layout(g);
+    w.prep_stride = p.bytes;
+    w.cost_stride = int64_t(g.NP) * g.Kmax * g.Spad;            // uint64 words
+    w.loads_stride = int64_t(g.Pcap) * g.NP * g.Kpad;           // uint64 words
+    w.dp_stride = int64_t(g.Pcap) * g.Lmax * g.Cmax * g.Dpad;   // cells
+    int64_t off = 0;
+    w.prep = off;
+    off = align_up(off + ch * w.prep_stride, 256);
+    w.cost = off;
+    off = align_up(off + ch * w.cost_stride * 8, 256);
+    w.loads = off;
+    off = align_up(off + ch * w.loads_stride * 8, 256);
+    w.dpv = off;
+    off = align_up(off + ch * w.dp_stride * 8, 256);
+    w.dpa = off;
+    off = align_up(off + ch * w.dp_stride * 4, 256);
+    w.total = off;
+    return w;
+}
+
+__host__ __device__ inline int64_t plan_bytes(const Geo &g) {
+    return align_up(int64_t(sizeof(nest_plan_header)) + int64_t(sizeof(nest_stage)) * g.Pcap, 8);
+}
+
+// Row offset of pair (i, i+1) among the pairs of an L-layer chain.
+__host__ __device__ inline int64_t row_offset(int i, int L) {
+    return int64_t(i) * L - int64_t(i) * (i - 1) / 2;
+}
+
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Arguments shared by the kernels of one pass.
+struct PassArgs {
+    Geo g;
+    WsLayout w;
+    PrepLayout pl;
+    nest_layout rl;
+    const unsigned char *records;  // device, first instance of the pass
+    unsigned char *ws;             // device workspace base
+    int64_t *costs_out;            // device, first instance of the pass
+    unsigned char *plans_out;      // device, first plan of the pass
+    int64_t plan_stride;
+    int32_t n;                     // instances in this pass
+    int32_t cluster;               // sweep CTAs per instance
+    int32_t jsplit;                // sweep threads per DP cell
+    int32_t jc;                    // sweep j-chunk (layers staged per tile)
+    int32_t threads;               // sweep threads per CTA
+    int64_t spin_limit;            // polls per bounded wait (negative: give up at once)
+};
+
+__host__ __device__ inline PrepHdr *prep_hdr(const PassArgs &a, int b) {
+    return reinterpret_cast<PrepHdr *>(a.ws + a.w.prep + int64_t(b) * a.w.prep_stride);
+}
+
+// Launchers (one translation unit each).
+int launch_prep(const PassArgs &a, void *stream);
+int launch_cost(const PassArgs &a, void *stream);
+int launch_reduce(const PassArgs &a, void *stream);
+int launch_sweep(const PassArgs &a, void *stream);
+int launch_backtrack(const PassArgs &a, void *stream);
+// Dynamic shared memory of the sweep for a given configuration (0 if it cannot fit).
+int64_t sweep_smem_bytes(const Geo &g, int jc, int jsplit, int threads);
+
+}  // namespace nest

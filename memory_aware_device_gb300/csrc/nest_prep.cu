@@ -1,0 +1,185 @@
+// Prep kernel: validates each instance and derives the per-instance tables the
+// cost builder and the DP sweep read.
+//
+// Nest (Network- and Memory-Aware Device Placement) §3.2: the solver receives the
+// operator chain annotated with per-layer compute, parameter and activation sizes
+// plus the tiered network description (Appendix B).  This kernel turns those
+// inputs into prefix sums over layers (stage sums in O(1)), a sparse table for
+// the largest working activation of a stage, the link cost of every layer
+// boundary over every candidate tier (the forward / backward traffic terms of
+// §4 load()), and packed strategy codes.  One CTA per instance.
+#include <cuda_runtime.h>
+
+#include "nest_internal.cuh"
+
+namespace nest {
+
+namespace {
+
+__device__ __forceinline__ bool pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+__device__ __forceinline__ int ilog2(int64_t v) { return 63 - __clzll(v); }
+
+__global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
+    const int b = blockIdx.x;
+    const unsigned char *rec = a.records + int64_t(b) * a.rl.record_bytes;
+    const nest_record_header h = *reinterpret_cast<const nest_record_header *>(rec);
+    PrepHdr *ph = prep_hdr(a, b);
+    unsigned char *pb = reinterpret_cast<unsigned char *>(ph);
+    const Geo &g = a.g;
+    __shared__ int bad;
+    if (threadIdx.x == 0) {
+        int bd = 0;
+        bd |= h.L < 1 || h.L > g.Lmax;
+        bd |= !pow2(h.unit) || h.D < h.unit || h.D > 8192 || (h.unit > 0 && h.D % h.unit);
+        bd |= h.unit > 0 && h.D / h.unit > g.Dumax;
+        bd |= h.T < 1 || h.T > g.Tmax;
+        bd |= h.C < 1 || h.C > g.Cmax;
+        bd |= h.S < 1 || h.S > g.Smax;
+        bd |= h.Pmax < 1 || h.Pmax > g.Pcap;
+        bd |= h.M < h.Pmax || h.M > (int64_t(1) << 20);
+        bd |= h.R < 1 || h.R > (int64_t(1) << 40);
+        bd |= h.budget < 0 || h.budget > (int64_t(1) << 62);
+        bd |= h.opt_factor < 0 || h.opt_factor > 16;
+        bad = bd;
+    }
+    __syncthreads();
+    if (!bad) {
+        const int64_t *G = reinterpret_cast<const int64_t *>(rec + a.rl.G);
+        const int64_t *bw = reinterpret_cast<const int64_t *>(rec + a.rl.bw);
+        const int64_t *lat = reinterpret_cast<const int64_t *>(rec + a.rl.lat);
+        const int32_t *cand = reinterpret_cast<const int32_t *>(rec + a.rl.cand);
+        const int16_t *st = reinterpret_cast<const int16_t *>(rec + a.rl.strat);
+        int bd = 0;
+        for (int l = threadIdx.x; l < h.L; l += blockDim.x) {
+            const int64_t *arr[5] = {
+                reinterpret_cast<const int64_t *>(rec + a.rl.pd), reinterpret_cast<const int64_t *>(rec + a.rl.pe),
+                reinterpret_cast<const int64_t *>(rec + a.rl.ao), reinterpret_cast<const int64_t *>(rec + a.rl.aw),
+                reinterpret_cast<const int64_t *>(rec + a.rl.a2a)};
+            const int64_t f = reinterpret_cast<const int64_t *>(rec + a.rl.fl)[l];
+            bd |= f < 0 || f > (int64_t(1) << 48);
+            for (int q = 0; q < 5; q++) bd |= arr[q][l] < 0 || arr[q][l] > (int64_t(1) << 38);
+            bd |= rec[a.rl.moe + l] > 1;
+        }
+        for (int t = threadIdx.x; t < h.T; t += blockDim.x) {
+            bd |= !pow2(G[t]) || (t > 0 && G[t] <= G[t - 1]);
+            bd |= bw[t] < 1000 || bw[t] > (int64_t(1) << 40);
+            bd |= lat[t] < 0 || lat[t] > (int64_t(1) << 24);
+        }
+        if (threadIdx.x == 0) bd |= G[h.T - 1] < h.D;
+        for (int c = threadIdx.x; c < h.C; c += blockDim.x) {
+            bd |= cand[c] < 0 || cand[c] >= h.T || (c > 0 && cand[c] <= cand[c - 1]);
+        }
+        for (int s = threadIdx.x; s < h.S; s += blockDim.x) {
+            const int16_t *x = st + 8 * s;
+            for (int f = 0; f < 3; f++) bd |= !pow2(x[f]) || x[f] > 8192;
+            bd |= x[3] < 0 || x[3] > 3 || x[4] < 0 || x[4] > 1;
+        }
+        bd = __syncthreads_or(bd);
+        if (threadIdx.x == 0) bad = bd;
+        __syncthreads();
+    }
+    if (bad) {
+        if (threadIdx.x == 0) ph->status = NEST_BAD_INPUT;
+        return;
+    }
+
+    const int L = h.L;
+    const int64_t Du = h.D / h.unit;
+    if (threadIdx.x == 0) {
+        ph->L = L;
+        ph->D = h.D;
+        ph->unit = h.unit;
+        ph->lu = ilog2(h.unit);
+        ph->Du = int32_t(Du);
+        ph->K = ilog2(Du) + 1;
+        ph->T = h.T;
+        ph->C = h.C;
+        ph->S = h.S;
+        ph->P = h.Pmax;
+        ph->R = h.R;
+        ph->M = h.M;
+        ph->budget = h.budget;
+        ph->opt = h.opt_factor;
+    }
+    const int64_t *G = reinterpret_cast<const int64_t *>(rec + a.rl.G);
+    const int64_t *bw = reinterpret_cast<const int64_t *>(rec + a.rl.bw);
+    const int64_t *lat = reinterpret_cast<const int64_t *>(rec + a.rl.lat);
+    const int32_t *cand = reinterpret_cast<const int32_t *>(rec + a.rl.cand);
+    for (int t = threadIdx.x; t < 8; t += blockDim.x) {
+        ph->G[t] = t < h.T ? G[t] : 0;
+        ph->bw[t] = t < h.T ? bw[t] : 1;
+        ph->lat[t] = t < h.T ? lat[t] : 0;
+    }
+    for (int c = threadIdx.x; c < 16; c += blockDim.x) {
+        int ml = -1;
+        if (c < h.C) {
+            const int64_t cap = G[cand[c]];
+            for (int m = 0; m < 16; m++)
+                if (2 * (int64_t(h.unit) << m) <= cap) ml = m;
+        }
+        ph->cand[c] = c < h.C ? cand[c] : 0;
+        ph->mlim[c] = ml;
+    }
+
+    // prefix sums: one thread per array (L <= 255)
+    int64_t *pfx = reinterpret_cast<int64_t *>(pb + a.pl.pfx);
+    if (threadIdx.x < kNumPfx) {
+        const int q = threadIdx.x;
+        int64_t *out = pfx + int64_t(q) * (g.Lmax + 1);
+        int64_t acc = 0;
+        out[0] = 0;
+        if (q == kNm) {
+            for (int l = 0; l < L; l++) out[l + 1] = acc += rec[a.rl.moe + l];
+        } else {
+            const int64_t off[6] = {a.rl.fl, a.rl.pd, a.rl.pe, a.rl.ao, a.rl.aw, a.rl.a2a};
+            const int64_t *src = reinterpret_cast<const int64_t *>(rec + off[q]);
+            for (int l = 0; l < L; l++) out[l + 1] = acc += src[l];
+        }
+    }
+    // raw activations, sparse table of max(aw), link costs, packed strategies
+    int64_t *ao = reinterpret_cast<int64_t *>(pb + a.pl.ao);
+    int64_t *awst = reinterpret_cast<int64_t *>(pb + a.pl.awst);
+    const int64_t *aw_in = reinterpret_cast<const int64_t *>(rec + a.rl.aw);
+    const int64_t *ao_in = reinterpret_cast<const int64_t *>(rec + a.rl.ao);
+    for (int l = threadIdx.x; l < L; l += blockDim.x) {
+        ao[l] = ao_in[l];
+        awst[l] = aw_in[l];
+    }
+    __syncthreads();
+    for (int lv = 1; lv < kLogL; lv++) {
+        const int span = 1 << (lv - 1);
+        for (int l = threadIdx.x; l < L; l += blockDim.x) {
+            const int64_t x = awst[int64_t(lv - 1) * g.Lmax + l];
+            const int64_t y = l + span < L ? awst[int64_t(lv - 1) * g.Lmax + l + span] : x;
+            awst[int64_t(lv) * g.Lmax + l] = x > y ? x : y;
+        }
+        __syncthreads();
+    }
+    int64_t *X = reinterpret_cast<int64_t *>(pb + a.pl.X);
+    for (int e = threadIdx.x; e < (L + 1) * h.C; e += blockDim.x) {
+        const int bnd = e / h.C, c = e % h.C;
+        int64_t v = 0;
+        if (bnd > 0 && bnd < L) {
+            const int tr = cand[c];
+            v = lat[tr] + cdiv(ao_in[bnd - 1] * 1000, bw[tr]);
+        }
+        X[int64_t(bnd) * g.Cmax + c] = v;
+    }
+    uint32_t *sp = reinterpret_cast<uint32_t *>(pb + a.pl.strat);
+    const int16_t *st = reinterpret_cast<const int16_t *>(rec + a.rl.strat);
+    for (int s = threadIdx.x; s < h.S; s += blockDim.x) {
+        const int16_t *x = st + 8 * s;
+        sp[s] = uint32_t(ilog2(x[0])) | uint32_t(ilog2(x[1])) << 4 | uint32_t(ilog2(x[2])) << 8 |
+                uint32_t(x[3]) << 12 | uint32_t(x[4]) << 14;
+    }
+    if (threadIdx.x == 0) ph->status = NEST_SOLVED;
+}
+
+}  // namespace
+
+int launch_prep(const PassArgs &a, void *stream) {
+    prep_kernel<<<a.n, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return cudaGetLastError() == cudaSuccess ? NEST_OK : NEST_E_CUDA;
+}
+
+}  // namespace nest

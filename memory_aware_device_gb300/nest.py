@@ -1,0 +1,247 @@
+"""Python binding of libnest (include/nest.h): argument marshalling only.
+
+Every step of the solve runs in the library's CUDA kernels; this module packs
+instances into the record layout the library reports, passes device pointers
+and a stream, and decodes the plan records.  PyTorch supplies device memory and
+streams.  There is no CPU fallback: if libnest.so is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import List, Sequence
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libnest.so")
+
+NEST_OK, NEST_E_INVALID, NEST_E_LIMITS, NEST_E_WORKSPACE, NEST_E_CUDA, NEST_E_TIMEOUT = 0, -1, -2, -3, -4, -5
+SOLVED, INFEASIBLE, BAD_INPUT, TIMED_OUT = 0, 1, 2, 3
+CAP = (1 << 40) - 1
+ERRORS = {NEST_E_INVALID: "invalid argument", NEST_E_LIMITS: "batch dimensions beyond the limits",
+          NEST_E_WORKSPACE: "workspace too small or misaligned", NEST_E_CUDA: "CUDA call failed",
+          NEST_E_TIMEOUT: "a device wait gave up"}
+
+# Every function declared in include/nest.h.
+EXPORTS = ("nest_record_layout", "nest_plan_bytes", "nest_workspace_size", "nest_workspace_layout",
+           "nest_solve", "nest_workspace_size_host", "nest_solve_host")
+
+
+class NestError(RuntimeError):
+    def __init__(self, rc: int, what: str = "nest_solve"):
+        super().__init__(f"{what} returned {rc}: {ERRORS.get(rc, 'unknown error')}")
+        self.rc = rc
+
+
+class Dims(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("B", "Lmax", "Tmax", "Cmax", "Smax", "Pcap", "Dumax", "reserved")]
+
+
+class Layout(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("record_bytes", "fl", "pd", "pe", "ao", "aw", "a2a", "moe",
+                                         "G", "bw", "lat", "cand", "strat")]
+
+
+class WsLayout(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("cost", "loads", "dpv", "dpa", "total")] + \
+               [(n, C.c_int32) for n in ("NP", "Kmax", "Kpad", "Spad", "Dpad", "chunk")]
+
+
+class Options(C.Structure):
+    _fields_ = [("chunk", C.c_int32), ("sweep_cluster", C.c_int32), ("sweep_jsplit", C.c_int32),
+                ("reserved", C.c_int32), ("spin_limit", C.c_int64), ("events", C.c_void_p)]
+
+
+HEADER_DT = np.dtype([("L", "<i4"), ("D", "<i4"), ("unit", "<i4"), ("T", "<i4"), ("C", "<i4"),
+                      ("S", "<i4"), ("Pmax", "<i4"), ("reserved", "<i4"), ("R", "<i8"), ("M", "<i8"),
+                      ("budget", "<i8"), ("opt_factor", "<i8")])
+PLAN_HDR_DT = np.dtype([("status", "<i4"), ("n_stages", "<i4"), ("t_batch", "<i8"), ("bottleneck", "<i8")])
+STAGE_DT = np.dtype([("i", "<i2"), ("j", "<i2"), ("s", "<i2"), ("c_next", "i1"), ("reserved", "i1"),
+                     ("k", "<i4")])
+
+_lib = None
+
+
+def lib():
+    """Load libnest.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(the solver has no CPU fallback)")
+        L = C.CDLL(LIB_PATH)
+        P = C.POINTER
+        L.nest_record_layout.argtypes = [P(Dims), P(Layout)]
+        L.nest_plan_bytes.argtypes = [P(Dims)]
+        L.nest_plan_bytes.restype = C.c_size_t
+        L.nest_workspace_size.argtypes = [P(Dims), C.c_int32]
+        L.nest_workspace_size.restype = C.c_size_t
+        L.nest_workspace_size_host.argtypes = [P(Dims), C.c_int32]
+        L.nest_workspace_size_host.restype = C.c_size_t
+        L.nest_workspace_layout.argtypes = [P(Dims), C.c_int32, P(WsLayout)]
+        L.nest_solve.argtypes = [P(Dims), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
+                                 C.c_void_p, P(Options)]
+        L.nest_solve_host.argtypes = [P(Dims), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
+                                      C.c_void_p, P(Options)]
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------------
+# Geometry and packing
+# ---------------------------------------------------------------------------------
+
+def make_dims(instances: Sequence, Pcap: int | None = None, Dumax: int | None = None) -> Dims:
+    return Dims(B=len(instances), Lmax=max(int(x.L) for x in instances),
+                Tmax=max(len(x.tierG) for x in instances), Cmax=max(len(x.cand) for x in instances),
+                Smax=max(len(x.strat) for x in instances),
+                Pcap=Pcap or max(int(x.Pmax) for x in instances),
+                Dumax=Dumax or max(int(x.D) // int(x.unit) for x in instances), reserved=0)
+
+
+def record_layout(dims: Dims) -> Layout:
+    out = Layout()
+    rc = lib().nest_record_layout(C.byref(dims), C.byref(out))
+    if rc:
+        raise NestError(rc, "nest_record_layout")
+    return out
+
+
+def plan_bytes(dims: Dims) -> int:
+    return int(lib().nest_plan_bytes(C.byref(dims)))
+
+
+def workspace_size(dims: Dims, chunk: int = 0, host: bool = False) -> int:
+    f = lib().nest_workspace_size_host if host else lib().nest_workspace_size
+    return int(f(C.byref(dims), chunk))
+
+
+def workspace_layout(dims: Dims, chunk: int = 0) -> WsLayout:
+    out = WsLayout()
+    rc = lib().nest_workspace_layout(C.byref(dims), chunk, C.byref(out))
+    if rc:
+        raise NestError(rc, "nest_workspace_layout")
+    return out
+
+
+def pack_records(instances: Sequence, dims: Dims, out: np.ndarray | None = None) -> np.ndarray:
+    """Instance records in the library's layout: uint8 [B, record_bytes]."""
+    lay = record_layout(dims)
+    rb = lay.record_bytes
+    buf = out if out is not None else np.zeros((len(instances), rb), dtype=np.uint8)
+    buf[...] = 0
+    for b, x in enumerate(instances):
+        row = buf[b]
+        h = np.zeros(1, HEADER_DT)
+        h["L"], h["D"], h["unit"], h["T"], h["C"], h["S"], h["Pmax"] = (
+            x.L, x.D, x.unit, len(x.tierG), len(x.cand), len(x.strat), x.Pmax)
+        h["R"], h["M"], h["budget"], h["opt_factor"] = x.R, x.M, x.budget, x.opt_factor
+        row[:HEADER_DT.itemsize] = h.view(np.uint8)
+
+        def put(off, arr, dt):
+            a = np.ascontiguousarray(np.asarray(arr, dtype=dt)).view(np.uint8).ravel()
+            row[off:off + a.size] = a
+        for f in ("fl", "pd", "pe", "ao", "aw", "a2a"):
+            put(getattr(lay, f), getattr(x, f), "<i8")
+        put(lay.moe, x.moe, np.uint8)
+        put(lay.G, x.tierG, "<i8")
+        put(lay.bw, x.tierBw, "<i8")
+        put(lay.lat, x.tierLat, "<i8")
+        put(lay.cand, x.cand, "<i4")
+        st = np.zeros((len(x.strat), 8), dtype="<i2")
+        st[:, :5] = np.asarray(x.strat, dtype=np.int16).reshape(-1, 5)
+        put(lay.strat, st, "<i2")
+    return buf
+
+
+def decode_plans(raw: np.ndarray, dims: Dims) -> List[dict]:
+    """Plan records -> [{status, t_batch, bottleneck, plan: [(i, j, k, s, c_next)]}]."""
+    pb = plan_bytes(dims)
+    raw = np.ascontiguousarray(raw).view(np.uint8).reshape(dims.B, pb)
+    out = []
+    for b in range(dims.B):
+        h = raw[b, :PLAN_HDR_DT.itemsize].view(PLAN_HDR_DT)[0]
+        n = int(h["n_stages"])
+        st = raw[b, PLAN_HDR_DT.itemsize:PLAN_HDR_DT.itemsize + n * STAGE_DT.itemsize].view(STAGE_DT)
+        out.append({"status": int(h["status"]), "t_batch": int(h["t_batch"]),
+                    "bottleneck": int(h["bottleneck"]),
+                    "plan": [(int(s["i"]), int(s["j"]), int(s["k"]), int(s["s"]), int(s["c_next"]))
+                             for s in st]})
+    return out
+
+
+def options(chunk=0, cluster=0, jsplit=0, spin_limit=0, events=None) -> Options:
+    o = Options(chunk=chunk, sweep_cluster=cluster, sweep_jsplit=jsplit, reserved=0, spin_limit=spin_limit,
+                events=None)
+    if events is not None:
+        arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+        o._events_keep = arr
+        o.events = C.cast(arr, C.c_void_p)
+    return o
+
+
+# ---------------------------------------------------------------------------------
+# Calls
+# ---------------------------------------------------------------------------------
+
+def solve_raw(dims: Dims, records, costs, plans, workspace, stream=None, opt: Options | None = None) -> int:
+    """nest_solve on torch CUDA tensors (uint8 records/plans/workspace, int64 costs)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return lib().nest_solve(C.byref(dims), records.data_ptr(), costs.data_ptr(), plans.data_ptr(),
+                            workspace.data_ptr(), workspace.numel(), C.c_void_p(stream.cuda_stream),
+                            C.byref(opt) if opt is not None else None)
+
+
+def solve_host_raw(dims: Dims, records_host: np.ndarray, costs_host: np.ndarray, plans_host: np.ndarray,
+                   workspace, stream=None, opt: Options | None = None) -> int:
+    """nest_solve_host: HOST records in, HOST costs and plans out (synchronous)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return lib().nest_solve_host(C.byref(dims), records_host.ctypes.data, costs_host.ctypes.data,
+                                 plans_host.ctypes.data, workspace.data_ptr(), workspace.numel(),
+                                 C.c_void_p(stream.cuda_stream), C.byref(opt) if opt is not None else None)
+
+
+class Solver:
+    """Owns device buffers (via torch) for repeated solves of batches with fixed dims."""
+
+    def __init__(self, dims: Dims, chunk: int = 0, device="cuda", host_io: bool = False):
+        import torch
+        self.dims = dims
+        self.chunk = chunk
+        self.device = torch.device(device)
+        self.layout = record_layout(dims)
+        self.pb = plan_bytes(dims)
+        B = dims.B
+        self.records = torch.empty(B * self.layout.record_bytes, dtype=torch.uint8, device=self.device)
+        self.costs = torch.empty(B, dtype=torch.int64, device=self.device)
+        self.plans = torch.empty(B * self.pb, dtype=torch.uint8, device=self.device)
+        ws = workspace_size(dims, chunk, host=host_io)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device)
+
+    def load(self, records_np: np.ndarray):
+        import torch
+        self.records.copy_(torch.from_numpy(np.ascontiguousarray(records_np).ravel()))
+
+    def run(self, stream=None, opt: Options | None = None):
+        rc = solve_raw(self.dims, self.records, self.costs, self.plans, self.workspace, stream, opt)
+        if rc:
+            raise NestError(rc)
+
+    def results(self) -> List[dict]:
+        return decode_plans(self.plans.cpu().numpy(), self.dims)
+
+
+def solve_instances(instances: Sequence, device="cuda", **opt_kw) -> List[dict]:
+    """Convenience: pack, solve on the GPU, decode."""
+    import torch
+    dims = make_dims(instances)
+    s = Solver(dims, chunk=opt_kw.get("chunk", 0), device=device)
+    s.load(pack_records(instances, dims))
+    s.run(opt=options(**opt_kw))
+    torch.cuda.synchronize(s.device)
+    return s.results()

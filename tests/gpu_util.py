@@ -1,0 +1,80 @@
+"""Helpers for GPU parity tests: run the CUDA path and read its intermediate tables."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from memory_aware_device_gb300 import build as nbuild
+from memory_aware_device_gb300 import nest
+from oracle import oracle as O
+
+U64 = np.uint64
+
+
+def ensure_built():
+    nbuild.build()
+    O.build()
+
+
+def run(instances, chunk=0, cluster=0, jsplit=0, spin_limit=0, Pcap=None, Dumax=None):
+    """Solve on cuda:0; returns (solver, results)."""
+    import torch
+    dims = nest.make_dims(instances, Pcap=Pcap, Dumax=Dumax)
+    s = nest.Solver(dims, chunk=chunk)
+    s.load(nest.pack_records(instances, dims))
+    s.run(opt=nest.options(chunk=chunk, cluster=cluster, jsplit=jsplit, spin_limit=spin_limit))
+    torch.cuda.synchronize()
+    return s, s.results()
+
+
+def _slice(ws, off, count, dtype):
+    b = np.dtype(dtype).itemsize
+    return ws[off:off + count * b].cpu().numpy().view(dtype)
+
+
+def cost_table(s, b, inst):
+    lay = nest.workspace_layout(s.dims, s.chunk)
+    per = lay.NP * lay.Kmax * lay.Spad
+    t = _slice(s.workspace, lay.cost + 8 * per * b, per, U64).reshape(lay.NP, lay.Kmax, lay.Spad)
+    K = (inst.D // inst.unit).bit_length()
+    npi = inst.L * (inst.L + 1) // 2
+    return t[:npi, :K, :len(inst.strat)]
+
+
+def loads_table(s, b, inst):
+    lay = nest.workspace_layout(s.dims, s.chunk)
+    per = s.dims.Pcap * lay.NP * lay.Kpad
+    t = _slice(s.workspace, lay.loads + 8 * per * b, per, U64).reshape(s.dims.Pcap, lay.NP, lay.Kpad)
+    K = (inst.D // inst.unit).bit_length()
+    npi = inst.L * (inst.L + 1) // 2
+    return np.transpose(t[:inst.Pmax, :npi, :K], (1, 2, 0))   # [pair][m][p-1] like the oracle
+
+
+def dp_keys(s, b, inst):
+    """GPU DP table as packed keys in the oracle's [i][d][p][c] order (p >= 1, i < L)."""
+    lay = nest.workspace_layout(s.dims, s.chunk)
+    shape = (s.dims.Pcap, s.dims.Lmax, s.dims.Cmax, lay.Dpad)
+    per = int(np.prod(shape))
+    v = _slice(s.workspace, lay.dpv + 8 * per * b, per, np.int64).reshape(shape)
+    a = _slice(s.workspace, lay.dpa + 4 * per * b, per, np.uint32).reshape(shape)
+    Du, C = inst.D // inst.unit, len(inst.cand)
+    v = v[:inst.Pmax, :inst.L, :C, :Du + 1].astype(U64)
+    a = a[:inst.Pmax, :inst.L, :C, :Du + 1].astype(U64)
+    keys = (v << U64(24)) | a
+    return np.transpose(keys, (1, 3, 0, 2))   # [i][d][p-1][c]
+
+
+def oracle_dp_keys(inst, dp):
+    return dp[:inst.L, :, 1:, :]
+
+
+def oracle_many(instances, fn=O.solve, threads=None):
+    threads = threads or os.cpu_count() or 1
+    O.lib()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, instances))
+
+
+def same_result(g, o):
+    return (g["status"] == o["status"] and g["t_batch"] == o["t_batch"] and
+            (g["status"] != 0 or (g["bottleneck"] == o["bottleneck"] and g["plan"] == o["plan"])))

@@ -1,0 +1,185 @@
+"""GPU parity: every kernel of the CUDA path against the CPU oracle, bit for bit.
+
+All quantities are int64 nanoseconds, bytes and packed integer keys, so the bar is
+exact equality: the stage-cost words (cost builder), the per-position strategy
+loads (reduction), every DP cell key (sweep), and the batch time, bottleneck and
+plan (backtrack).  Workloads 1, 2 and 4 are compared in full; workload 3 on its
+full batch with every result checked and two instances' tables checked cell by
+cell; workload 5 at its full size (1024 instances, chunked as the benchmark runs
+it) on sampled instances.
+"""
+import numpy as np
+import pytest
+
+import gpu_util as G
+from memory_aware_device_gb300 import nest, synth
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    G.ensure_built()
+
+
+def check_tables(s, b, inst):
+    np.testing.assert_array_equal(G.cost_table(s, b, inst), O.cost_tensor(inst))
+    np.testing.assert_array_equal(G.loads_table(s, b, inst), O.loads(inst))
+    o = O.solve(inst, want_dp=True)
+    np.testing.assert_array_equal(G.dp_keys(s, b, inst), G.oracle_dp_keys(inst, o["dp"]))
+    return o
+
+
+def test_workload1_all_tables():
+    inst = synth.config_instance(1, 0)
+    s, res = G.run([inst])
+    o = check_tables(s, 0, inst)
+    assert G.same_result(res[0], o)
+
+
+@pytest.mark.parametrize("cluster,jsplit", [(0, 0), (1, 1), (2, 2), (4, 4), (8, 8), (8, 1), (1, 8)])
+def test_workload2_all_tables(cluster, jsplit):
+    insts = synth.config_batch(2)
+    s, res = G.run(insts, cluster=cluster, jsplit=jsplit)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+    for b in (0, 7, 15):
+        check_tables(s, b, insts[b])
+
+
+def test_workload3_full_batch():
+    insts = synth.config_batch(3)
+    s, res = G.run(insts)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+    for b in (0, 63):
+        check_tables(s, b, insts[b])
+
+
+def test_workload4_full_batch():
+    insts = synth.config_batch(4)
+    s, res = G.run(insts)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+    for b in (0, 100, 255):
+        check_tables(s, b, insts[b])
+
+
+def test_workload5_full_size_sampled():
+    """All 1024 instances solved in chunks of 152; sampled instances against the oracle."""
+    insts = synth.config_batch(5)
+    s, res = G.run(insts, chunk=152)
+    assert all(r["status"] in (nest.SOLVED, nest.INFEASIBLE) for r in res)
+    sample = [0, 511, 1023]
+    oracle = G.oracle_many([insts[b] for b in sample])
+    for b, o in zip(sample, oracle):
+        assert G.same_result(res[b], o), b
+    # the last chunk's tables are still in the workspace: check one of its instances
+    last0 = (1024 // 152) * 152
+    np.testing.assert_array_equal(G.cost_table(s, 1023 - last0, insts[1023]), O.cost_tensor(insts[1023]))
+
+
+@pytest.mark.parametrize("part", range(4))
+def test_random_tiny_batches(part):
+    insts = [synth.random_tiny(1000 * part + k, Lmax=7, Dmax=16) for k in range(300)]
+    s, res = G.run(insts, Pcap=6)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), (b, res[b], oracle[b])
+    for b in range(0, 300, 37):
+        if oracle[b]["status"] != 2:
+            check_tables(s, b, insts[b])
+
+
+def test_ragged_chunks_and_mixed_shapes():
+    """Instances of different sizes in one batch, processed in ragged chunks."""
+    insts = synth.config_batch(2, B=5) + synth.config_batch(1) + \
+        [synth.random_tiny(k, Lmax=7, Dmax=16) for k in range(11)]
+    oracle = G.oracle_many(insts)
+    for chunk in (0, 4, 7):
+        s, res = G.run(insts, chunk=chunk)
+        for b in range(len(insts)):
+            assert G.same_result(res[b], oracle[b]), (chunk, b)
+
+
+def test_edge_cases():
+    one_layer = synth.config_instance(1, 0)
+    one_layer.L = 1
+    for f in ("fl", "pd", "pe", "ao", "aw", "a2a", "moe"):
+        setattr(one_layer, f, getattr(one_layer, f)[:1].copy())
+    single_stage = synth.config_instance(2, 1)
+    single_stage.Pmax = 1
+    one_unit = synth.config_instance(4, 0)
+    one_unit.D = one_unit.unit
+    starved = synth.config_instance(2, 2)
+    starved.budget = 0
+    bad = synth.config_instance(2, 3)
+    bad.tierBw = np.asarray([900000, 999, 25000], np.int64)
+    bad2 = synth.config_instance(2, 4)
+    bad2.M = 3   # below Pmax
+    insts = [one_layer, single_stage, one_unit, starved, bad, bad2, synth.config_instance(2, 5)]
+    s, res = G.run(insts)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+    assert [r["status"] for r in res][3:6] == [nest.INFEASIBLE, nest.BAD_INPUT, nest.BAD_INPUT]
+
+
+def test_maximum_positions():
+    """Pcap = 31 stages (the largest the keys allow) on a 40-layer chain."""
+    inst = synth.config_instance(2, 6)
+    L = 40
+    for f in ("fl", "pd", "pe", "ao", "aw", "a2a", "moe"):
+        a = getattr(inst, f)
+        setattr(inst, f, np.resize(a, L).astype(a.dtype))
+    inst.L, inst.Pmax, inst.budget = L, 31, 12 * 10**9
+    s, res = G.run([inst])
+    o = check_tables(s, 0, inst)
+    assert G.same_result(res[0], o)
+
+
+def test_deterministic_bytes():
+    insts = synth.config_batch(2)
+    s1, r1 = G.run(insts)
+    s2, r2 = G.run(insts)
+    assert r1 == r2
+    assert (s1.plans.cpu().numpy() == s2.plans.cpu().numpy()).all()
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import torch
+    insts = synth.config_batch(2)
+    dims = nest.make_dims(insts)
+    rec = nest.pack_records(insts, dims)
+    ws = torch.empty(nest.workspace_size(dims, host=True), dtype=torch.uint8, device="cuda")
+    costs = np.zeros(dims.B, np.int64)
+    plans = np.zeros(dims.B * nest.plan_bytes(dims), np.uint8)
+    assert nest.solve_host_raw(dims, rec, costs, plans, ws) == nest.NEST_OK
+    _, res = G.run(insts)
+    assert nest.decode_plans(plans, dims) == res
+    assert costs.tolist() == [r["t_batch"] for r in res]
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """A wait forced to give up marks the instances NEST_TIMED_OUT; the GPU context
+    stays usable and the next call is exact again."""
+    import torch
+    insts = synth.config_batch(2, B=4)
+    _, res = G.run(insts, spin_limit=-1)
+    assert all(r["status"] == nest.TIMED_OUT and r["t_batch"] == -1 for r in res)
+    dims = nest.make_dims(insts)
+    ws = torch.empty(nest.workspace_size(dims, host=True), dtype=torch.uint8, device="cuda")
+    costs = np.zeros(dims.B, np.int64)
+    plans = np.zeros(dims.B * nest.plan_bytes(dims), np.uint8)
+    rc = nest.solve_host_raw(dims, nest.pack_records(insts, dims), costs, plans, ws,
+                             opt=nest.options(spin_limit=-1))
+    assert rc == nest.NEST_E_TIMEOUT
+    _, res2 = G.run(insts)
+    oracle = G.oracle_many(insts)
+    assert all(G.same_result(a, b) for a, b in zip(res2, oracle))
