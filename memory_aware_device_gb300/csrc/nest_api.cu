@@ -6,9 +6,22 @@
 // backtrack.  Nothing is allocated and no state survives the call.
 #include <cuda_runtime.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "nest_internal.cuh"
+
+namespace nest {
+
+int cuda_status(int err, const char *what) {
+    if (err == cudaSuccess) return NEST_OK;
+    if (std::getenv("NEST_DEBUG"))
+        std::fprintf(stderr, "nest: %s failed: %s\n", what, cudaGetErrorString(cudaError_t(err)));
+    return NEST_E_CUDA;
+}
+
+}  // namespace nest
 
 using namespace nest;
 
@@ -134,8 +147,7 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
     cudaEvent_t *ev = opt ? reinterpret_cast<cudaEvent_t *>(opt->events) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto mark = [&](int chunk_idx, int k) {
-        if (ev && cudaEventRecord(ev[6 * chunk_idx + k], st) != cudaSuccess) return NEST_E_CUDA;
-        return NEST_OK;
+        return ev ? cuda_status(cudaEventRecord(ev[6 * chunk_idx + k], st), "cudaEventRecord") : NEST_OK;
     };
     int ci = 0;
     for (int32_t first = 0; first < dims->B; first += chunk, ci++) {
@@ -182,14 +194,18 @@ int nest_solve_host(const nest_dims *dims, const void *records_host, int64_t *co
     unsigned char *ws = plans_d + align_up(B * plan_bytes(g), 256);
     const size_t ws_left = ws_bytes - size_t(ws - base);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(rec_d, records_host, size_t(B * rl.record_bytes), cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return NEST_E_CUDA;
-    int rc = nest_solve(dims, rec_d, costs_d, plans_d, ws, ws_left, stream, opt);
+    int rc = cuda_status(
+        cudaMemcpyAsync(rec_d, records_host, size_t(B * rl.record_bytes), cudaMemcpyHostToDevice, st),
+        "cudaMemcpyAsync (records)");
     if (rc != NEST_OK) return rc;
-    if (cudaMemcpyAsync(costs_host, costs_d, size_t(8 * B), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaMemcpyAsync(plans_host, plans_d, size_t(B * plan_bytes(g)), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return NEST_E_CUDA;
+    rc = nest_solve(dims, rec_d, costs_d, plans_d, ws, ws_left, stream, opt);
+    if (rc != NEST_OK) return rc;
+    if ((rc = cuda_status(cudaMemcpyAsync(costs_host, costs_d, size_t(8 * B), cudaMemcpyDeviceToHost, st),
+                          "cudaMemcpyAsync (costs)")) ||
+        (rc = cuda_status(cudaMemcpyAsync(plans_host, plans_d, size_t(B * plan_bytes(g)), cudaMemcpyDeviceToHost, st),
+                          "cudaMemcpyAsync (plans)")) ||
+        (rc = cuda_status(cudaStreamSynchronize(st), "cudaStreamSynchronize")))
+        return rc;
     const unsigned char *ph = static_cast<const unsigned char *>(plans_host);
     for (int64_t b = 0; b < B; b++)
         if (reinterpret_cast<const nest_plan_header *>(ph + b * plan_bytes(g))->status == NEST_TIMED_OUT)

@@ -100,7 +100,7 @@ int launch_backtrack(const PassArgs &a, void *stream) {
     const int threads = 128;
     const int64_t total = int64_t(a.n) * 32;
     backtrack_kernel<<<unsigned((total + threads - 1) / threads), threads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cudaGetLastError() == cudaSuccess ? NEST_OK : NEST_E_CUDA;
+    return cuda_status(cudaGetLastError(), "backtrack launch");
 }
 
 }  // namespace nest

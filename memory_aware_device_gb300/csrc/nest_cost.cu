@@ -141,7 +141,7 @@ int launch_cost(const PassArgs &a, void *stream) {
     const int threads = 256;
     dim3 grid(unsigned((work + threads - 1) / threads), unsigned(a.n));
     cost_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cudaGetLastError() == cudaSuccess ? NEST_OK : NEST_E_CUDA;
+    return cuda_status(cudaGetLastError(), "cost launch");
 }
 
 }  // namespace nest

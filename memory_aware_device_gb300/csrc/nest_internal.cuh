@@ -176,6 +176,10 @@ __host__ __device__ inline PrepHdr *prep_hdr(const PassArgs &a, int b) {
     return reinterpret_cast<PrepHdr *>(a.ws + a.w.prep + int64_t(b) * a.w.prep_stride);
 }
 
+// Maps a CUDA runtime status to NEST_OK / NEST_E_CUDA; with NEST_DEBUG set in the
+// environment a failure is also reported on stderr with the call that failed.
+int cuda_status(int err, const char *what);
+
 // Launchers (one translation unit each).
 int launch_prep(const PassArgs &a, void *stream);
 int launch_cost(const PassArgs &a, void *stream);

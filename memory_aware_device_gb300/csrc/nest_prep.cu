@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
 
 int launch_prep(const PassArgs &a, void *stream) {
     prep_kernel<<<a.n, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cudaGetLastError() == cudaSuccess ? NEST_OK : NEST_E_CUDA;
+    return cuda_status(cudaGetLastError(), "prep launch");
 }
 
 }  // namespace nest

@@ -69,12 +69,12 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(PassArgs a) {
 int launch_reduce(const PassArgs &a, void *stream) {
     const int64_t rows = int64_t(a.g.NP) * a.g.Kmax;
     const size_t smem = size_t(a.g.Pcap + 1) * kThreads * sizeof(uint64_t);
-    if (cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-        cudaSuccess)
-        return NEST_E_CUDA;
+    if (int rc = cuda_status(cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+                             "reduce smem attribute"))
+        return rc;
     dim3 grid(unsigned((rows + kThreads - 1) / kThreads), unsigned(a.n));
     reduce_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
-    return cudaGetLastError() == cudaSuccess ? NEST_OK : NEST_E_CUDA;
+    return cuda_status(cudaGetLastError(), "reduce launch");
 }
 
 }  // namespace nest

@@ -333,8 +333,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) sweep_kernel(PassArgs a) {
 template <int CT>
 int launch_ct(const PassArgs &a, void *stream, size_t smem) {
     auto fn = sweep_kernel<CT>;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-        return NEST_E_CUDA;
+    if (int rc = cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+                             "sweep smem attribute"))
+        return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(a.n * a.cluster), 1, 1);
     cfg.blockDim = dim3(unsigned(a.threads), 1, 1);
@@ -347,7 +348,7 @@ int launch_ct(const PassArgs &a, void *stream, size_t smem) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, a) == cudaSuccess ? NEST_OK : NEST_E_CUDA;
+    return cuda_status(cudaLaunchKernelEx(&cfg, fn, a), "sweep launch");
 }
 
 }  // namespace

@@ -175,8 +175,11 @@ def options(chunk=0, cluster=0, jsplit=0, spin_limit=0, events=None) -> Options:
     o = Options(chunk=chunk, sweep_cluster=cluster, sweep_jsplit=jsplit, reserved=0, spin_limit=spin_limit,
                 events=None)
     if events is not None:
+        for e in events:
+            if not e.cuda_event:   # torch creates the CUDA event lazily, on its first record
+                e.record()
         arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
-        o._events_keep = arr
+        o._events_keep = (arr, list(events))   # the CUDA events live as long as the options
         o.events = C.cast(arr, C.c_void_p)
     return o
 
