@@ -193,6 +193,28 @@ typedef struct {
 } nest_ws_layout;
 int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out);
 
+/* ---- solve without allocation ------------------------------------------------
+ * No counterpart in the paper: this serves callers that cannot allocate device
+ * memory - a serving or scheduling process that has handed all device memory to its
+ * own pool, a plug-in inside a host application that forbids device allocations in
+ * its callbacks, code that must not stall on the device-wide synchronisation that
+ * cudaMalloc / cudaFree can cause.
+ *
+ * Same arguments and results as nest_solve, without the workspace: the scratch
+ * memory is a fixed array of NEST_STATIC_SCRATCH_BYTES inside the library, held by
+ * every GPU that loads the library until the process exits.  The call allocates
+ * nothing and frees nothing.  Returns NEST_E_WORKSPACE when the batch (or chunk,
+ * opt->chunk) needs more scratch than that - nest_workspace_size() tells how much -
+ * and otherwise what nest_solve returns.  The first call made with a device current
+ * looks up the array's device address for that device; make that first call before
+ * any stream capture.  All calls share the array and it keeps the last call's
+ * contents (nothing in it needs clearing: the solve writes every scratch word before
+ * reading it); calls whose work overlaps on the GPU race on it, so the caller must
+ * serialise them (one stream, or an event between them). */
+#define NEST_STATIC_SCRATCH_BYTES (64u << 20)
+int nest_solve_static(const nest_dims *dims, const void *records, int64_t *costs_out, void *plans_out,
+                      void *stream, const nest_options *opt);
+
 #ifdef __cplusplus
 }
 #endif

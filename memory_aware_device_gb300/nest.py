@@ -25,7 +25,8 @@ ERRORS = {NEST_E_INVALID: "invalid argument", NEST_E_LIMITS: "batch dimensions b
 
 # Every function declared in include/nest.h.
 EXPORTS = ("nest_record_layout", "nest_plan_bytes", "nest_workspace_size", "nest_workspace_layout",
-           "nest_solve", "nest_workspace_size_host", "nest_solve_host")
+           "nest_solve", "nest_workspace_size_host", "nest_solve_host", "nest_solve_static")
+STATIC_SCRATCH_BYTES = 64 << 20   # NEST_STATIC_SCRATCH_BYTES
 
 
 class NestError(RuntimeError):
@@ -84,6 +85,7 @@ def lib():
                                  C.c_void_p, P(Options)]
         L.nest_solve_host.argtypes = [P(Dims), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
                                       C.c_void_p, P(Options)]
+        L.nest_solve_static.argtypes = [P(Dims), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, P(Options)]
         _lib = L
     return _lib
 
