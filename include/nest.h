@@ -55,7 +55,7 @@ extern "C" {
  * on the host before any launch, NEST_E_LIMITS otherwise):
  *   1 <= Lmax <= 255 layers, 1 <= Tmax <= 8 tiers, 1 <= Cmax <= 15 candidates,
  *   1 <= Smax <= 4095 strategies, 1 <= Pcap <= 31 stages,
- *   1 <= Dumax <= 1024 device units, Cmax * (Dumax + 2) <= 8192.            */
+ *   1 <= Dumax <= 512 device units.                                          */
 typedef struct {
     int32_t B;      /* instances in the batch (0 is a no-op) */
     int32_t Lmax;
@@ -128,12 +128,15 @@ typedef struct {
 typedef struct {
     int32_t chunk;          /* instances per pass through the kernels; 0 = all, at most 65535 (the
                                workspace must be sized for the same chunk) */
-    int32_t sweep_cluster;  /* CTAs per instance in the DP sweep: 0 = auto, or 1, 2, 4, 8 */
-    int32_t sweep_jsplit;   /* threads sharing one DP cell: 0 = auto, or 1, 2, 4, 8 */
-    int32_t reserved;
-    int64_t spin_limit;     /* polls before a device wait gives up: 0 = default (2^26);
-                               a negative value makes every wait give up at once, which
-                               exercises the timeout path (instances end NEST_TIMED_OUT) */
+    int32_t sweep_cluster;  /* CTAs per instance in the DP sweep: 0 = auto, or 1, 2, 4, 8, 16 */
+    int32_t sweep_jsplit;   /* threads sharing one DP cell: 0 = auto, or 1, 2, 4, 8, with
+                               jsplit * (Dumax rounded up to 32) <= 512 (else NEST_E_INVALID) */
+    int32_t sweep_variant;  /* 0 = auto; 1 = rows resident in shared memory (NEST_E_LIMITS
+                               if they do not fit); 2 = rows streamed from global memory */
+    int64_t spin_limit;     /* polls before a device wait gives up (each poll suspends for at
+                               most 1 us): 0 = default (2^20, about a second); a negative
+                               value makes every wait give up at once, which exercises the
+                               timeout path (instances end NEST_TIMED_OUT) */
     void **events;          /* optional cudaEvent_t[6 * chunks]; for chunk n, events
                                [6n .. 6n+5] are recorded on the stream before prep, cost
                                build, strategy reduction, DP sweep, backtrack, and after

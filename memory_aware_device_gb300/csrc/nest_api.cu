@@ -27,41 +27,6 @@ using namespace nest;
 
 namespace {
 
-constexpr int64_t kSweepSmemBudget = 200 * 1024;
-
-struct Config {
-    int cluster, jsplit, jc, threads;
-};
-
-int pick_config(const Geo &g, int n, const nest_options *opt, Config &cfg) {
-    const int NTd = (g.Dumax + 31) / 32 * 32;
-    int jsplit = opt ? opt->sweep_jsplit : 0;
-    if (jsplit == 0) {
-        jsplit = 1;
-        while (jsplit < 8 && NTd * jsplit * 2 <= 512) jsplit *= 2;
-    }
-    if (jsplit != 1 && jsplit != 2 && jsplit != 4 && jsplit != 8) return NEST_E_INVALID;
-    if (NTd * jsplit > 1024) return NEST_E_LIMITS;
-    int cluster = opt ? opt->sweep_cluster : 0;
-    if (cluster == 0) {
-        int dev = 0, sms = 148;
-        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cluster = 1;
-        while (cluster < 8 && cluster * 2 <= g.Pcap && int64_t(n) * cluster * 2 <= sms) cluster *= 2;
-    }
-    if (cluster != 1 && cluster != 2 && cluster != 4 && cluster != 8) return NEST_E_INVALID;
-    int dev = 0, optin = 227 * 1024;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    const int64_t budget = kSweepSmemBudget < optin - 1024 ? kSweepSmemBudget : optin - 1024;
-    const int threads = NTd * jsplit;
-    int jc = g.Lmax > 1 ? g.Lmax - 1 : 1;
-    while (jc > 1 && sweep_smem_bytes(g, jc, jsplit, threads) > budget) jc--;
-    if (sweep_smem_bytes(g, jc, jsplit, threads) > budget) return NEST_E_LIMITS;
-    cfg = {cluster, jsplit, jc, threads};
-    return NEST_OK;
-}
-
 // Instances per pass: the whole batch by default, at most 65535 (the cost and
 // reduction kernels index instances with blockIdx.y).
 int32_t chunk_of(const nest_dims *dims, int32_t chunk) {
@@ -127,8 +92,9 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
     const int32_t chunk = chunk_of(dims, opt ? opt->chunk : 0);
     const WsLayout w = ws_layout(g, chunk);
     if (ws_bytes < size_t(w.total)) return NEST_E_WORKSPACE;
-    Config cfg;
-    int rc = pick_config(g, chunk, opt, cfg);
+    SweepConfig cfg;
+    int rc = sweep_configure(g, chunk, opt ? opt->sweep_cluster : 0, opt ? opt->sweep_jsplit : 0,
+                             opt ? opt->sweep_variant : 0, cfg);
     if (rc != NEST_OK) return rc;
 
     PassArgs a;
@@ -143,6 +109,7 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
     a.jsplit = cfg.jsplit;
     a.jc = cfg.jc;
     a.threads = cfg.threads;
+    a.resident = cfg.resident;
     a.spin_limit = opt ? opt->spin_limit : 0;
     cudaEvent_t *ev = opt ? reinterpret_cast<cudaEvent_t *>(opt->events) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "../../include/nest.h"
+#include "nest_divide.cuh"
 
 namespace nest {
 
@@ -31,7 +32,7 @@ struct Geo {
 inline bool make_geo(const nest_dims &d, Geo &g) {
     if (d.B < 0 || d.Lmax < 1 || d.Lmax > 255 || d.Tmax < 1 || d.Tmax > 8 || d.Cmax < 1 ||
         d.Cmax > 15 || d.Smax < 1 || d.Smax > 4095 || d.Pcap < 1 || d.Pcap > 31 || d.Dumax < 1 ||
-        d.Dumax > 1024 || int64_t(d.Cmax) * (d.Dumax + 2) > 8192)
+        d.Dumax > 512)
         return false;
     g.B = d.B;
     g.Lmax = d.Lmax;
@@ -81,8 +82,10 @@ struct PrepHdr {
     int64_t R, M, budget, opt;
     int64_t G[8], bw[8], lat[8];
     int32_t cand[16];
-    int32_t mlim[16];  // largest m with 2 * unit * 2^m <= G[cand c], -1 if none
-    int64_t pad1[2];
+    int32_t mlim[16];    // largest m with 2 * unit * 2^m <= G[cand c], -1 if none
+    int8_t tier_log[16]; // smallest tier whose groups hold 2^x devices, x = 0 .. 13
+    Divisor bwdiv[8];    // invariant divisors for bw[t]
+    Divisor Mdiv, Rdiv;  // and for M and R
 };
 static_assert(sizeof(PrepHdr) % 16 == 0, "PrepHdr alignment");
 
@@ -169,6 +172,7 @@ struct PassArgs {
     int32_t jsplit;                // sweep threads per DP cell
     int32_t jc;                    // sweep j-chunk (layers staged per tile)
     int32_t threads;               // sweep threads per CTA
+    int32_t resident;              // sweep variant: 1 = dp rows resident in shared memory
     int64_t spin_limit;            // polls per bounded wait (negative: give up at once)
 };
 
@@ -186,7 +190,16 @@ int launch_cost(const PassArgs &a, void *stream);
 int launch_reduce(const PassArgs &a, void *stream);
 int launch_sweep(const PassArgs &a, void *stream);
 int launch_backtrack(const PassArgs &a, void *stream);
-// Dynamic shared memory of the sweep for a given configuration (0 if it cannot fit).
+// Dynamic shared memory of the streaming and resident sweep variants.
 int64_t sweep_smem_bytes(const Geo &g, int jc, int jsplit, int threads);
+int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads);
+
+// Launch shape of the DP sweep for passes of n instances.  cluster_opt / jsplit_opt
+// (0 = choose) and variant (0 = choose, 1 = resident, 2 = streaming) come from
+// nest_options.  Returns NEST_OK, NEST_E_INVALID or NEST_E_LIMITS.
+struct SweepConfig {
+    int cluster, jsplit, jc, threads, resident, resident_waves;
+};
+int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int variant, SweepConfig &out);
 
 }  // namespace nest

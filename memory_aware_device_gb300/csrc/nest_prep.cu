@@ -109,6 +109,14 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
         ph->G[t] = t < h.T ? G[t] : 0;
         ph->bw[t] = t < h.T ? bw[t] : 1;
         ph->lat[t] = t < h.T ? lat[t] : 0;
+        ph->bwdiv[t] = make_divisor(uint64_t(t < h.T ? bw[t] : 1));
+    }
+    if (threadIdx.x == 8) ph->Mdiv = make_divisor(uint64_t(h.M));
+    if (threadIdx.x == 9) ph->Rdiv = make_divisor(uint64_t(h.R));
+    for (int x = threadIdx.x; x < 16; x += blockDim.x) {
+        int t = 0;
+        while (t < h.T - 1 && G[t] < (int64_t(1) << x)) t++;
+        ph->tier_log[x] = int8_t(t);
     }
     for (int c = threadIdx.x; c < 16; c += blockDim.x) {
         int ml = -1;

@@ -51,7 +51,7 @@ class WsLayout(C.Structure):
 
 class Options(C.Structure):
     _fields_ = [("chunk", C.c_int32), ("sweep_cluster", C.c_int32), ("sweep_jsplit", C.c_int32),
-                ("reserved", C.c_int32), ("spin_limit", C.c_int64), ("events", C.c_void_p)]
+                ("sweep_variant", C.c_int32), ("spin_limit", C.c_int64), ("events", C.c_void_p)]
 
 
 HEADER_DT = np.dtype([("L", "<i4"), ("D", "<i4"), ("unit", "<i4"), ("T", "<i4"), ("C", "<i4"),
@@ -173,9 +173,9 @@ def decode_plans(raw: np.ndarray, dims: Dims) -> List[dict]:
     return out
 
 
-def options(chunk=0, cluster=0, jsplit=0, spin_limit=0, events=None) -> Options:
-    o = Options(chunk=chunk, sweep_cluster=cluster, sweep_jsplit=jsplit, reserved=0, spin_limit=spin_limit,
-                events=None)
+def options(chunk=0, cluster=0, jsplit=0, spin_limit=0, events=None, variant=0) -> Options:
+    o = Options(chunk=chunk, sweep_cluster=cluster, sweep_jsplit=jsplit, sweep_variant=variant,
+                spin_limit=spin_limit, events=None)
     if events is not None:
         for e in events:
             if not e.cuda_event:   # torch creates the CUDA event lazily, on its first record

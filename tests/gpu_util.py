@@ -16,13 +16,14 @@ def ensure_built():
     O.build()
 
 
-def run(instances, chunk=0, cluster=0, jsplit=0, spin_limit=0, Pcap=None, Dumax=None):
+def run(instances, chunk=0, cluster=0, jsplit=0, spin_limit=0, Pcap=None, Dumax=None, variant=0):
     """Solve on cuda:0; returns (solver, results)."""
     import torch
     dims = nest.make_dims(instances, Pcap=Pcap, Dumax=Dumax)
     s = nest.Solver(dims, chunk=chunk)
     s.load(nest.pack_records(instances, dims))
-    s.run(opt=nest.options(chunk=chunk, cluster=cluster, jsplit=jsplit, spin_limit=spin_limit))
+    s.run(opt=nest.options(chunk=chunk, cluster=cluster, jsplit=jsplit, spin_limit=spin_limit,
+                           variant=variant))
     torch.cuda.synchronize()
     return s, s.results()
 

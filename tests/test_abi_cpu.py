@@ -63,7 +63,7 @@ def test_pack_roundtrip():
 
 
 @pytest.mark.parametrize("field,value", [("Lmax", 256), ("Lmax", 0), ("Tmax", 9), ("Cmax", 16),
-                                         ("Smax", 4096), ("Pcap", 32), ("Dumax", 1025), ("Dumax", 0)])
+                                         ("Smax", 4096), ("Pcap", 32), ("Dumax", 513), ("Dumax", 0)])
 def test_limits_rejected_on_host(field, value):
     dims = nest.make_dims(synth.config_batch(2, B=2))
     setattr(dims, field, value)
@@ -73,10 +73,9 @@ def test_limits_rejected_on_host(field, value):
     assert rc == nest.NEST_E_LIMITS
 
 
-def test_candidate_smem_limit():
-    dims = nest.make_dims(synth.config_batch(2, B=1))
-    dims.Cmax, dims.Dumax = 15, 1024   # 15 * 1026 > 8192
-    assert nest.workspace_size(dims) == 0
+def test_largest_dims_accepted():
+    dims = nest.Dims(B=1, Lmax=255, Tmax=8, Cmax=15, Smax=4095, Pcap=31, Dumax=512)
+    assert nest.workspace_size(dims) > 0 and nest.plan_bytes(dims) == 24 + 12 * 31 + 4
 
 
 def test_bad_arguments_rejected_before_any_launch():

@@ -33,17 +33,31 @@ def check_tables(s, b, inst):
     return o
 
 
-def test_workload1_all_tables():
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_workload1_all_tables(variant):
     inst = synth.config_instance(1, 0)
-    s, res = G.run([inst])
+    s, res = G.run([inst], variant=variant)
     o = check_tables(s, 0, inst)
     assert G.same_result(res[0], o)
 
 
-@pytest.mark.parametrize("cluster,jsplit", [(0, 0), (1, 1), (2, 2), (4, 4), (8, 8), (8, 1), (1, 8)])
-def test_workload2_all_tables(cluster, jsplit):
+# (CTAs per instance, threads per cell, sweep variant: 0 auto, 1 resident, 2 streaming)
+SWEEP_CONFIGS = [(0, 0, 0), (1, 1, 2), (2, 2, 2), (4, 4, 2), (4, 2, 2), (8, 4, 1), (8, 1, 2), (8, 2, 1),
+                 (16, 4, 1), (16, 8, 2), (16, 1, 1), (16, 2, 1)]
+
+
+def test_resident_variant_rejected_when_it_does_not_fit():
+    # 4 CTAs per instance would hold 4 positions' rows and loads: about 270 KB per CTA
+    insts = synth.config_batch(2, B=2)
+    with pytest.raises(nest.NestError) as e:
+        G.run(insts, cluster=4, jsplit=4, variant=1)
+    assert e.value.rc == nest.NEST_E_LIMITS
+
+
+@pytest.mark.parametrize("cluster,jsplit,variant", SWEEP_CONFIGS)
+def test_workload2_all_tables(cluster, jsplit, variant):
     insts = synth.config_batch(2)
-    s, res = G.run(insts, cluster=cluster, jsplit=jsplit)
+    s, res = G.run(insts, cluster=cluster, jsplit=jsplit, variant=variant)
     oracle = G.oracle_many(insts)
     for b in range(len(insts)):
         assert G.same_result(res[b], oracle[b]), b
@@ -85,10 +99,10 @@ def test_workload5_full_size_sampled():
     np.testing.assert_array_equal(G.cost_table(s, 1023 - last0, insts[1023]), O.cost_tensor(insts[1023]))
 
 
-@pytest.mark.parametrize("part", range(4))
-def test_random_tiny_batches(part):
+@pytest.mark.parametrize("part,variant", [(0, 0), (1, 1), (2, 2), (3, 1)])
+def test_random_tiny_batches(part, variant):
     insts = [synth.random_tiny(1000 * part + k, Lmax=7, Dmax=16) for k in range(300)]
-    s, res = G.run(insts, Pcap=6)
+    s, res = G.run(insts, Pcap=6, variant=variant)
     oracle = G.oracle_many(insts)
     for b in range(len(insts)):
         assert G.same_result(res[b], oracle[b]), (b, res[b], oracle[b])
@@ -166,12 +180,13 @@ def test_host_entry_point_matches_device_entry_point():
     assert costs.tolist() == [r["t_batch"] for r in res]
 
 
-def test_bounded_wait_gives_up_and_context_survives():
+@pytest.mark.parametrize("variant", [1, 2])
+def test_bounded_wait_gives_up_and_context_survives(variant):
     """A wait forced to give up marks the instances NEST_TIMED_OUT; the GPU context
     stays usable and the next call is exact again."""
     import torch
     insts = synth.config_batch(2, B=4)
-    _, res = G.run(insts, spin_limit=-1)
+    _, res = G.run(insts, spin_limit=-1, variant=variant)
     assert all(r["status"] == nest.TIMED_OUT and r["t_batch"] == -1 for r in res)
     dims = nest.make_dims(insts)
     ws = torch.empty(nest.workspace_size(dims, host=True), dtype=torch.uint8, device="cuda")
