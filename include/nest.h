@@ -134,7 +134,7 @@ typedef struct {
     int32_t sweep_variant;  /* 0 = auto; 1 = rows resident in shared memory (NEST_E_LIMITS
                                if they do not fit); 2 = rows streamed from global memory */
     int64_t spin_limit;     /* polls before a device wait gives up (each poll suspends for at
-                               most 1 us): 0 = default (2^20, about a second); a negative
+                               most 20 us): 0 = default (2^16, about a second); a negative
                                value makes every wait give up at once, which exercises the
                                timeout path (instances end NEST_TIMED_OUT) */
     void **events;          /* optional cudaEvent_t[6 * chunks]; for chunk n, events

@@ -78,7 +78,10 @@ inline void record_layout(const Geo &g, nest_layout &o) {
 struct PrepHdr {
     int32_t status;  // NEST_SOLVED (0) when the instance is valid, NEST_BAD_INPUT otherwise;
                      // the sweep raises it to NEST_TIMED_OUT when a wait gives up
-    int32_t L, D, unit, lu, Du, K, T, C, S, P, pad0;
+    int32_t L, D, unit, lu, Du, K, T, C, S, P;
+    uint32_t maxX32;     // largest link cost X, saturated at 2^31 - 1 (prep)
+    uint32_t maxload32;  // largest finite per-position load tau*, saturated (reduction)
+    int32_t pad0, pad1, pad2;
     int64_t R, M, budget, opt;
     int64_t G[8], bw[8], lat[8];
     int32_t cand[16];

@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
         __syncthreads();
     }
     int64_t *X = reinterpret_cast<int64_t *>(pb + a.pl.X);
+    __shared__ uint32_t xmax;
+    if (threadIdx.x == 0) xmax = 0;
+    __syncthreads();
     for (int e = threadIdx.x; e < (L + 1) * h.C; e += blockDim.x) {
         const int bnd = e / h.C, c = e % h.C;
         int64_t v = 0;
@@ -172,6 +175,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
             v = lat[tr] + cdiv(ao_in[bnd - 1] * 1000, bw[tr]);
         }
         X[int64_t(bnd) * g.Cmax + c] = v;
+        atomicMax(&xmax, v < 0x7FFFFFFF ? uint32_t(v) : 0x7FFFFFFFu);
     }
     uint32_t *sp = reinterpret_cast<uint32_t *>(pb + a.pl.strat);
     const int16_t *st = reinterpret_cast<const int16_t *>(rec + a.rl.strat);
@@ -180,7 +184,12 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
         sp[s] = uint32_t(ilog2(x[0])) | uint32_t(ilog2(x[1])) << 4 | uint32_t(ilog2(x[2])) << 8 |
                 uint32_t(x[3]) << 12 | uint32_t(x[4]) << 14;
     }
-    if (threadIdx.x == 0) ph->status = NEST_SOLVED;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ph->maxX32 = xmax;
+        ph->maxload32 = 0;   // raised by the strategy reduction
+        ph->status = NEST_SOLVED;
+    }
 }
 
 }  // namespace

@@ -29,8 +29,8 @@ constexpr int kUnroll = 4;
 __global__ void __launch_bounds__(kThreads) reduce_kernel(PassArgs a, int lg) {
     extern __shared__ uint64_t bucket[];   // [Pcap + 1][kThreads], one column per lane
     const int b = blockIdx.y;
-    const PrepHdr *ph = prep_hdr(a, b);
-    if (ph->status != NEST_SOLVED) return;
+    PrepHdr *ph = prep_hdr(a, b);
+    if (ph->status != NEST_SOLVED) return;   // uniform over the block
     const int G = 1 << lg;
     const int L = ph->L, K = ph->K, S = ph->S, P = ph->P;
     const int64_t rows = int64_t(L) * (L + 1) / 2 * K;
@@ -69,19 +69,34 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(PassArgs a, int lg) {
         }
     }
     __syncwarp();
-    if (!live) return;
     // lane `sub` of the group writes positions p = sub + 1, sub + 1 + G, ...
-    uint64_t *out = reinterpret_cast<uint64_t *>(a.ws + a.w.loads) + int64_t(b) * a.w.loads_stride +
-                    pair * a.g.Kpad + m;
-    const int base = threadIdx.x - sub;
-    for (int p = sub + 1; p <= P; p += G) {
-        uint64_t v = kInf;
-        for (int q = 0; q < G; q++) {
-            const uint64_t o = bucket[p * kThreads + base + q];
-            v = o < v ? o : v;
+    uint32_t tmax = 0;   // largest finite tau written, saturated at 2^31 - 1
+    if (live) {
+        uint64_t *out = reinterpret_cast<uint64_t *>(a.ws + a.w.loads) + int64_t(b) * a.w.loads_stride +
+                        pair * a.g.Kpad + m;
+        const int base = threadIdx.x - sub;
+        for (int p = sub + 1; p <= P; p += G) {
+            uint64_t v = kInf;
+            for (int q = 0; q < G; q++) {
+                const uint64_t o = bucket[p * kThreads + base + q];
+                v = o < v ? o : v;
+            }
+            out[int64_t(p - 1) * a.g.NP * a.g.Kpad] = v;
+            if (v != kInf) {
+                const uint64_t tau = v >> 16;
+                const uint32_t t32 = tau < 0x7FFFFFFFu ? uint32_t(tau) : 0x7FFFFFFFu;
+                tmax = t32 > tmax ? t32 : tmax;
+            }
         }
-        out[int64_t(p - 1) * a.g.NP * a.g.Kpad] = v;
     }
+    // one atomic per block: the sweep uses 32-bit words when every value is small
+    __shared__ uint32_t bmax;
+    if (threadIdx.x == 0) bmax = 0;
+    __syncthreads();
+    tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
+    if ((threadIdx.x & 31) == 0 && tmax) atomicMax(&bmax, tmax);
+    __syncthreads();
+    if (threadIdx.x == 0 && bmax) atomicMax(&ph->maxload32, bmax);
 }
 
 }  // namespace

@@ -41,7 +41,7 @@ namespace nest {
 
 namespace {
 
-constexpr int64_t kDefaultSpin = int64_t(1) << 20;   // polls of up to kSuspendNs: about a second
+constexpr int64_t kDefaultSpin = int64_t(1) << 16;   // polls of up to kSuspendNs: about a second
 constexpr int kMaxThreads = 512;
 
 // ---------------------------------------------------------------------------------
@@ -83,7 +83,7 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // suspends the warp in hardware for up to kSuspendNs while the phase is incomplete,
 // so waiting warps do not take issue slots; after `limit` polls the wait gives up
 // (limit < 0: at once).
-constexpr uint32_t kSuspendNs = 1000;
+constexpr uint32_t kSuspendNs = 20000;   // a try_wait also returns as soon as the phase completes
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase, int64_t limit) {
     if (limit < 0) return false;
     const uint32_t a = smem_addr(bar);
@@ -105,10 +105,6 @@ __device__ __forceinline__ uint32_t cluster_map(const void *local, uint32_t rank
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
     return r;
-}
-
-__device__ __forceinline__ void st_cluster(uint32_t addr, int64_t v) {
-    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------------
@@ -261,263 +257,329 @@ __device__ __forceinline__ void init_cmin(int *cmin, const PrepHdr *ph, int C) {
 }
 
 // ---------------------------------------------------------------------------------
-// Resident variant: one thread per cell (c, d) and slice of the cut points
+// Resident variant
 // ---------------------------------------------------------------------------------
 
-// One DP cell (c, d) held by one thread.
-struct Cell {
-    int64_t bv;   // best value (kCap = none)
-    int64_t bvx;  // bv - X[i][c]: a transition improves the cell iff a0 < bvx and nv < bv
-    int64_t xf;   // X[i][c]
-    uint32_t bi;  // argument (j << 8) | (m << 4) | c'
-
-    __device__ __forceinline__ void init(int64_t x) {
-        xf = x;
-        bv = kCap;
-        bvx = kCap - x;
-        bi = kNoArg;
-    }
-    __device__ __forceinline__ uint64_t key() const { return (uint64_t(bv) << 24) | bi; }
-
-    // Cut point j < L with widths m = 0 .. mtop (those this cell's input link admits):
-    // lrow[m] = load*(i, j, m, p), xs_j[c'] = X[j][c'], candidate c' admits width m iff
-    // m <= mlim2[c'], and row[c' * stride + x] = v(dp[j][x][p-1][c']).
-    template <int CT>
-    __device__ __forceinline__ void relax(int j, int d, int mtop, int C, const int *mlim2, const uint64_t *lrow,
-                                          const int64_t *xs_j, const int64_t *row, int64_t stride) {
-        int64_t xb[CT];
-#pragma unroll
-        for (int c2 = 0; c2 < CT; c2++) xb[c2] = c2 < C ? xs_j[c2] : 0;
-        for (int m = 0; m <= mtop; m++) {
-            const uint64_t lw = lrow[m];
-            if (lw == kInf) continue;
-            const int64_t tst = int64_t(lw >> 16);
-            const int x = d - (1 << m);
-#pragma unroll
-            for (int c2 = 0; c2 < CT; c2++) {
-                if (c2 >= C || m > mlim2[c2]) continue;
-                const int64_t a0 = tst + xb[c2];
-                const int64_t nv = row[c2 * stride + x];
-                if (a0 < bvx && nv < bv) {
-                    const int64_t a = a0 + xf;
-                    bv = a > nv ? a : nv;
-                    bvx = bv - xf;
-                    bi = (uint32_t(j) << 8) | (uint32_t(m) << 4) | uint32_t(c2);
-                }
-            }
-        }
-    }
-
-    // The last stage [i, L): lrow[m] = load*(i, L, m, p); the previous state is 0.
-    __device__ __forceinline__ void last(int L, int mtop, const uint64_t *lrow) {
-        for (int m = 0; m <= mtop; m++) {
-            const uint64_t lw = lrow[m];
-            if (lw == kInf) continue;
-            const int64_t a0 = int64_t(lw >> 16);
-            if (a0 < bvx) {
-                bv = a0 + xf;
-                bvx = a0;
-                bi = (uint32_t(L) << 8) | (uint32_t(m) << 4);
-            }
-        }
-    }
-};
-
-// Asynchronous 8-byte store into another CTA's shared memory that completes
-// 8 transaction bytes on an mbarrier of that CTA (both addresses from mapa).
+// Asynchronous store into another CTA's shared memory that completes its size in
+// transaction bytes on an mbarrier of that CTA (both addresses from mapa).
 __device__ __forceinline__ void st_async_remote(uint32_t addr, int64_t v, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u64 [%0], %1, [%2];" ::"r"(addr), "l"(v),
                  "r"(bar)
                  : "memory");
 }
+__device__ __forceinline__ void st_async_remote(uint32_t addr, uint32_t v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+                 "r"(bar)
+                 : "memory");
+}
 
-struct ResPlan {
-    int64_t mbar, rowbar, X, H, Lt, red, total;
-    int64_t H_slot, Lt_slot;  // bytes per owned position
+// Value words of the resident variant.  `cap` marks a cell without a value, `far` an
+// A entry no cell can take; every finite value stays below `cap`, and far plus any
+// link cost neither overflows nor drops below cap.  32-bit words are exact when the
+// largest load plus two link costs is below 2^30, which the strategy reduction and
+// the prep pass record per instance; otherwise the instance uses 64-bit words.
+template <typename V>
+struct Word;
+template <>
+struct Word<uint32_t> {
+    static constexpr uint32_t cap = 0x7FFFFFFFu;
+    static constexpr uint32_t far = 0x80000000u;
+};
+template <>
+struct Word<int64_t> {
+    static constexpr int64_t cap = kCap;
+    static constexpr int64_t far = int64_t(1) << 46;
 };
 
-__host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, int threads) {
+__device__ __forceinline__ bool narrow_words(const PrepHdr *ph) {
+    return uint64_t(ph->maxload32) + 2 * uint64_t(ph->maxX32) < (uint64_t(1) << 30);
+}
+
+// Shared-memory plan of the resident variant, in 8-byte words (sized for 64-bit
+// values; 32-bit values use the first half of the H and A regions).
+struct ResPlan {
+    int rowbar, X, H, A, red, total;   // word offsets; total = words
+    int Hslot, Hrow, Aj, Aslot, Abuf;  // strides in values
+};
+
+__host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, int threads, int CT, int KT) {
     ResPlan s;
-    int64_t off = 0;
-    s.mbar = off;
-    off += 16;
-    s.rowbar = off;                                   // one mbarrier per (owned slot, row j)
-    off = align_up(off + 8 * int64_t(nown) * g.Lmax, 128);
+    auto up = [](int w) { return (w + 15) / 16 * 16; };   // 128-byte alignment
+    int off = 0;
+    s.rowbar = off;                                       // one mbarrier per (owned slot, row j)
+    off = up(off + nown * g.Lmax);
     s.X = off;
-    off = align_up(off + 8 * int64_t(g.Lmax + 1) * g.Cmax, 128);
-    s.H_slot = 8 * int64_t(g.Lmax) * g.Cmax * g.Dpad;
+    off = up(off + (g.Lmax + 1) * g.Cmax);
+    s.Hrow = g.Cmax * g.Dpad;
+    s.Hslot = g.Lmax * s.Hrow;
     s.H = off;
-    off = align_up(off + nown * s.H_slot, 128);
-    s.Lt_slot = 8 * int64_t(g.NP) * g.Kpad;
-    s.Lt = off;
-    off = align_up(off + nown * s.Lt_slot, 128);
+    off = up(off + nown * s.Hslot);
+    s.Aj = CT * KT;                                       // A[j][c'][m]
+    s.Aslot = (g.Lmax + 1) * s.Aj;
+    s.Abuf = nown * s.Aslot;
+    s.A = off;
+    off = up(off + 2 * s.Abuf);
     s.red = off;
-    if (jsplit > 1) off = align_up(off + 8 * int64_t(threads), 128);
+    off = up(off + 2 * threads * CT);                     // slice minima, two buffers
     s.total = off;
     return s;
 }
 
-// Resident variant.  Each CTA owns positions p = rank + 1 + k * cs (slots k).  It
-// holds in shared memory the whole loads table of its positions (one TMA bulk copy
-// at the start) and, in slot k, the rows dp[j][*][p_k - 1][*] pushed to it by the
-// owner of position p_k - 1: each row arrives as st.async stores that complete on
-// that row's own mbarrier, so a CTA waits only for the rows it reads and the CTAs
-// of a cluster form a pipeline over positions instead of moving in lockstep.  The
-// footprint is kept small (three CTAs per SM) so that the clusters of a whole batch
-// are resident at once.  The dp tables in global memory are written for the backtrack.
-template <int CT>
-__global__ void __launch_bounds__(kMaxThreads, 3) sweep_resident_kernel(PassArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ volatile int abort_flag;
+// Relaxation of one cut point j for the cells (c, d) of one thread, c < CT: for every
+// width m <= mall and next-link candidate c' the candidate is
+// v = max(A[j][c'][m] + X[i][c], v(dp[j][d - 2^m][p-1][c'])).  A and the dp value are
+// read once and tried against every cell of the thread.  Widths are visited in the
+// canonical order (m, c'), so the first strict improvement is the smallest key.
+template <int CT, int KT, typename V>
+__device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Dpad, int C, int j, int mall, const int *mtop,
+                                          V *bv, V *bvx, uint32_t *bi, const V *xf) {
+#pragma unroll
+    for (int m = 0; m < KT; m++) {
+        if (m > mall) break;
+#pragma unroll
+        for (int c2 = 0; c2 < CT; c2++) {
+            if (c2 >= C) break;
+            const V av = Aj[c2 * KT + m];
+            const V nv = Hj[c2 * Dpad - (1 << m)];
+            const uint32_t idx = (uint32_t(j) << 8) | (uint32_t(m) << 4) | uint32_t(c2);
+#pragma unroll
+            for (int c = 0; c < CT; c++) {
+                if (m <= mtop[c] && av < bvx[c] && nv < bv[c]) {
+                    const V ax = av + xf[c];
+                    bv[c] = ax > nv ? ax : nv;
+                    bvx[c] = bv[c] - xf[c];
+                    bi[c] = idx;
+                }
+            }
+        }
+    }
+}
+
+// Resident variant.  Each CTA owns positions p = rank + 1 + k * cs (slots k).
+//  - Slot k holds the rows dp[j][*][p_k - 1][*] pushed to it by the owner of
+//    position p_k - 1: each row arrives as st.async stores that complete on that
+//    row's own mbarrier, so a CTA waits only for the rows it reads and the CTAs of
+//    a cluster form a pipeline over positions instead of moving in lockstep.
+//  - At step i only row i + 1 of a slot is new: the cut points j >= i + 2 are relaxed
+//    first, and the wait for row i + 1 comes after them, so the neighbour's push
+//    overlaps this CTA's own work.  The slice that takes j = i + 1 adds it last, with
+//    ties going to it (its key is the smaller one).
+//  - For step i it reads A[j][c'][m] = load*(i, j, m, p_k) + X[j][c'], with the
+//    outgoing link's width rule and the empty loads folded in as `far`; the rows of
+//    step i - 1 are built during step i into the other buffer (their global loads
+//    are issued before the relaxation, so their latency is hidden).
+//  - A thread owns one device count d, every candidate c of it, and a slice of the
+//    cut points j; the jsplit slices are combined through a double-buffered shared
+//    array, one barrier per slot.
+// The footprint is kept small so that the clusters of a whole batch are resident at
+// once.  dp is also written to global memory (64-bit) for the backtrack.
+template <int CT, int KT, typename V>
+__device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
+                                              volatile int &abort_flag) {
     const Geo &g = a.g;
     const int cs = a.cluster;
-    const int b = blockIdx.x / cs;
-    const int rank = int(cluster_rank());
-    PrepHdr *ph = prep_hdr(a, b);
-    if (ph->status != NEST_SOLVED) return;  // uniform over the cluster
     const Inst s = load_inst(a, ph, b);
     const int nown = (g.Pcap + cs - 1) / cs;
-    const ResPlan sp = res_plan(g, nown, a.jsplit, a.threads);
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + sp.mbar);
-    uint64_t *rowbar = reinterpret_cast<uint64_t *>(smem + sp.rowbar);   // [nown][Lmax]
-    int64_t *Xs = reinterpret_cast<int64_t *>(smem + sp.X);
-    int64_t *H = reinterpret_cast<int64_t *>(smem + sp.H);
-    uint64_t *Lt = reinterpret_cast<uint64_t *>(smem + sp.Lt);
-    uint64_t *red = reinterpret_cast<uint64_t *>(smem + sp.red);
+    const ResPlan sp = res_plan(g, nown, a.jsplit, a.threads, CT, KT);
+    uint64_t *rowbar = reinterpret_cast<uint64_t *>(sm + sp.rowbar);   // [nown][Lmax]
+    uint64_t *red = reinterpret_cast<uint64_t *>(sm + sp.red);         // [2][jsplit][CT][NTd]
+    V *H = reinterpret_cast<V *>(sm + sp.H);                           // [nown][Lmax][Cmax][Dpad]
+    V *A = reinterpret_cast<V *>(sm + sp.A);                           // [2][nown][Lmax + 1][CT][KT]
+    constexpr V cap = Word<V>::cap, far = Word<V>::far;
 
-    // thread = (js, c, d): d fastest
-    const int NTd = a.threads / (a.jsplit * g.Cmax);
-    const int tid = threadIdx.x, tid_d = tid % NTd, c = (tid / NTd) % g.Cmax, js = tid / (NTd * g.Cmax);
+    // thread = (js, d): d fastest
+    const int NTd = a.threads / a.jsplit;
+    const int tid = threadIdx.x, tid_d = tid % NTd, js = tid / NTd;
     const int d = tid_d + 1;
+    const int jlast = a.jsplit - 1;   // the slice that also takes j = i + 1
     const int64_t spin = a.spin_limit == 0 ? kDefaultSpin : a.spin_limit;
-    const int64_t Hrow = int64_t(g.Cmax) * g.Dpad;   // cells of one resident row
-    const int64_t Hslot = sp.H_slot / 8;
-    const int64_t Lslot = sp.Lt_slot / 8;
-    const int red_stride = NTd * g.Cmax;             // threads of one js slice
-    const uint32_t row_bytes = uint32_t(8 * s.C * (s.Du + 1));   // one pushed row
-
-    int mlim2[CT];   // candidate c' admits width m iff m <= mlim2[c']
+    const uint32_t row_bytes = uint32_t(sizeof(V) * s.C * (s.Du + 1));   // one pushed row
+    const int L = s.L, K = s.K, C = s.C;
+    // widths up to d units
+    int mlog = 0;
+    while (mlog + 1 < K && (2 << mlog) <= d) mlog++;
+    // ... and within the tier of the cell's input link (not for the first stage)
+    int mlink[CT];
 #pragma unroll
-    for (int c2 = 0; c2 < CT; c2++) mlim2[c2] = c2 < s.C ? ph->mlim[c2] : -1;
-    int mlog = 0;    // widths up to d units
-    while (mlog + 1 < s.K && (2 << mlog) <= d) mlog++;
+    for (int c = 0; c < CT; c++) mlink[c] = c < C ? ph->mlim[c] : -1;
+    const int nown_live = rank + 1 > s.P ? 0 : (s.P - rank - 1) / cs + 1;
 
     const int64_t *Xg = reinterpret_cast<const int64_t *>(reinterpret_cast<const unsigned char *>(ph) + a.pl.X);
-    for (int e = tid; e < (s.L + 1) * g.Cmax; e += blockDim.x) Xs[e] = Xg[e];
+    for (int e = tid; e < (L + 1) * g.Cmax; e += blockDim.x) sm[sp.X + e] = Xg[e];
     for (int q = tid; q < nown * g.Lmax; q += blockDim.x) mbar_init(&rowbar[q], 1);
-    const bool any = rank + 1 <= s.P;   // this CTA owns at least one position
-    if (tid == 0) {
-        abort_flag = 0;
-        mbar_init(&mbar[0], 1);
-    }
+    if (tid == 0) abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
     // arm the row barriers this CTA will receive: rows 1 .. L-1 of positions p_k - 1 >= 1
     for (int q = tid; q < nown * g.Lmax; q += blockDim.x) {
         const int k = q / g.Lmax, j = q % g.Lmax;
         const int p = rank + 1 + k * cs;
-        if (p >= 2 && p <= s.P && j >= 1 && j < s.L) mbar_expect_tx(&rowbar[q], row_bytes);
+        if (p >= 2 && p <= s.P && j >= 1 && j < L) mbar_expect_tx(&rowbar[q], row_bytes);
     }
-    if (tid == 0 && any) {
-        // the loads of every owned position, once
-        const uint32_t tbytes = uint32_t(8 * (int64_t(s.L) * (s.L + 1) / 2) * g.Kpad);
-        uint32_t bytes = 0;
-        for (int k = 0; k < nown; k++)
-            if (rank + 1 + k * cs <= s.P) bytes += tbytes;
-        mbar_expect_tx(&mbar[0], bytes);
-        for (int k = 0; k < nown; k++) {
-            const int p = rank + 1 + k * cs;
-            if (p > s.P) continue;
-            bulk_g2s(Lt + int64_t(k) * Lslot, s.loads + int64_t(p - 1) * s.pos_loads, tbytes, &mbar[0]);
-        }
-    }
-    cluster_sync();  // barriers armed and every CTA started: DSMEM pushes may begin
-    bool loads_pending = any;   // the loads copy is in flight until waited for
-    if (any) {
-        if (mbar_wait(&mbar[0], 0, spin))
-            loads_pending = false;
-        else
-            abort_flag = 1;
-    }
-    __syncwarp();
 
-    for (int i = s.L - 1; i >= 0; i--) {
-        const int Pi = s.P < s.L - i ? s.P : s.L - i;
-        const int nc = i == 0 ? 1 : s.C;
-        const bool live = d <= s.Du && c < nc;
-        // widths this cell admits: up to d units and, after the first stage, within its link tier
-        int mcell = mlog;
-        if (i > 0) {
-#pragma unroll
-            for (int c2 = 0; c2 < CT; c2++)
-                if (c2 == c && mlim2[c2] < mcell) mcell = mlim2[c2];
+    // A rows of step i: entries (slot k, cut point j = i + 1 .. L, width m)
+    auto a_entries = [&](int i) { return nown_live * (L - i) * K; };
+    auto a_load = [&](int i, int e) -> uint64_t {
+        const int per = (L - i) * K;
+        const int k = e / per, r = e % per;
+        const int p = rank + 1 + k * cs;
+        return s.loads[int64_t(p - 1) * s.pos_loads + (row_offset(i, L) + r / K) * g.Kpad + r % K];
+    };
+    auto a_store = [&](int i, int e, uint64_t lw) {
+        const int per = (L - i) * K;
+        const int k = e / per, r = e % per;
+        const int j = i + 1 + r / K, m = r % K;
+        V *at = A + (i & 1) * sp.Abuf + k * sp.Aslot + j * sp.Aj + m;
+        for (int c2 = 0; c2 < C; c2++) {
+            V v = far;
+            if (lw != kInf && (j == L || m <= ph->mlim[c2])) v = V(lw >> 16) + V(sm[sp.X + j * g.Cmax + c2]);
+            at[c2 * KT] = v;
         }
-        const int64_t pair0 = row_offset(i, s.L);   // pair (i, j) = pair0 + j - i - 1
-        for (int k = 0; k < nown; k++) {
+    };
+    for (int e = tid; e < a_entries(L - 1); e += blockDim.x) a_store(L - 1, e, a_load(L - 1, e));
+    cluster_sync();  // first A rows built, barriers armed, every CTA started: pushes may begin
+
+    int rb = 0;   // red buffer in use
+    for (int i = L - 1; i >= 0; i--) {
+        const int Pi = s.P < L - i ? s.P : L - i;
+        const int nc = i == 0 ? 1 : C;
+        const bool dlive = d <= s.Du;
+        int mtop[CT], mall = -1;
+        V xf[CT];
+#pragma unroll
+        for (int c = 0; c < CT; c++) {
+            const int mt = i > 0 && mlink[c] < mlog ? mlink[c] : mlog;
+            mtop[c] = dlive && c < nc ? mt : -1;
+            mall = mtop[c] > mall ? mtop[c] : mall;
+            xf[c] = c < nc ? V(sm[sp.X + i * g.Cmax + c]) : V(0);
+        }
+        // the loads of step i - 1, fetched now and stored after the relaxation
+        const int n_next = i > 0 ? a_entries(i - 1) : 0;
+        const uint64_t pre = tid < n_next ? a_load(i - 1, tid) : 0;
+        for (int k = 0; k < nown_live; k++) {
             const int p = rank + 1 + k * cs;
-            if (p > s.P) break;
-            const uint64_t *lt = Lt + int64_t(k) * Lslot + (pair0 - i - 1) * g.Kpad;   // + j * Kpad
-            Cell cl;
-            cl.init(live ? Xs[int64_t(i) * g.Cmax + c] : 0);
-            if (p >= 2 && p <= Pi) {
-                // rows i+1 .. L-1 of position p - 1 must have arrived (bounded waits).  Position
-                // p first relaxes at step i = L - p and then needs all of them; at every later
-                // step only row i + 1 is new.
-                const int jtop = p == s.L - i ? s.L - 1 : i + 1;
-                for (int j = jtop; j > i; j--) {
-                    if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + j], 0, spin)) abort_flag = 1;
-                }
-                __syncwarp();
+            V bv[CT], bvx[CT];   // the cell's best value, bv - X[i][c]
+            uint32_t bi[CT];
+#pragma unroll
+            for (int c = 0; c < CT; c++) {
+                bv[c] = cap;
+                bvx[c] = cap - xf[c];
+                bi[c] = kNoArg;
             }
-            if (live && !abort_flag && p <= Pi) {
-                if (p == 1) {
-                    if (js == 0) cl.last(s.L, mcell, lt + int64_t(s.L) * g.Kpad);
-                } else {
-                    const int64_t *Hk = H + int64_t(k) * Hslot;
-                    for (int j = i + 1 + js; j < s.L; j += a.jsplit)
-                        cl.relax<CT>(j, d, mcell, s.C, mlim2, lt + int64_t(j) * g.Kpad, Xs + int64_t(j) * g.Cmax,
-                                     Hk + int64_t(j) * Hrow, g.Dpad);
+            const V *Ak = A + (i & 1) * sp.Abuf + k * sp.Aslot;
+            const V *Hk = H + k * sp.Hslot + d;
+            if (p == 1) {
+                if (js == 0) {   // the last stage [i, L): A[L][0][m] = load*(i, L, m, 1)
+#pragma unroll
+                    for (int m = 0; m < KT; m++) {
+                        if (m > mall) break;
+                        const V a0 = Ak[L * sp.Aj + m];
+#pragma unroll
+                        for (int c = 0; c < CT; c++) {
+                            if (m <= mtop[c] && a0 < bvx[c]) {
+                                bv[c] = a0 + xf[c];
+                                bvx[c] = a0;
+                                bi[c] = (uint32_t(L) << 8) | (uint32_t(m) << 4);
+                            }
+                        }
+                    }
+                }
+            } else if (p <= Pi) {
+                // position p first relaxes at step i = L - p: rows i + 2 .. L - 1 of
+                // position p - 1 arrived during earlier steps but were not waited for yet
+                if (p == L - i) {
+                    for (int j = L - 1; j >= i + 2; j--)
+                        if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + j], 0, spin)) abort_flag = 1;
+                    __syncwarp();
+                }
+                if (!abort_flag)
+                    for (int j = i + 2 + js; j < L; j += a.jsplit)
+                        relax_cut<CT, KT, V>(Ak + j * sp.Aj, Hk + j * sp.Hrow, g.Dpad, C, j, mall, mtop, bv, bvx, bi,
+                                             xf);
+                if (js == jlast) {
+                    // row i + 1 is the one the neighbour pushed last (bounded wait)
+                    if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + i + 1], 0, spin)) abort_flag = 1;
+                    __syncwarp();
+                    if (!abort_flag) {
+                        // j = i + 1 is the smallest cut point: it wins ties, so compare
+                        // against bv + 1 until it has improved a cell
+#pragma unroll
+                        for (int c = 0; c < CT; c++)
+                            if (bv[c] < cap) {
+                                bv[c] += 1;
+                                bvx[c] += 1;
+                            }
+                        relax_cut<CT, KT, V>(Ak + (i + 1) * sp.Aj, Hk + (i + 1) * sp.Hrow, g.Dpad, C, i + 1, mall,
+                                             mtop, bv, bvx, bi, xf);
+#pragma unroll
+                        for (int c = 0; c < CT; c++)
+                            if (bi[c] != kNoArg && int(bi[c] >> 8) != i + 1) {   // bumped and not improved
+                                bv[c] -= 1;
+                                bvx[c] -= 1;
+                            }
+                    }
                 }
             }
-            uint64_t key = live ? cl.key() : kInf;
-            if (a.jsplit > 1) {
-                red[tid] = key;
-                __syncthreads();
-                if (js == 0)
-                    for (int q = 1; q < a.jsplit; q++) {
-                        const uint64_t o = red[tid + q * red_stride];
+            // combine the slices: red[rb][js][c][d]
+            uint64_t *rr = red + rb * (a.threads * CT);
+#pragma unroll
+            for (int c = 0; c < CT; c++)
+                rr[(js * CT + c) * NTd + tid_d] = bv[c] < cap ? (uint64_t(bv[c]) << 24) | bi[c] : kInf;
+            __syncthreads();
+            rb ^= 1;
+            // slice js finishes the cells c = js, js + jsplit, ..
+            for (int c = js; c < C; c += a.jsplit) {
+                uint64_t key = kInf;
+                if (c < nc && !abort_flag)
+                    for (int q = 0; q < a.jsplit; q++) {
+                        const uint64_t o = rr[(q * CT + c) * NTd + tid_d];
                         key = o < key ? o : key;
                     }
-                __syncthreads();
-            }
-            if (js == 0 && c < s.C) {
                 // the owner of position p + 1 keeps row i of position p in its slot p / cs
                 const bool push = p < s.P && i > 0;
                 const uint32_t crank = uint32_t(p % cs);
-                const int64_t *dst = H + int64_t(p / cs) * Hslot + int64_t(i) * Hrow + int64_t(c) * g.Dpad;
+                const V *dst = H + (p / cs) * sp.Hslot + i * sp.Hrow + c * g.Dpad;
                 const uint32_t bar = push ? cluster_map(&rowbar[(p / cs) * g.Lmax + i], crank) : 0;
-                if (d <= s.Du) {
+                if (dlive) {
                     write_cell(s, g.Dpad, p, i, c, d, key);
-                    if (push) st_async_remote(cluster_map(dst + d, crank), int64_t(key >> 24), bar);
+                    if (push) st_async_remote(cluster_map(dst + d, crank), key == kInf ? cap : V(key >> 24), bar);
                 }
                 if (tid_d == 0) {
                     write_cell(s, g.Dpad, p, i, c, 0, kInf);
-                    if (push) st_async_remote(cluster_map(dst, crank), kCap, bar);
+                    if (push) st_async_remote(cluster_map(dst, crank), cap, bar);
                 }
             }
         }
+        // the A rows of step i - 1, into the other buffer (last read at step i + 1)
+        if (tid < n_next) a_store(i - 1, tid, pre);
+        for (int e = tid + blockDim.x; e < n_next; e += blockDim.x) a_store(i - 1, e, a_load(i - 1, e));
+        __syncthreads();
     }
     // every row pushed to this CTA has landed before it may exit (bounded waits)
     if (tid == 0) {
         for (int k = 0; k < nown; k++) {
             const int p = rank + 1 + k * cs;
             if (p < 2 || p > s.P) continue;
-            for (int j = 1; j < s.L; j++) mbar_wait(&rowbar[k * g.Lmax + j], 0, kDefaultSpin);
+            for (int j = 1; j < L; j++) mbar_wait(&rowbar[k * g.Lmax + j], 0, kDefaultSpin);
         }
-        if (loads_pending) mbar_wait(&mbar[0], 0, kDefaultSpin);
     }
     cluster_sync();
     if (tid == 0 && abort_flag) ph->status = NEST_TIMED_OUT;
+}
+
+template <int CT, int KT>
+__global__ void __launch_bounds__(kMaxThreads, CT == 2 ? 3 : 2) sweep_resident_kernel(PassArgs a) {
+    extern __shared__ __align__(128) int64_t sm[];
+    __shared__ volatile int abort_flag;
+    const int b = blockIdx.x / a.cluster;
+    const int rank = int(cluster_rank());
+    PrepHdr *ph = prep_hdr(a, b);
+    if (ph->status != NEST_SOLVED) return;  // uniform over the cluster
+    // the word width is uniform over the cluster too: every CTA reads the same header
+    if (narrow_words(ph))
+        resident_body<CT, KT, uint32_t>(a, ph, b, rank, sm, abort_flag);
+    else
+        resident_body<CT, KT, int64_t>(a, ph, b, rank, sm, abort_flag);
 }
 
 // ---------------------------------------------------------------------------------
@@ -718,34 +780,54 @@ int launch_cluster(Kern fn, const PassArgs &a, void *stream, size_t smem, const 
     return cuda_status(cudaLaunchKernelEx(&cfg, fn, a), what);
 }
 
-// Clusters of the resident kernel that can be resident at once (0 if it cannot launch).
-template <int CT>
+// The resident variant is instantiated for up to 4 candidates and KT = 4, 8 or 16 widths.
+inline int kt_of(int Kmax) { return Kmax <= 4 ? 4 : Kmax <= 8 ? 8 : 16; }
+inline int ct_of(int Cmax) { return Cmax <= 1 ? 1 : Cmax <= 2 ? 2 : 4; }
+
+template <int CT, int KT>
 int resident_capacity(int cluster, int threads, size_t smem) {
-    if (set_attributes(sweep_resident_kernel<CT>, smem, cluster, "resident occupancy") != NEST_OK) return 0;
+    if (set_attributes(sweep_resident_kernel<CT, KT>, smem, cluster, "resident occupancy") != NEST_OK) return 0;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = cluster_config(1, cluster, threads, smem, nullptr, attr);
     int num = 0;
-    if (cudaOccupancyMaxActiveClusters(&num, sweep_resident_kernel<CT>, &cfg) != cudaSuccess) {
-        cudaGetLastError();   // clear the sticky-free error of an unsupported shape
+    if (cudaOccupancyMaxActiveClusters(&num, sweep_resident_kernel<CT, KT>, &cfg) != cudaSuccess) {
+        cudaGetLastError();   // clear the error of an unsupported shape
         return 0;
     }
     return num;
 }
 
-int resident_capacity_ct(int Cmax, int cluster, int threads, size_t smem) {
-    if (Cmax <= 1) return resident_capacity<1>(cluster, threads, smem);
-    if (Cmax <= 2) return resident_capacity<2>(cluster, threads, smem);
-    if (Cmax <= 4) return resident_capacity<4>(cluster, threads, smem);
-    if (Cmax <= 8) return resident_capacity<8>(cluster, threads, smem);
-    return resident_capacity<16>(cluster, threads, smem);
+template <int CT>
+int resident_capacity_kt(int KT, int cluster, int threads, size_t smem) {
+    if (KT == 4) return resident_capacity<CT, 4>(cluster, threads, smem);
+    if (KT == 8) return resident_capacity<CT, 8>(cluster, threads, smem);
+    return resident_capacity<CT, 16>(cluster, threads, smem);
+}
+
+int resident_capacity_ct(const Geo &g, int cluster, int threads, size_t smem) {
+    const int KT = kt_of(g.Kmax), CT = ct_of(g.Cmax);
+    if (g.Cmax > 4) return 0;
+    if (CT == 1) return resident_capacity_kt<1>(KT, cluster, threads, smem);
+    if (CT == 2) return resident_capacity_kt<2>(KT, cluster, threads, smem);
+    return resident_capacity_kt<4>(KT, cluster, threads, smem);
+}
+
+template <int CT, int KT>
+int launch_resident(const PassArgs &a, void *stream) {
+    const size_t smem = size_t(sweep_resident_smem_bytes(a.g, a.cluster, a.jsplit, a.threads));
+    return launch_cluster(sweep_resident_kernel<CT, KT>, a, stream, smem, "sweep (resident) launch");
+}
+
+template <int CT>
+int launch_resident_kt(const PassArgs &a, void *stream) {
+    const int KT = kt_of(a.g.Kmax);
+    if (KT == 4) return launch_resident<CT, 4>(a, stream);
+    if (KT == 8) return launch_resident<CT, 8>(a, stream);
+    return launch_resident<CT, 16>(a, stream);
 }
 
 template <int CT>
 int launch_ct(const PassArgs &a, void *stream) {
-    if (a.resident) {
-        const size_t smem = size_t(sweep_resident_smem_bytes(a.g, a.cluster, a.jsplit, a.threads));
-        return launch_cluster(sweep_resident_kernel<CT>, a, stream, smem, "sweep (resident) launch");
-    }
     const size_t smem = size_t(sweep_smem_bytes(a.g, a.jc, a.jsplit, a.threads));
     return launch_cluster(sweep_stream_kernel<CT>, a, stream, smem, "sweep (streaming) launch");
 }
@@ -758,7 +840,7 @@ int64_t sweep_smem_bytes(const Geo &g, int jc, int jsplit, int threads) {
 
 int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads) {
     const int nown = (g.Pcap + cluster - 1) / cluster;
-    return res_plan(g, nown, jsplit, threads).total;
+    return 8 * int64_t(res_plan(g, nown, jsplit, threads, ct_of(g.Cmax), kt_of(g.Kmax)).total);
 }
 
 int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int variant, SweepConfig &out) {
@@ -773,10 +855,11 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
     if ((cluster_opt && !ok_cluster(cluster_opt)) || (jsplit_opt && !ok_jsplit(jsplit_opt))) return NEST_E_INVALID;
     const int NTd = (g.Dumax + 31) / 32 * 32;
 
-    // resident: one thread per (slice, candidate, device count); every instance's
-    // cluster resident at once if possible, then the least work per thread and step
-    if (variant != 2) {
-        const int base = g.Cmax * NTd;
+    // resident: one thread per (slice, device count) holding every candidate; every
+    // instance's cluster resident at once if possible, then the least work per thread
+    // and step
+    if (variant != 2 && g.Cmax <= 4) {
+        const int base = NTd;
         double best = 0;
         SweepConfig pick = {};
         const int cl_list[5] = {16, 8, 4, 2, 1};
@@ -790,7 +873,7 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
                 if (threads > kMaxThreads) continue;
                 const int64_t smem = sweep_resident_smem_bytes(g, cs, js, threads);
                 if (smem > budget) continue;
-                const int cap = resident_capacity_ct(g.Cmax, cs, threads, size_t(smem));
+                const int cap = resident_capacity_ct(g, cs, threads, size_t(smem));
                 if (std::getenv("NEST_DEBUG"))
                     std::fprintf(stderr, "nest: resident sweep cluster %d jsplit %d threads %d smem %lld: %d clusters at once\n",
                                  cs, js, threads, (long long)smem, cap);
@@ -838,6 +921,11 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
 }
 
 int launch_sweep(const PassArgs &a, void *stream) {
+    if (a.resident) {
+        if (a.g.Cmax <= 1) return launch_resident_kt<1>(a, stream);
+        if (a.g.Cmax <= 2) return launch_resident_kt<2>(a, stream);
+        return launch_resident_kt<4>(a, stream);
+    }
     if (a.g.Cmax <= 1) return launch_ct<1>(a, stream);
     if (a.g.Cmax <= 2) return launch_ct<2>(a, stream);
     if (a.g.Cmax <= 4) return launch_ct<4>(a, stream);

@@ -76,6 +76,24 @@ def oracle_many(instances, fn=O.solve, threads=None):
         return list(ex.map(fn, instances))
 
 
+def narrow_words(inst):
+    """Whether the resident sweep takes its 32-bit value words for this instance: the
+    largest finite per-position load plus twice the largest link cost is below 2^30."""
+    lo = O.loads(inst)
+    fin = lo[lo != np.uint64(2**64 - 1)]
+    ml = int((fin >> U64(16)).max()) if fin.size else 0
+    mx = int(np.max(O.links(inst)))
+    return min(ml, 2**31 - 1) + 2 * min(mx, 2**31 - 1) < 2**30
+
+
+def scaled(inst, factor):
+    """The same instance with every layer's flops multiplied by `factor`."""
+    import copy
+    y = copy.deepcopy(inst)
+    y.fl = y.fl * factor
+    return y
+
+
 def same_result(g, o):
     return (g["status"] == o["status"] and g["t_batch"] == o["t_batch"] and
             (g["status"] != 0 or (g["bottleneck"] == o["bottleneck"] and g["plan"] == o["plan"])))

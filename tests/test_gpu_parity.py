@@ -42,15 +42,15 @@ def test_workload1_all_tables(variant):
 
 
 # (CTAs per instance, threads per cell, sweep variant: 0 auto, 1 resident, 2 streaming)
-SWEEP_CONFIGS = [(0, 0, 0), (1, 1, 2), (2, 2, 2), (4, 4, 2), (4, 2, 2), (8, 4, 1), (8, 1, 2), (8, 2, 1),
-                 (16, 4, 1), (16, 8, 2), (16, 1, 1), (16, 2, 1)]
+SWEEP_CONFIGS = [(0, 0, 0), (1, 1, 2), (2, 2, 2), (4, 4, 2), (4, 4, 1), (4, 2, 2), (8, 4, 1), (8, 1, 2),
+                 (8, 2, 1), (16, 4, 1), (16, 8, 2), (16, 1, 1), (16, 2, 1)]
 
 
 def test_resident_variant_rejected_when_it_does_not_fit():
-    # 4 CTAs per instance would hold 4 positions' rows and loads: about 270 KB per CTA
+    # 2 CTAs per instance would hold the rows of 8 positions each: about 270 KB per CTA
     insts = synth.config_batch(2, B=2)
     with pytest.raises(nest.NestError) as e:
-        G.run(insts, cluster=4, jsplit=4, variant=1)
+        G.run(insts, cluster=2, jsplit=4, variant=1)
     assert e.value.rc == nest.NEST_E_LIMITS
 
 
@@ -62,6 +62,31 @@ def test_workload2_all_tables(cluster, jsplit, variant):
     for b in range(len(insts)):
         assert G.same_result(res[b], oracle[b]), b
     for b in (0, 7, 15):
+        check_tables(s, b, insts[b])
+
+
+# The resident sweep keeps 32-bit value words when every value is small and 64-bit
+# words otherwise; flops scaled by 64 push workload 2's loads past 2^30.
+@pytest.mark.parametrize("cluster,jsplit,variant", [(0, 0, 1), (16, 8, 1), (8, 4, 1), (4, 2, 1), (0, 0, 2)])
+def test_workload2_wide_words(cluster, jsplit, variant):
+    insts = [G.scaled(x, 64) for x in synth.config_batch(2, B=4)]
+    assert not any(G.narrow_words(x) for x in insts)
+    s, res = G.run(insts, cluster=cluster, jsplit=jsplit, variant=variant)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+        check_tables(s, b, insts[b])
+
+
+def test_mixed_word_widths_in_one_launch():
+    insts = synth.config_batch(2, B=6)
+    for b in (1, 3, 4):
+        insts[b] = G.scaled(insts[b], 64)
+    assert [G.narrow_words(x) for x in insts] == [True, False, True, False, False, True]
+    s, res = G.run(insts, variant=1)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
         check_tables(s, b, insts[b])
 
 
@@ -99,9 +124,11 @@ def test_workload5_full_size_sampled():
     np.testing.assert_array_equal(G.cost_table(s, 1023 - last0, insts[1023]), O.cost_tensor(insts[1023]))
 
 
-@pytest.mark.parametrize("part,variant", [(0, 0), (1, 1), (2, 2), (3, 1)])
-def test_random_tiny_batches(part, variant):
-    insts = [synth.random_tiny(1000 * part + k, Lmax=7, Dmax=16) for k in range(300)]
+@pytest.mark.parametrize("part,variant,factor", [(0, 0, 1), (1, 1, 1), (2, 2, 1), (3, 1, 1), (4, 1, 1 << 20)])
+def test_random_tiny_batches(part, variant, factor):
+    insts = [G.scaled(synth.random_tiny(1000 * part + k, Lmax=7, Dmax=16), factor) for k in range(300)]
+    if factor > 1:   # most take the 64-bit words of the resident sweep, some the 32-bit ones
+        assert 0 < sum(G.narrow_words(x) for x in insts) < 100
     s, res = G.run(insts, Pcap=6, variant=variant)
     oracle = G.oracle_many(insts)
     for b in range(len(insts)):
