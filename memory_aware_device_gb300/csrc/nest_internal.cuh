@@ -26,7 +26,7 @@ struct Geo {
     int32_t Kmax;  // widths unit * 2^m, m < Kmax
     int32_t Kpad;  // Kmax rounded up to even (16-byte rows)
     int32_t Spad;  // Smax rounded up to even
-    int32_t Dpad;  // Dumax + 1 rounded up to even
+    int32_t Dpad;  // Dumax + 1 rounded up to a multiple of 4 (rows of 16-byte multiples)
 };
 
 inline bool make_geo(const nest_dims &d, Geo &g) {
@@ -47,7 +47,7 @@ inline bool make_geo(const nest_dims &d, Geo &g) {
     g.Kmax = K;
     g.Kpad = (K + 1) & ~1;
     g.Spad = (d.Smax + 1) & ~1;
-    g.Dpad = (d.Dumax + 2) & ~1;
+    g.Dpad = (d.Dumax + 4) & ~3;
     return true;
 }
 

@@ -32,6 +32,7 @@
 // cluster barrier.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 
@@ -78,6 +79,20 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
+
+// Bulk copy shared -> global, tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The sources of every committed group have been read (they may be overwritten).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every committed group has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Bounded wait for the given phase of an mbarrier.  Each poll is a try_wait that
 // suspends the warp in hardware for up to kSuspendNs while the phase is incomplete,
@@ -295,14 +310,36 @@ __device__ __forceinline__ bool narrow_words(const PrepHdr *ph) {
     return uint64_t(ph->maxload32) + 2 * uint64_t(ph->maxX32) < (uint64_t(1) << 30);
 }
 
-// Shared-memory plan of the resident variant, in 8-byte words (sized for 64-bit
-// values; 32-bit values use the first half of the H and A regions).
+// Shared-memory plan of the resident variant, in 8-byte words.
+//  - H[slot][j][c'][Hpad + x] = v(dp[j][x][p-1][c']).  With 32-bit values Hpad values
+//    of `cap` precede x = 0, so a width 2^m above a lane's d reads cap instead of
+//    needing a test; 64-bit values (Hpad = 0) clamp x at the cap column 0 instead.
+//    The lanes of a warp read different cut points j, so the row stride Hrow is chosen
+//    with Hrow = dpw / s (mod 32 / s) for values of s 4-byte words and dpw device
+//    counts per warp: those reads land in different banks.
+//  - A[buf][slot][j][c][c'][m] = load*(i, j, m, p) + X[i][c] + X[j][c'] when both
+//    links admit the width, else `far`; A[j] holds an odd number of values (banks).
+//  - staged dp rows [2][slot][Cmax][Dpad] (int64 values, uint32 arguments).
+// The H region is sized for whichever word width needs more.
 struct ResPlan {
-    int rowbar, X, H, A, red, total;   // word offsets; total = words
-    int Hslot, Hrow, Aj, Aslot, Abuf;  // strides in values
+    int rowbar, X, H, A, sdv, sda, total;  // word offsets; total = words
+    int Hpad, Hcol, Hrow, Hslot;           // H strides in values of the chosen width
+    int Aj, Aslot, Abuf;                   // A strides in values
+    int Srow;                              // values per staged dp row: Cmax * Dpad
 };
 
-__host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, int threads, int CT, int KT) {
+__host__ __device__ inline int res_hpad(const Geo &g, int vbytes) {
+    return vbytes == 4 ? ((1 << (g.Kmax - 1)) + 3) & ~3 : 0;
+}
+
+__host__ __device__ inline int res_hrow(const Geo &g, int jsplit, int vbytes) {
+    const int s = vbytes / 4, mod = 32 / s, want = (32 / jsplit / s) % mod;
+    int h = g.Cmax * (res_hpad(g, vbytes) + g.Dpad);
+    while (h % mod != want) h++;
+    return h;
+}
+
+__host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, int CT, int KT, int vbytes) {
     ResPlan s;
     auto up = [](int w) { return (w + 15) / 16 * 16; };   // 128-byte alignment
     int off = 0;
@@ -310,46 +347,73 @@ __host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, 
     off = up(off + nown * g.Lmax);
     s.X = off;
     off = up(off + (g.Lmax + 1) * g.Cmax);
-    s.Hrow = g.Cmax * g.Dpad;
+    s.Hpad = res_hpad(g, vbytes);
+    s.Hcol = s.Hpad + g.Dpad;
+    s.Hrow = res_hrow(g, jsplit, vbytes);
     s.Hslot = g.Lmax * s.Hrow;
+    const int h4 = (nown * g.Lmax * res_hrow(g, jsplit, 4) + 1) / 2, h8 = nown * g.Lmax * res_hrow(g, jsplit, 8);
     s.H = off;
-    off = up(off + nown * s.Hslot);
-    s.Aj = CT * KT;                                       // A[j][c'][m]
+    off = up(off + (h4 > h8 ? h4 : h8));
+    s.Aj = CT * CT * KT + 1;
     s.Aslot = (g.Lmax + 1) * s.Aj;
     s.Abuf = nown * s.Aslot;
     s.A = off;
     off = up(off + 2 * s.Abuf);
-    s.red = off;
-    off = up(off + 2 * threads * CT);                     // slice minima, two buffers
+    s.Srow = g.Cmax * g.Dpad;
+    s.sdv = off;
+    off = up(off + 2 * nown * s.Srow);
+    s.sda = off;
+    off = up(off + nown * s.Srow);
     s.total = off;
     return s;
 }
 
-// Relaxation of one cut point j for the cells (c, d) of one thread, c < CT: for every
-// width m <= mall and next-link candidate c' the candidate is
-// v = max(A[j][c'][m] + X[i][c], v(dp[j][d - 2^m][p-1][c'])).  A and the dp value are
-// read once and tried against every cell of the thread.  Widths are visited in the
-// canonical order (m, c'), so the first strict improvement is the smallest key.
-template <int CT, int KT, typename V>
-__device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Dpad, int C, int j, int mall, const int *mtop,
-                                          V *bv, V *bvx, uint32_t *bi, const V *xf) {
+// Relaxation of one cut point j for the cells (c, d) of one thread: for every width
+// m <= mw and next-link candidate c' the candidate is v = max(A[j][c][c'][m],
+// v(dp[j][d - 2^m][p-1][c'])), tried against the running best of cell c.  Excluded
+// widths read far or cap and never improve.  With NA = CT each c' has its own running
+// best, visited in (c', m) order and merged by key afterwards (independent dependency
+// chains); with NA = 1 one running best per cell is visited in the canonical (m, c')
+// order.  Either way the first strict improvement within a running best is its
+// smallest key.  `mw` is the widest width any lane of the warp admits (uniform).
+template <int CT, int KT, int NA, typename V>
+__device__ __forceinline__ void relax_one(const V *Aj, const V *Hj, int Hcol, int d, uint32_t jarg, int m, int c2,
+                                          int a_, V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+    constexpr bool kPad = sizeof(V) == 4;   // rows padded with cap below x = 0
+    const int x = kPad ? d - (1 << m) : (d - (1 << m) > 0 ? d - (1 << m) : 0);
+    const V nv = Hj[c2 * Hcol + x];
+    const uint32_t idx = jarg | (uint32_t(m) << 4) | uint32_t(c2);
 #pragma unroll
-    for (int m = 0; m < KT; m++) {
-        if (m > mall) break;
+    for (int c = 0; c < CT; c++) {
+        const V av = Aj[(c * CT + c2) * KT + m];
+        const V v = av > nv ? av : nv;
+        const bool take = v < bv[c][a_];
+        bv[c][a_] = take ? v : bv[c][a_];
+        bi[c][a_] = take ? idx : bi[c][a_];
+    }
+}
+
+template <int CT, int KT, int NA, typename V>
+__device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, int d, int C, uint32_t jarg, int mw,
+                                          V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+    if constexpr (NA > 1) {
 #pragma unroll
         for (int c2 = 0; c2 < CT; c2++) {
             if (c2 >= C) break;
-            const V av = Aj[c2 * KT + m];
-            const V nv = Hj[c2 * Dpad - (1 << m)];
-            const uint32_t idx = (uint32_t(j) << 8) | (uint32_t(m) << 4) | uint32_t(c2);
 #pragma unroll
-            for (int c = 0; c < CT; c++) {
-                if (m <= mtop[c] && av < bvx[c] && nv < bv[c]) {
-                    const V ax = av + xf[c];
-                    bv[c] = ax > nv ? ax : nv;
-                    bvx[c] = bv[c] - xf[c];
-                    bi[c] = idx;
-                }
+            for (int m = 0; m < KT; m++) {
+                if (m > mw) break;
+                relax_one<CT, KT, NA, V>(Aj, Hj, Hcol, d, jarg, m, c2, c2, bv, bi);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < KT; m++) {
+            if (m > mw) break;
+#pragma unroll
+            for (int c2 = 0; c2 < CT; c2++) {
+                if (c2 >= C) break;
+                relax_one<CT, KT, NA, V>(Aj, Hj, Hcol, d, jarg, m, c2, 0, bv, bi);
             }
         }
     }
@@ -361,52 +425,76 @@ __device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Dpad, in
 //    row's own mbarrier, so a CTA waits only for the rows it reads and the CTAs of
 //    a cluster form a pipeline over positions instead of moving in lockstep.
 //  - At step i only row i + 1 of a slot is new: the cut points j >= i + 2 are relaxed
-//    first, and the wait for row i + 1 comes after them, so the neighbour's push
-//    overlaps this CTA's own work.  The slice that takes j = i + 1 adds it last, with
-//    ties going to it (its key is the smaller one).
-//  - For step i it reads A[j][c'][m] = load*(i, j, m, p_k) + X[j][c'], with the
-//    outgoing link's width rule and the empty loads folded in as `far`; the rows of
-//    step i - 1 are built during step i into the other buffer (their global loads
-//    are issued before the relaxation, so their latency is hidden).
+//    first, and j = i + 1 is the final item of the last slice, after a bounded wait
+//    for its row, so the neighbour's push overlaps this CTA's own work.  It wins ties
+//    (its key is the smaller one).
+//  - The A rows of step i - 1 are built during step i into the other buffer (their
+//    global loads are issued before the relaxation, so their latency is hidden).
 //  - A thread owns one device count d, every candidate c of it, and a slice of the
-//    cut points j; the jsplit slices are combined through a double-buffered shared
-//    array, one barrier per slot.
+//    cut points j.  The jsplit slices of one d are adjacent lanes of a warp and are
+//    combined with shuffles, so a warp covers 32 / jsplit consecutive device counts
+//    and a step has a single CTA barrier.
+//  - Each step's dp rows are staged in shared memory and written to global memory
+//    (for the backtrack) by bulk copies.
 // The footprint is kept small so that the clusters of a whole batch are resident at
-// once.  dp is also written to global memory (64-bit) for the backtrack.
+// once.
 template <int CT, int KT, typename V>
 __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
                                               volatile int &abort_flag) {
+    constexpr int NA = CT <= 2 ? CT : 1;   // running bests per cell
     const Geo &g = a.g;
     const int cs = a.cluster;
     const Inst s = load_inst(a, ph, b);
     const int nown = (g.Pcap + cs - 1) / cs;
-    const ResPlan sp = res_plan(g, nown, a.jsplit, a.threads, CT, KT);
+    const ResPlan sp = res_plan(g, nown, a.jsplit, CT, KT, int(sizeof(V)));
     uint64_t *rowbar = reinterpret_cast<uint64_t *>(sm + sp.rowbar);   // [nown][Lmax]
-    uint64_t *red = reinterpret_cast<uint64_t *>(sm + sp.red);         // [2][jsplit][CT][NTd]
-    V *H = reinterpret_cast<V *>(sm + sp.H);                           // [nown][Lmax][Cmax][Dpad]
-    V *A = reinterpret_cast<V *>(sm + sp.A);                           // [2][nown][Lmax + 1][CT][KT]
+    V *H = reinterpret_cast<V *>(sm + sp.H);
+    V *A = reinterpret_cast<V *>(sm + sp.A);
+    int64_t *sdv = sm + sp.sdv;
+    uint32_t *sda = reinterpret_cast<uint32_t *>(sm + sp.sda);
     constexpr V cap = Word<V>::cap, far = Word<V>::far;
 
-    // thread = (js, d): d fastest
-    const int NTd = a.threads / a.jsplit;
-    const int tid = threadIdx.x, tid_d = tid % NTd, js = tid / NTd;
-    const int d = tid_d + 1;
-    const int jlast = a.jsplit - 1;   // the slice that also takes j = i + 1
+    // thread = (device count d, slice js), slices in adjacent lanes
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int jsplit = a.jsplit, lgs = __ffs(jsplit) - 1;
+    const int js = lane & (jsplit - 1);
+    const int d = (tid >> 5) * (32 >> lgs) + (lane >> lgs) + 1;
+    const int jlast = jsplit - 1;   // the slice that also takes j = i + 1
     const int64_t spin = a.spin_limit == 0 ? kDefaultSpin : a.spin_limit;
     const uint32_t row_bytes = uint32_t(sizeof(V) * s.C * (s.Du + 1));   // one pushed row
     const int L = s.L, K = s.K, C = s.C;
-    // widths up to d units
+    const bool dlive = d <= s.Du;
+    // the warp's widest width: up to d units and, after the first stage, within the
+    // widest input-link tier (narrower limits are folded into A and the H padding)
     int mlog = 0;
     while (mlog + 1 < K && (2 << mlog) <= d) mlog++;
-    // ... and within the tier of the cell's input link (not for the first stage)
-    int mlink[CT];
+    int mlink[CT], mall_n = -1;
 #pragma unroll
-    for (int c = 0; c < CT; c++) mlink[c] = c < C ? ph->mlim[c] : -1;
+    for (int c = 0; c < CT; c++) {
+        mlink[c] = c < C ? ph->mlim[c] : -1;
+        const int mt = dlive && c < C ? (mlink[c] < mlog ? mlink[c] : mlog) : -1;
+        mall_n = mt > mall_n ? mt : mall_n;
+    }
+    const int mw_n = __reduce_max_sync(0xFFFFFFFFu, mall_n);
+    const int mw_0 = __reduce_max_sync(0xFFFFFFFFu, dlive ? mlog : -1);
     const int nown_live = rank + 1 > s.P ? 0 : (s.P - rank - 1) / cs + 1;
+
+    // A entries (slot k, cut point j = i + 1 + r, width m) at e = (k * Lmax + r) * K + m:
+    // a fixed numbering, so a thread's first entry is decoded once
+    const int a_total = nown_live * g.Lmax * K;
+    const int a_m = tid % K, a_r = (tid / K) % g.Lmax, a_k = tid / (K * g.Lmax);
+    const bool a_have = tid < a_total;
+    const uint64_t *a_src = s.loads + int64_t(a_have ? rank + a_k * cs : 0) * s.pos_loads + int64_t(a_r) * g.Kpad + a_m;
+    V *a_dst = A + a_k * sp.Aslot + a_r * sp.Aj + a_m;
 
     const int64_t *Xg = reinterpret_cast<const int64_t *>(reinterpret_cast<const unsigned char *>(ph) + a.pl.X);
     for (int e = tid; e < (L + 1) * g.Cmax; e += blockDim.x) sm[sp.X + e] = Xg[e];
     for (int q = tid; q < nown * g.Lmax; q += blockDim.x) mbar_init(&rowbar[q], 1);
+    // the padding in front of every row: cap (never written again)
+    for (int e = tid; e < nown * g.Lmax * g.Cmax * sp.Hpad; e += blockDim.x) {
+        const int row = e / sp.Hpad;   // (slot, j, c') in order
+        H[(row / g.Cmax) * sp.Hrow + (row % g.Cmax) * sp.Hcol + e % sp.Hpad] = cap;
+    }
     if (tid == 0) abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
@@ -417,144 +505,168 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         if (p >= 2 && p <= s.P && j >= 1 && j < L) mbar_expect_tx(&rowbar[q], row_bytes);
     }
 
-    // A rows of step i: entries (slot k, cut point j = i + 1 .. L, width m)
-    auto a_entries = [&](int i) { return nown_live * (L - i) * K; };
-    auto a_load = [&](int i, int e) -> uint64_t {
-        const int per = (L - i) * K;
-        const int k = e / per, r = e % per;
-        const int p = rank + 1 + k * cs;
-        return s.loads[int64_t(p - 1) * s.pos_loads + (row_offset(i, L) + r / K) * g.Kpad + r % K];
-    };
-    auto a_store = [&](int i, int e, uint64_t lw) {
-        const int per = (L - i) * K;
-        const int k = e / per, r = e % per;
-        const int j = i + 1 + r / K, m = r % K;
-        V *at = A + (i & 1) * sp.Abuf + k * sp.Aslot + j * sp.Aj + m;
-        for (int c2 = 0; c2 < C; c2++) {
-            V v = far;
-            if (lw != kInf && (j == L || m <= ph->mlim[c2])) v = V(lw >> 16) + V(sm[sp.X + j * g.Cmax + c2]);
-            at[c2 * KT] = v;
-        }
-    };
-    for (int e = tid; e < a_entries(L - 1); e += blockDim.x) a_store(L - 1, e, a_load(L - 1, e));
-    cluster_sync();  // first A rows built, barriers armed, every CTA started: pushes may begin
-
-    int rb = 0;   // red buffer in use
-    for (int i = L - 1; i >= 0; i--) {
-        const int Pi = s.P < L - i ? s.P : L - i;
-        const int nc = i == 0 ? 1 : C;
-        const bool dlive = d <= s.Du;
-        int mtop[CT], mall = -1;
-        V xf[CT];
+    // A[j][c][c'][m] for a stage starting at layer i (the rows of step i): the load
+    // plus both link costs when the incoming link of cell c (none for the first stage,
+    // which has only c = 0) and the outgoing link c' (none for the last stage) admit m
+    auto a_entry = [&](V *at, int i, int j, int m, uint64_t lw) {
 #pragma unroll
         for (int c = 0; c < CT; c++) {
-            const int mt = i > 0 && mlink[c] < mlog ? mlink[c] : mlog;
-            mtop[c] = dlive && c < nc ? mt : -1;
-            mall = mtop[c] > mall ? mtop[c] : mall;
-            xf[c] = c < nc ? V(sm[sp.X + i * g.Cmax + c]) : V(0);
+            const bool cin = i == 0 ? c == 0 : c < C && m <= mlink[c];
+            const V xi = c < C ? V(sm[sp.X + i * g.Cmax + c]) : V(0);
+#pragma unroll
+            for (int c2 = 0; c2 < CT; c2++) {
+                if (c2 >= C) break;
+                const bool ok = lw != kInf && cin && (j == L || m <= mlink[c2]);
+                at[(c * CT + c2) * KT] = ok ? V(lw >> 16) + xi + V(sm[sp.X + j * g.Cmax + c2]) : far;
+            }
         }
+    };
+    auto a_rows = [&](int i, int e0) {   // entries e0, e0 + blockDim.x, .. (decoded here)
+        for (int e = e0; e < a_total; e += blockDim.x) {
+            const int m = e % K, r = (e / K) % g.Lmax, k = e / (K * g.Lmax);
+            if (r >= L - i) continue;
+            const int p = rank + 1 + k * cs, j = i + 1 + r;
+            const uint64_t lw = s.loads[int64_t(p - 1) * s.pos_loads + (row_offset(i, L) + r) * g.Kpad + m];
+            a_entry(A + (i & 1) * sp.Abuf + k * sp.Aslot + j * sp.Aj + m, i, j, m, lw);
+        }
+    };
+    a_rows(L - 1, tid);
+    cluster_sync();  // first A rows built, pads and barriers set, every CTA started: pushes may begin
+
+    int64_t ro = row_offset(L - 1, L);   // row_offset(i, L) of the current step
+    for (int i = L - 1; i >= 0; i--) {
+        const int Pi = s.P < L - i ? s.P : L - i;
+        const int mw = i > 0 ? mw_n : mw_0;
         // the loads of step i - 1, fetched now and stored after the relaxation
-        const int n_next = i > 0 ? a_entries(i - 1) : 0;
-        const uint64_t pre = tid < n_next ? a_load(i - 1, tid) : 0;
+        ro -= L - i + 1;   // row_offset(i - 1, L)
+        const bool a_mine = a_have && i > 0 && a_r <= L - i;
+        const uint64_t pre = a_mine ? a_src[ro * g.Kpad] : kInf;
+        // cut points j >= i + 2 dealt round-robin over the slices; j = i + 1 (whose row
+        // arrives last) is the final item of the last slice
+        const int n = L - i - 2 > 0 ? L - i - 2 : 0;
+        const int cnt = n > js ? (n - js + jsplit - 1) >> lgs : 0;
+        const int items = cnt + (js == jlast ? 1 : 0);
         for (int k = 0; k < nown_live; k++) {
             const int p = rank + 1 + k * cs;
-            V bv[CT], bvx[CT];   // the cell's best value, bv - X[i][c]
-            uint32_t bi[CT];
+            V bv[CT][NA];   // running bests
+            uint32_t bi[CT][NA];
 #pragma unroll
-            for (int c = 0; c < CT; c++) {
-                bv[c] = cap;
-                bvx[c] = cap - xf[c];
-                bi[c] = kNoArg;
-            }
+            for (int c = 0; c < CT; c++)
+#pragma unroll
+                for (int q = 0; q < NA; q++) {
+                    bv[c][q] = cap;
+                    bi[c][q] = kNoArg;
+                }
             const V *Ak = A + (i & 1) * sp.Abuf + k * sp.Aslot;
-            const V *Hk = H + k * sp.Hslot + d;
+            const V *Hk = H + k * sp.Hslot + sp.Hpad;
             if (p == 1) {
-                if (js == 0) {   // the last stage [i, L): A[L][0][m] = load*(i, L, m, 1)
+                if (js == 0) {   // the last stage [i, L): A[L][c][0][m] = load*(i, L, m, 1) + X[i][c]
 #pragma unroll
                     for (int m = 0; m < KT; m++) {
-                        if (m > mall) break;
-                        const V a0 = Ak[L * sp.Aj + m];
+                        if (m > mw) break;
+                        const V *a0 = Ak + L * sp.Aj + m;
 #pragma unroll
                         for (int c = 0; c < CT; c++) {
-                            if (m <= mtop[c] && a0 < bvx[c]) {
-                                bv[c] = a0 + xf[c];
-                                bvx[c] = a0;
-                                bi[c] = (uint32_t(L) << 8) | (uint32_t(m) << 4);
-                            }
+                            const V v = m <= mlog ? a0[c * CT * KT] : far;
+                            const bool take = v < bv[c][0];
+                            bv[c][0] = take ? v : bv[c][0];
+                            bi[c][0] = take ? (uint32_t(L) << 8) | (uint32_t(m) << 4) : bi[c][0];
                         }
                     }
                 }
             } else if (p <= Pi) {
                 // position p first relaxes at step i = L - p: rows i + 2 .. L - 1 of
                 // position p - 1 arrived during earlier steps but were not waited for yet
-                if (p == L - i) {
+                if (p == L - i)
                     for (int j = L - 1; j >= i + 2; j--)
                         if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + j], 0, spin)) abort_flag = 1;
-                    __syncwarp();
-                }
-                if (!abort_flag)
-                    for (int j = i + 2 + js; j < L; j += a.jsplit)
-                        relax_cut<CT, KT, V>(Ak + j * sp.Aj, Hk + j * sp.Hrow, g.Dpad, C, j, mall, mtop, bv, bvx, bi,
-                                             xf);
-                if (js == jlast) {
-                    // row i + 1 is the one the neighbour pushed last (bounded wait)
-                    if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + i + 1], 0, spin)) abort_flag = 1;
-                    __syncwarp();
-                    if (!abort_flag) {
-                        // j = i + 1 is the smallest cut point: it wins ties, so compare
-                        // against bv + 1 until it has improved a cell
+                for (int t = 0; t < items; t++) {
+                    const bool last = t == cnt;
+                    const int j = last ? i + 1 : i + 2 + js + (t << lgs);
+                    if (last) {
+                        // row i + 1 is the one the neighbour pushed last (bounded wait); it
+                        // is the smallest cut point and wins ties, so compare against bv + 1
+                        // until it has improved a running best
+                        if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + i + 1], 0, spin)) abort_flag = 1;
 #pragma unroll
                         for (int c = 0; c < CT; c++)
-                            if (bv[c] < cap) {
-                                bv[c] += 1;
-                                bvx[c] += 1;
-                            }
-                        relax_cut<CT, KT, V>(Ak + (i + 1) * sp.Aj, Hk + (i + 1) * sp.Hrow, g.Dpad, C, i + 1, mall,
-                                             mtop, bv, bvx, bi, xf);
+#pragma unroll
+                            for (int q = 0; q < NA; q++) bv[c][q] += bv[c][q] < cap ? 1 : 0;
+                    }
+                    relax_cut<CT, KT, NA, V>(Ak + j * sp.Aj, Hk + j * sp.Hrow, sp.Hcol, d, C, uint32_t(j) << 8, mw,
+                                             bv, bi);
+                    if (last) {
 #pragma unroll
                         for (int c = 0; c < CT; c++)
-                            if (bi[c] != kNoArg && int(bi[c] >> 8) != i + 1) {   // bumped and not improved
-                                bv[c] -= 1;
-                                bvx[c] -= 1;
-                            }
+#pragma unroll
+                            for (int q = 0; q < NA; q++)   // bumped and not improved: undo
+                                bv[c][q] -= bi[c][q] != kNoArg && int(bi[c][q] >> 8) != i + 1 ? 1 : 0;
                     }
                 }
             }
-            // combine the slices: red[rb][js][c][d]
-            uint64_t *rr = red + rb * (a.threads * CT);
+            // merge the running bests by key, then the slices of the same d (lanes)
+            uint64_t key[CT];
 #pragma unroll
-            for (int c = 0; c < CT; c++)
-                rr[(js * CT + c) * NTd + tid_d] = bv[c] < cap ? (uint64_t(bv[c]) << 24) | bi[c] : kInf;
-            __syncthreads();
-            rb ^= 1;
-            // slice js finishes the cells c = js, js + jsplit, ..
-            for (int c = js; c < C; c += a.jsplit) {
-                uint64_t key = kInf;
-                if (c < nc && !abort_flag)
-                    for (int q = 0; q < a.jsplit; q++) {
-                        const uint64_t o = rr[(q * CT + c) * NTd + tid_d];
-                        key = o < key ? o : key;
-                    }
-                // the owner of position p + 1 keeps row i of position p in its slot p / cs
-                const bool push = p < s.P && i > 0;
-                const uint32_t crank = uint32_t(p % cs);
-                const V *dst = H + (p / cs) * sp.Hslot + i * sp.Hrow + c * g.Dpad;
-                const uint32_t bar = push ? cluster_map(&rowbar[(p / cs) * g.Lmax + i], crank) : 0;
-                if (dlive) {
-                    write_cell(s, g.Dpad, p, i, c, d, key);
-                    if (push) st_async_remote(cluster_map(dst + d, crank), key == kInf ? cap : V(key >> 24), bar);
+            for (int c = 0; c < CT; c++) {
+                key[c] = kInf;
+#pragma unroll
+                for (int q = 0; q < NA; q++) {
+                    const uint64_t kq = bv[c][q] < cap ? (uint64_t(bv[c][q]) << 24) | bi[c][q] : kInf;
+                    key[c] = kq < key[c] ? kq : key[c];
                 }
-                if (tid_d == 0) {
-                    write_cell(s, g.Dpad, p, i, c, 0, kInf);
-                    if (push) st_async_remote(cluster_map(dst, crank), cap, bar);
+            }
+            __syncwarp();
+            for (int o = 1; o < jsplit; o <<= 1)
+#pragma unroll
+                for (int c = 0; c < CT; c++) {
+                    const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, key[c], o);
+                    key[c] = other < key[c] ? other : key[c];
+                }
+            // slice js finishes the cells c = js, js + jsplit, ..: the value goes to the
+            // owner of position p + 1 (its slot p / cs, row i), value and argument to the
+            // staged dp row that is copied to global memory after the step
+            const bool push = p < s.P && i > 0;
+            const uint32_t crank = uint32_t(p % cs);
+            const uint32_t rrow = push ? cluster_map(H + (p / cs) * sp.Hslot + i * sp.Hrow + sp.Hpad, crank) : 0;
+            const uint32_t bar = push ? cluster_map(&rowbar[(p / cs) * g.Lmax + i], crank) : 0;
+            const int so = ((i & 1) * nown + k) * sp.Srow;
+#pragma unroll
+            for (int c = 0; c < CT; c++) {
+                if (c >= C || (c & (jsplit - 1)) != js) continue;
+                const uint64_t kc = abort_flag ? kInf : key[c];
+                const int at = c * g.Dpad + d, ht = c * sp.Hcol + d;
+                if (dlive) {
+                    sdv[so + at] = int64_t(kc >> 24);
+                    sda[so + at] = uint32_t(kc & 0xFFFFFF);
+                    if (push) st_async_remote(rrow + uint32_t(ht * sizeof(V)), kc == kInf ? cap : V(kc >> 24), bar);
+                }
+                if (d == 1) {
+                    sdv[so + at - 1] = kCap;
+                    sda[so + at - 1] = kNoArg;
+                    if (push) st_async_remote(rrow + uint32_t((ht - 1) * sizeof(V)), cap, bar);
                 }
             }
         }
         // the A rows of step i - 1, into the other buffer (last read at step i + 1)
-        if (tid < n_next) a_store(i - 1, tid, pre);
-        for (int e = tid + blockDim.x; e < n_next; e += blockDim.x) a_store(i - 1, e, a_load(i - 1, e));
+        if (a_mine) a_entry(a_dst + ((i - 1) & 1) * sp.Abuf + i * sp.Aj, i - 1, i + a_r, a_m, pre);
+        if (i > 0 && a_total > int(blockDim.x)) a_rows(i - 1, tid + blockDim.x);
+        // the staged rows of step i go to global memory by bulk copies; those of step
+        // i + 1 have been read by now (their buffer is written again at step i - 1)
+        fence_proxy_async();
+        if (tid == 0) bulk_wait_read();
         __syncthreads();
+        if (tid == 0 && nown_live > 0) {
+            for (int k = 0; k < nown_live; k++) {
+                const int p = rank + 1 + k * cs;
+                const int so = ((i & 1) * nown + k) * sp.Srow;
+                const int64_t at = int64_t(p - 1) * s.pos_cells + int64_t(i) * s.row_cells;
+                bulk_s2g(s.dpv + at, sdv + so, uint32_t(8 * C * g.Dpad));
+                bulk_s2g(s.dpa + at, sda + so, uint32_t(4 * C * g.Dpad));
+            }
+            bulk_commit();
+        }
     }
+    if (tid == 0) bulk_wait_all();
     // every row pushed to this CTA has landed before it may exit (bounded waits)
     if (tid == 0) {
         for (int k = 0; k < nown; k++) {
@@ -568,7 +680,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
 }
 
 template <int CT, int KT>
-__global__ void __launch_bounds__(kMaxThreads, CT == 2 ? 3 : 2) sweep_resident_kernel(PassArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs a) {
     extern __shared__ __align__(128) int64_t sm[];
     __shared__ volatile int abort_flag;
     const int b = blockIdx.x / a.cluster;
@@ -840,7 +952,8 @@ int64_t sweep_smem_bytes(const Geo &g, int jc, int jsplit, int threads) {
 
 int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads) {
     const int nown = (g.Pcap + cluster - 1) / cluster;
-    return 8 * int64_t(res_plan(g, nown, jsplit, threads, ct_of(g.Cmax), kt_of(g.Kmax)).total);
+    (void)threads;
+    return 8 * int64_t(res_plan(g, nown, jsplit, ct_of(g.Cmax), kt_of(g.Kmax), 8).total);
 }
 
 int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int variant, SweepConfig &out) {
@@ -855,11 +968,10 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
     if ((cluster_opt && !ok_cluster(cluster_opt)) || (jsplit_opt && !ok_jsplit(jsplit_opt))) return NEST_E_INVALID;
     const int NTd = (g.Dumax + 31) / 32 * 32;
 
-    // resident: one thread per (slice, device count) holding every candidate; every
-    // instance's cluster resident at once if possible, then the least work per thread
-    // and step
+    // resident: one thread per (device count, slice) holding every candidate, the
+    // slices of a device count in adjacent lanes; every instance's cluster resident at
+    // once if possible, then the least work per thread and step
     if (variant != 2 && g.Cmax <= 4) {
-        const int base = NTd;
         double best = 0;
         SweepConfig pick = {};
         const int cl_list[5] = {16, 8, 4, 2, 1};
@@ -869,7 +981,7 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
             if (cs > 1 && cs > g.Pcap && !cluster_opt) continue;
             for (int ji = 0; ji < 4; ji++) {
                 const int js = jsplit_opt ? jsplit_opt : js_list[ji];
-                const int threads = base * js;
+                const int threads = (g.Dumax * js + 31) / 32 * 32;
                 if (threads > kMaxThreads) continue;
                 const int64_t smem = sweep_resident_smem_bytes(g, cs, js, threads);
                 if (smem > budget) continue;
@@ -880,7 +992,9 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
                 if (cap <= 0) continue;
                 const int waves = (n + cap - 1) / cap;
                 const int nown = (g.Pcap + cs - 1) / cs;
-                const double score = 1.0 / (double(waves) * nown / threads);   // higher is better
+                // fewer waves, then fewer positions per CTA, then about 8 warps: more
+                // warps add per-step work, fewer hide less latency
+                const double score = 1.0 / (double(waves) * nown * (1.0 + std::fabs(std::log2(threads / 256.0)) / 8));
                 if (score > best) {
                     best = score;
                     pick = {cs, js, 0, threads, 1, waves};

@@ -42,8 +42,8 @@ def test_workload1_all_tables(variant):
 
 
 # (CTAs per instance, threads per cell, sweep variant: 0 auto, 1 resident, 2 streaming)
-SWEEP_CONFIGS = [(0, 0, 0), (1, 1, 2), (2, 2, 2), (4, 4, 2), (4, 4, 1), (4, 2, 2), (8, 4, 1), (8, 1, 2),
-                 (8, 2, 1), (16, 4, 1), (16, 8, 2), (16, 1, 1), (16, 2, 1)]
+SWEEP_CONFIGS = [(0, 0, 0), (1, 1, 2), (2, 2, 2), (4, 4, 2), (8, 8, 1), (4, 2, 2), (8, 4, 1), (8, 1, 2),
+                 (8, 2, 1), (16, 4, 1), (16, 8, 1), (16, 8, 2), (16, 1, 1), (16, 2, 1)]
 
 
 def test_resident_variant_rejected_when_it_does_not_fit():
@@ -67,7 +67,8 @@ def test_workload2_all_tables(cluster, jsplit, variant):
 
 # The resident sweep keeps 32-bit value words when every value is small and 64-bit
 # words otherwise; flops scaled by 64 push workload 2's loads past 2^30.
-@pytest.mark.parametrize("cluster,jsplit,variant", [(0, 0, 1), (16, 8, 1), (8, 4, 1), (4, 2, 1), (0, 0, 2)])
+@pytest.mark.parametrize("cluster,jsplit,variant", [(0, 0, 1), (16, 8, 1), (8, 4, 1), (8, 2, 1), (16, 1, 1),
+                                                    (0, 0, 2)])
 def test_workload2_wide_words(cluster, jsplit, variant):
     insts = [G.scaled(x, 64) for x in synth.config_batch(2, B=4)]
     assert not any(G.narrow_words(x) for x in insts)
