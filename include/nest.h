@@ -129,8 +129,8 @@ typedef struct {
     int32_t chunk;          /* instances per pass through the kernels; 0 = all, at most 65535 (the
                                workspace must be sized for the same chunk) */
     int32_t sweep_cluster;  /* CTAs per instance in the DP sweep: 0 = auto, or 1, 2, 4, 8, 16 */
-    int32_t sweep_jsplit;   /* threads sharing one DP cell: 0 = auto, or 1, 2, 4, 8, with
-                               jsplit * (Dumax rounded up to 32) <= 512 (else NEST_E_INVALID) */
+    int32_t sweep_jsplit;   /* threads sharing one DP cell: 0 = auto, or 1, 2, 4, 8, as long as
+                               the CTA stays within 512 threads (else NEST_E_INVALID) */
     int32_t sweep_variant;  /* 0 = auto; 1 = rows resident in shared memory (NEST_E_LIMITS
                                if they do not fit); 2 = rows streamed from global memory */
     int64_t spin_limit;     /* polls before a device wait gives up (each poll suspends for at
@@ -140,7 +140,10 @@ typedef struct {
     void **events;          /* optional cudaEvent_t[6 * chunks]; for chunk n, events
                                [6n .. 6n+5] are recorded on the stream before prep, cost
                                build, strategy reduction, DP sweep, backtrack, and after
-                               backtrack.  NULL = no events. */
+                               backtrack.  NULL = no events; NULL entries are skipped.  The
+                               kernels otherwise launch with programmatic dependent launch
+                               (each may be scheduled while its predecessor finishes); an
+                               event between two of them serialises that boundary. */
 } nest_options;
 
 /* Fills *out with the record layout for dims.  Returns NEST_OK or NEST_E_LIMITS. */

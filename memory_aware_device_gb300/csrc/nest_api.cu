@@ -114,7 +114,8 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
     cudaEvent_t *ev = opt ? reinterpret_cast<cudaEvent_t *>(opt->events) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto mark = [&](int chunk_idx, int k) {
-        return ev ? cuda_status(cudaEventRecord(ev[6 * chunk_idx + k], st), "cudaEventRecord") : NEST_OK;
+        return ev && ev[6 * chunk_idx + k] ? cuda_status(cudaEventRecord(ev[6 * chunk_idx + k], st), "cudaEventRecord")
+                                           : NEST_OK;
     };
     int ci = 0;
     for (int32_t first = 0; first < dims->B; first += chunk, ci++) {

@@ -16,9 +16,12 @@ namespace nest {
 namespace {
 
 __global__ void __launch_bounds__(128) backtrack_kernel(PassArgs a) {
+    __shared__ int walk[4][32][2];   // per warp: stage q -> (i | j << 8 | m << 16 | c' << 20, p)
+    pdl_wait();
+    pdl_trigger();
     const int b = int((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (b >= a.n) return;
+    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
+    if (b >= a.n) return;   // whole warps
     const PrepHdr *ph = prep_hdr(a, b);
     nest_plan_header *hdr = reinterpret_cast<nest_plan_header *>(a.plans_out + int64_t(b) * a.plan_stride);
     nest_stage *st = reinterpret_cast<nest_stage *>(hdr + 1);
@@ -54,44 +57,56 @@ __global__ void __launch_bounds__(128) backtrack_kernel(PassArgs a) {
             bp = op;
         }
     }
-    if (lane != 0) return;
     if (status == NEST_SOLVED && bp == 0) status = NEST_INFEASIBLE;
     if (status != NEST_SOLVED) {
-        hdr->status = status;
-        hdr->n_stages = 0;
-        hdr->t_batch = -1;
-        hdr->bottleneck = -1;
-        a.costs_out[b] = -1;
+        if (lane == 0) {
+            hdr->status = status;
+            hdr->n_stages = 0;
+            hdr->t_batch = -1;
+            hdr->bottleneck = -1;
+            a.costs_out[b] = -1;
+        }
         return;
     }
-    const int L = ph->L, Du = ph->Du;
-    const int64_t tb = bt;
-    int i = 0, p = bp, c = 0, n = 0;
-    int d = Du;
-    const int64_t v0 = dpv[int64_t(bp - 1) * pos_cells + Du];
-    while (i < L && p >= 1 && n < g.Pcap) {
-        const int64_t at = int64_t(p - 1) * pos_cells + int64_t(i) * row_cells + int64_t(c) * g.Dpad + d;
-        const uint32_t arg = dpa[at];
-        const int j = int((arg >> 8) & 0xFF), m = int((arg >> 4) & 0xF), c2 = int(arg & 0xF);
-        if (j <= i || j > L || m >= ph->K || (1 << m) > d || c2 >= ph->C) break;  // not for a solved cell
-        const uint64_t lw = loads[int64_t(p - 1) * g.NP * g.Kpad + (row_offset(i, L) + (j - i - 1)) * g.Kpad + m];
-        st[n].i = int16_t(i);
-        st[n].j = int16_t(j);
-        st[n].s = int16_t(lw & 0xFFFF);
-        st[n].c_next = int8_t(j < L ? c2 : -1);
-        st[n].reserved = 0;
-        st[n].k = ph->unit << m;
-        n++;
-        d -= 1 << m;
-        p -= 1;
-        c = c2;
-        i = j;
+    // lane 0 follows the argument fields (a chain of dependent reads); the stages'
+    // strategies are looked up afterwards by one lane each
+    const int L = ph->L;
+    int n = 0;
+    if (lane == 0) {
+        int i = 0, p = bp, c = 0, d = ph->Du;
+        while (i < L && p >= 1 && n < g.Pcap) {
+            const uint32_t arg = dpa[int64_t(p - 1) * pos_cells + int64_t(i) * row_cells + int64_t(c) * g.Dpad + d];
+            const int j = int((arg >> 8) & 0xFF), m = int((arg >> 4) & 0xF), c2 = int(arg & 0xF);
+            if (j <= i || j > L || m >= ph->K || (1 << m) > d || c2 >= ph->C) break;  // not for a solved cell
+            walk[wq][n][0] = i | j << 8 | m << 16 | c2 << 20;
+            walk[wq][n][1] = p;
+            n++;
+            d -= 1 << m;
+            p -= 1;
+            c = c2;
+            i = j;
+        }
     }
-    hdr->status = NEST_SOLVED;
-    hdr->n_stages = n;
-    hdr->t_batch = tb;
-    hdr->bottleneck = v0;
-    a.costs_out[b] = tb;
+    n = __shfl_sync(0xffffffffu, n, 0);
+    __syncwarp();
+    if (lane < n) {
+        const int w = walk[wq][lane][0], p = walk[wq][lane][1];
+        const int i = w & 0xFF, j = (w >> 8) & 0xFF, m = (w >> 16) & 0xF, c2 = (w >> 20) & 0xF;
+        const uint64_t lw = loads[int64_t(p - 1) * g.NP * g.Kpad + (row_offset(i, L) + (j - i - 1)) * g.Kpad + m];
+        st[lane].i = int16_t(i);
+        st[lane].j = int16_t(j);
+        st[lane].s = int16_t(lw & 0xFFFF);
+        st[lane].c_next = int8_t(j < L ? c2 : -1);
+        st[lane].reserved = 0;
+        st[lane].k = ph->unit << m;
+    }
+    if (lane == 0) {
+        hdr->status = NEST_SOLVED;
+        hdr->n_stages = n;
+        hdr->t_batch = bt;
+        hdr->bottleneck = dpv[int64_t(bp - 1) * pos_cells + ph->Du];
+        a.costs_out[b] = bt;
+    }
 }
 
 }  // namespace
@@ -99,8 +114,8 @@ __global__ void __launch_bounds__(128) backtrack_kernel(PassArgs a) {
 int launch_backtrack(const PassArgs &a, void *stream) {
     const int threads = 128;
     const int64_t total = int64_t(a.n) * 32;
-    backtrack_kernel<<<unsigned((total + threads - 1) / threads), threads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cuda_status(cudaGetLastError(), "backtrack launch");
+    return launch_kernel(backtrack_kernel, dim3(unsigned((total + threads - 1) / threads)), dim3(threads), 0, stream, 1,
+                         "backtrack launch", a);
 }
 
 }  // namespace nest

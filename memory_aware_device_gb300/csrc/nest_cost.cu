@@ -44,6 +44,8 @@ struct Net {
 };
 
 __global__ void __launch_bounds__(256) cost_kernel(PassArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.y;
     const PrepHdr *ph = prep_hdr(a, b);
     if (ph->status != NEST_SOLVED) return;
@@ -145,8 +147,7 @@ int launch_cost(const PassArgs &a, void *stream) {
     const int64_t work = int64_t(a.g.NP) * a.g.Smax;
     const int threads = 256;
     dim3 grid(unsigned((work + threads - 1) / threads), unsigned(a.n));
-    cost_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cuda_status(cudaGetLastError(), "cost launch");
+    return launch_kernel(cost_kernel, grid, dim3(threads), 0, stream, 1, "cost launch", a);
 }
 
 }  // namespace nest

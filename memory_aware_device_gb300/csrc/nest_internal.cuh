@@ -187,6 +187,41 @@ __host__ __device__ inline PrepHdr *prep_hdr(const PassArgs &a, int b) {
 // environment a failure is also reported on stderr with the call that failed.
 int cuda_status(int err, const char *what);
 
+// Programmatic dependent launch.  Every kernel of a pass is launched with
+// programmatic stream serialization allowed, so it can be scheduled while the
+// previous kernel on the stream is still running: it lets its own dependents launch
+// at once (pdl_trigger) and waits for the previous kernel to complete and its memory
+// to be visible (pdl_wait) before touching anything that kernel wrote.  Both are
+// no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `fn(args...)` with the PDL attribute, plus a cluster shape when cluster > 1.
+template <typename... KArgs, typename... Args>
+int launch_kernel(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, void *stream, int cluster,
+                  const char *what, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
+    if (cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = unsigned(cluster);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        na++;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cuda_status(cudaLaunchKernelEx(&cfg, fn, args...), what);
+}
+
 // Launchers (one translation unit each).
 int launch_prep(const PassArgs &a, void *stream);
 int launch_cost(const PassArgs &a, void *stream);

@@ -20,6 +20,8 @@ __device__ __forceinline__ bool pow2(int64_t v) { return v > 0 && (v & (v - 1)) 
 __device__ __forceinline__ int ilog2(int64_t v) { return 63 - __clzll(v); }
 
 __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
+    pdl_wait();   // records and the workspace may still be in use by the previous kernel
+    pdl_trigger();
     const int b = blockIdx.x;
     const unsigned char *rec = a.records + int64_t(b) * a.rl.record_bytes;
     const nest_record_header h = *reinterpret_cast<const nest_record_header *>(rec);
@@ -129,40 +131,58 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
         ph->mlim[c] = ml;
     }
 
-    // prefix sums: one thread per array (L <= 255)
+    // prefix sums and the sparse table, built in shared memory (L <= 255): the layer
+    // arrays are read once with coalesced loads, each array is scanned by one warp,
+    // and the results are written back with coalesced stores
+    __shared__ int64_t sv[kNumPfx][256];   // layer values, scanned in place
+    __shared__ int64_t sst[kLogL][256];    // sparse table of max(aw)
     int64_t *pfx = reinterpret_cast<int64_t *>(pb + a.pl.pfx);
-    if (threadIdx.x < kNumPfx) {
-        const int q = threadIdx.x;
-        int64_t *out = pfx + int64_t(q) * (g.Lmax + 1);
-        int64_t acc = 0;
-        out[0] = 0;
-        if (q == kNm) {
-            for (int l = 0; l < L; l++) out[l + 1] = acc += rec[a.rl.moe + l];
-        } else {
-            const int64_t off[6] = {a.rl.fl, a.rl.pd, a.rl.pe, a.rl.ao, a.rl.aw, a.rl.a2a};
-            const int64_t *src = reinterpret_cast<const int64_t *>(rec + off[q]);
-            for (int l = 0; l < L; l++) out[l + 1] = acc += src[l];
-        }
-    }
-    // raw activations, sparse table of max(aw), link costs, packed strategies
     int64_t *ao = reinterpret_cast<int64_t *>(pb + a.pl.ao);
     int64_t *awst = reinterpret_cast<int64_t *>(pb + a.pl.awst);
-    const int64_t *aw_in = reinterpret_cast<const int64_t *>(rec + a.rl.aw);
-    const int64_t *ao_in = reinterpret_cast<const int64_t *>(rec + a.rl.ao);
-    for (int l = threadIdx.x; l < L; l += blockDim.x) {
-        ao[l] = ao_in[l];
-        awst[l] = aw_in[l];
+    {
+        const int64_t off[6] = {a.rl.fl, a.rl.pd, a.rl.pe, a.rl.ao, a.rl.aw, a.rl.a2a};
+        for (int e = threadIdx.x; e < kNumPfx * L; e += blockDim.x) {
+            const int q = e / L, l = e % L;
+            const int64_t v = q == kNm ? int64_t(rec[a.rl.moe + l]) : reinterpret_cast<const int64_t *>(rec + off[q])[l];
+            sv[q][l] = v;
+            if (q == kAw) sst[0][l] = v;
+            if (q == kAo) ao[l] = v;
+        }
     }
     __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < kNumPfx) {
+        int64_t carry = 0;
+        for (int base = 0; base < L; base += 32) {
+            int64_t x = base + lane < L ? sv[warp][base + lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            x += carry;
+            if (base + lane < L) sv[warp][base + lane] = x;
+            carry = __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
+    }
     for (int lv = 1; lv < kLogL; lv++) {
         const int span = 1 << (lv - 1);
         for (int l = threadIdx.x; l < L; l += blockDim.x) {
-            const int64_t x = awst[int64_t(lv - 1) * g.Lmax + l];
-            const int64_t y = l + span < L ? awst[int64_t(lv - 1) * g.Lmax + l + span] : x;
-            awst[int64_t(lv) * g.Lmax + l] = x > y ? x : y;
+            const int64_t x = sst[lv - 1][l];
+            const int64_t y = l + span < L ? sst[lv - 1][l + span] : x;
+            sst[lv][l] = x > y ? x : y;
         }
         __syncthreads();
     }
+    for (int e = threadIdx.x; e < kNumPfx * (L + 1); e += blockDim.x) {
+        const int q = e / (L + 1), l = e % (L + 1);
+        pfx[int64_t(q) * (g.Lmax + 1) + l] = l == 0 ? 0 : sv[q][l - 1];
+    }
+    for (int e = threadIdx.x; e < kLogL * L; e += blockDim.x) {
+        const int lv = e / L, l = e % L;
+        awst[int64_t(lv) * g.Lmax + l] = sst[lv][l];
+    }
+    const int64_t *ao_in = reinterpret_cast<const int64_t *>(rec + a.rl.ao);
     int64_t *X = reinterpret_cast<int64_t *>(pb + a.pl.X);
     __shared__ uint32_t xmax;
     if (threadIdx.x == 0) xmax = 0;
@@ -195,8 +215,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
 }  // namespace
 
 int launch_prep(const PassArgs &a, void *stream) {
-    prep_kernel<<<a.n, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cuda_status(cudaGetLastError(), "prep launch");
+    return launch_kernel(prep_kernel, dim3(unsigned(a.n)), dim3(256), 0, stream, 1, "prep launch", a);
 }
 
 }  // namespace nest

@@ -28,6 +28,8 @@ constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads) reduce_kernel(PassArgs a, int lg) {
     extern __shared__ uint64_t bucket[];   // [Pcap + 1][kThreads], one column per lane
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.y;
     PrepHdr *ph = prep_hdr(a, b);
     if (ph->status != NEST_SOLVED) return;   // uniform over the block
@@ -112,8 +114,7 @@ int launch_reduce(const PassArgs &a, void *stream) {
                              "reduce smem attribute"))
         return rc;
     dim3 grid(unsigned((rows + rows_per_block - 1) / rows_per_block), unsigned(a.n));
-    reduce_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, lg);
-    return cuda_status(cudaGetLastError(), "reduce launch");
+    return launch_kernel(reduce_kernel, grid, dim3(kThreads), smem, stream, 1, "reduce launch", a, lg);
 }
 
 }  // namespace nest

@@ -683,6 +683,8 @@ template <int CT, int KT>
 __global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs a) {
     extern __shared__ __align__(128) int64_t sm[];
     __shared__ volatile int abort_flag;
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x / a.cluster;
     const int rank = int(cluster_rank());
     PrepHdr *ph = prep_hdr(a, b);
@@ -727,6 +729,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) sweep_stream_kernel(PassArgs a
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int cmin[16];
     __shared__ volatile int abort_flag;
+    pdl_wait();
+    pdl_trigger();
     const Geo &g = a.g;
     const int cs = a.cluster;
     const int b = blockIdx.x / cs;
@@ -887,9 +891,8 @@ cudaLaunchConfig_t cluster_config(int n, int cluster, int threads, size_t smem, 
 template <typename Kern>
 int launch_cluster(Kern fn, const PassArgs &a, void *stream, size_t smem, const char *what) {
     if (int rc = set_attributes(fn, smem, a.cluster, what)) return rc;
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = cluster_config(a.n, a.cluster, a.threads, smem, stream, attr);
-    return cuda_status(cudaLaunchKernelEx(&cfg, fn, a), what);
+    return launch_kernel(fn, dim3(unsigned(a.n * a.cluster)), dim3(unsigned(a.threads)), smem, stream, a.cluster, what,
+                         a);
 }
 
 // The resident variant is instantiated for up to 4 candidates and KT = 4, 8 or 16 widths.

@@ -176,11 +176,11 @@ def decode_plans(raw: np.ndarray, dims: Dims) -> List[dict]:
 def options(chunk=0, cluster=0, jsplit=0, spin_limit=0, events=None, variant=0) -> Options:
     o = Options(chunk=chunk, sweep_cluster=cluster, sweep_jsplit=jsplit, sweep_variant=variant,
                 spin_limit=spin_limit, events=None)
-    if events is not None:
+    if events is not None:   # torch.cuda.Event entries; None entries are not recorded
         for e in events:
-            if not e.cuda_event:   # torch creates the CUDA event lazily, on its first record
+            if e is not None and not e.cuda_event:   # torch creates the CUDA event lazily
                 e.record()
-        arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+        arr = (C.c_void_p * len(events))(*[e.cuda_event if e is not None else None for e in events])
         o._events_keep = (arr, list(events))   # the CUDA events live as long as the options
         o.events = C.cast(arr, C.c_void_p)
     return o
