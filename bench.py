@@ -33,9 +33,10 @@ from memory_aware_device_gb300 import synth  # noqa: E402
 
 METRIC = "DP relaxations/sec and placement solves/sec on 1 GB300; % of HBM roofline"
 UNIT = "relaxations/s"
-KERNELS = ("prep", "cost_build", "strategy_reduce", "dp_sweep", "backtrack")
-KERNEL_SRC = {"prep": "nest_prep.cu", "cost_build": "nest_cost.cu", "strategy_reduce": "nest_reduce.cu",
-              "dp_sweep": "nest_sweep.cu", "backtrack": "nest_backtrack.cu"}
+KERNELS = ("prep", "stage_loads", "dp_sweep", "backtrack")
+NEV = len(KERNELS) + 1   # events per chunk
+KERNEL_SRC = {"prep": "nest_prep.cu", "stage_loads": "nest_loads.cu", "dp_sweep": "nest_sweep.cu",
+              "backtrack": "nest_backtrack.cu"}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -257,8 +258,8 @@ def main():
     def make_opt(only=None):
         # events at every kernel boundary, or only around kernel `only` (the others keep
         # their programmatic dependent launches)
-        ev = [torch.cuda.Event(enable_timing=True) if only is None or q % 6 in (only, only + 1) else None
-              for q in range(6 * nchunks)]
+        ev = [torch.cuda.Event(enable_timing=True) if only is None or q % NEV in (only, only + 1) else None
+              for q in range(NEV * nchunks)]
         return nest.options(chunk=args.chunk, events=ev), ev
 
     def kernel_ms(opts):   # average ms per step of each kernel, over all chunks
@@ -266,8 +267,8 @@ def main():
         for _, ev in opts:
             for c in range(nchunks):
                 for q, k in enumerate(KERNELS):
-                    if ev[6 * c + q] is not None and ev[6 * c + q + 1] is not None:
-                        out[k] += ev[6 * c + q].elapsed_time(ev[6 * c + q + 1])
+                    if ev[NEV * c + q] is not None and ev[NEV * c + q + 1] is not None:
+                        out[k] += ev[NEV * c + q].elapsed_time(ev[NEV * c + q + 1])
         return {k: v / len(opts) for k, v in out.items()}
 
     def step(opt):
@@ -370,8 +371,9 @@ def main():
                 "peak_source": f"derived: {SMS} SMs x {INT32_LANES} INT32 lanes x {peaks['sm_max_mhz']:.0f} MHz"
                                f" / {OPS_PER_RELAX} ops per relaxation", "sm_mhz_seen": mhz}
     else:
-        algo = {"cost_build": 8 * words, "strategy_reduce": 8 * words,
-                "prep": 0, "backtrack": 0}[dom]
+        # the per-position loads table is what the stage-loads kernel must write
+        loads_bytes = sum(8 * x.Pmax * (x.L * (x.L + 1) // 2) * (x.D // x.unit).bit_length() for x in instances)
+        algo = {"stage_loads": loads_bytes, "prep": 0, "backtrack": 0}[dom]
         achieved = algo / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": stored_traffic(dom, workload),

@@ -137,14 +137,22 @@ typedef struct {
                                most 20 us): 0 = default (2^16, about a second); a negative
                                value makes every wait give up at once, which exercises the
                                timeout path (instances end NEST_TIMED_OUT) */
-    void **events;          /* optional cudaEvent_t[6 * chunks]; for chunk n, events
-                               [6n .. 6n+5] are recorded on the stream before prep, cost
-                               build, strategy reduction, DP sweep, backtrack, and after
-                               backtrack.  NULL = no events; NULL entries are skipped.  The
-                               kernels otherwise launch with programmatic dependent launch
-                               (each may be scheduled while its predecessor finishes); an
-                               event between two of them serialises that boundary. */
+    void **events;          /* optional cudaEvent_t[5 * chunks]; for chunk n, events
+                               [5n .. 5n+4] are recorded on the stream before prep, the stage
+                               loads (cost build and strategy reduction), DP sweep and
+                               backtrack, and after backtrack.  NULL = no events; NULL
+                               entries are skipped.  The kernels otherwise launch with
+                               programmatic dependent launch (each may be scheduled while its
+                               predecessor finishes); an event between two of them
+                               serialises that boundary. */
+    uint32_t flags;         /* NEST_KEEP_COSTS, or 0 */
+    int32_t reserved;
 } nest_options;
+
+/* Also write the stage-cost tensor (every (stage, width, strategy) word, before the
+ * per-position strategy minimum) into the workspace, for inspection.  The solve does
+ * not need it; the workspace must then hold nest_workspace_size_costs() bytes. */
+#define NEST_KEEP_COSTS 1u
 
 /* Fills *out with the record layout for dims.  Returns NEST_OK or NEST_E_LIMITS. */
 int nest_record_layout(const nest_dims *dims, nest_layout *out);
@@ -154,9 +162,13 @@ size_t nest_plan_bytes(const nest_dims *dims);
 
 /* Device workspace bytes that nest_solve needs for passes of `chunk` instances
  * (chunk <= 0 means dims->B).  0 when dims break the limits.  The workspace holds,
- * per instance of a chunk, the stage-cost tensor cost[pair(i, j)][m][s] (8 bytes
- * per word), the per-position strategy loads, and the DP value and argument tables. */
+ * per instance of a chunk, the derived per-instance tables, the per-position
+ * strategy loads, and the DP value and argument tables. */
 size_t nest_workspace_size(const nest_dims *dims, int32_t chunk);
+
+/* The same plus room for the stage-cost tensor cost[pair(i, j)][m][s] (8 bytes per
+ * word): what nest_solve needs with NEST_KEEP_COSTS. */
+size_t nest_workspace_size_costs(const nest_dims *dims, int32_t chunk);
 
 /* Solve a batch on the GPU.
  *   records    DEVICE, B instance records (layout above), read only
@@ -186,15 +198,17 @@ int nest_solve_host(const nest_dims *dims, const void *records_host, int64_t *co
 
 /* Offsets (bytes from the workspace start) of the intermediate tables of the
  * LAST chunk a nest_solve call processed, for inspection after the stream syncs:
- *   cost  uint64 [chunk][NP][Kmax][Spad]  (tau << 8) | pmax, all ones = not applicable
  *   loads uint64 [chunk][Pcap][NP][Kpad]  (tau* << 16) | s* per position p (index p-1)
  *   dpv   int64  [chunk][Pcap][Lmax][Cmax][Dpad]  DP value per (p, i, c, d), 2^40-1 = none
  *   dpa   uint32 [chunk][Pcap][Lmax][Cmax][Dpad]  (j << 8) | (m << 4) | c'
+ *   cost  uint64 [chunk][NP][Kmax][Spad]  (tau << 8) | pmax, all ones = not applicable;
+ *         written only with NEST_KEEP_COSTS, after the end of the plain workspace
  * where NP = Lmax (Lmax + 1) / 2 pairs (i, j) ordered by i then j, Kmax =
  * floor(log2 Dumax) + 1, Kpad = Kmax rounded up to even, Spad = Smax rounded up
- * to even, Dpad = Dumax + 1 rounded up to even. */
+ * to even, Dpad = Dumax + 1 rounded up to a multiple of 4.  total and total_costs
+ * are nest_workspace_size and nest_workspace_size_costs. */
 typedef struct {
-    int64_t cost, loads, dpv, dpa, total;
+    int64_t loads, dpv, dpa, cost, total, total_costs;
     int32_t NP, Kmax, Kpad, Spad, Dpad, chunk;
 } nest_ws_layout;
 int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out);

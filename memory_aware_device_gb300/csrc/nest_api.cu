@@ -1,9 +1,9 @@
 // C ABI of the placement-DP solver (declared in include/nest.h).
 //
 // A call validates the batch dimensions on the host, then, for each chunk of
-// instances, enqueues five kernels on the caller's stream: prep (validation,
-// prefix sums, link costs), cost build, strategy reduction, DP sweep and
-// backtrack.  Nothing is allocated and no state survives the call.
+// instances, enqueues four kernels on the caller's stream: prep (validation,
+// prefix sums, link costs), stage loads (cost build and strategy reduction), DP
+// sweep and backtrack.  Nothing is allocated and no state survives the call.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -27,8 +27,8 @@ using namespace nest;
 
 namespace {
 
-// Instances per pass: the whole batch by default, at most 65535 (the cost and
-// reduction kernels index instances with blockIdx.y).
+// Instances per pass: the whole batch by default, at most 65535 (the stage-loads
+// kernel indexes instances with blockIdx.y).
 int32_t chunk_of(const nest_dims *dims, int32_t chunk) {
     if (chunk <= 0 || chunk > dims->B) chunk = dims->B;
     return chunk < 65535 ? chunk : 65535;
@@ -59,17 +59,25 @@ size_t nest_workspace_size(const nest_dims *dims, int32_t chunk) {
     return size_t(ws_layout(g, ch < 1 ? 1 : ch).total);
 }
 
+size_t nest_workspace_size_costs(const nest_dims *dims, int32_t chunk) {
+    Geo g;
+    if (!dims || !make_geo(*dims, g)) return 0;
+    const int32_t ch = chunk_of(dims, chunk);
+    return size_t(ws_layout(g, ch < 1 ? 1 : ch).total_costs);
+}
+
 int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out) {
     Geo g;
     if (!dims || !out) return NEST_E_INVALID;
     if (!make_geo(*dims, g)) return NEST_E_LIMITS;
     const int32_t ch = chunk_of(dims, chunk);
     const WsLayout w = ws_layout(g, ch < 1 ? 1 : ch);
-    out->cost = w.cost;
     out->loads = w.loads;
     out->dpv = w.dpv;
     out->dpa = w.dpa;
+    out->cost = w.cost;
     out->total = w.total;
+    out->total_costs = w.total_costs;
     out->NP = g.NP;
     out->Kmax = g.Kmax;
     out->Kpad = g.Kpad;
@@ -91,7 +99,10 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
         return NEST_E_WORKSPACE;
     const int32_t chunk = chunk_of(dims, opt ? opt->chunk : 0);
     const WsLayout w = ws_layout(g, chunk);
-    if (ws_bytes < size_t(w.total)) return NEST_E_WORKSPACE;
+    const uint32_t flags = opt ? opt->flags : 0u;
+    if (flags & ~NEST_KEEP_COSTS) return NEST_E_INVALID;
+    const bool keep = (flags & NEST_KEEP_COSTS) != 0;
+    if (ws_bytes < size_t(keep ? w.total_costs : w.total)) return NEST_E_WORKSPACE;
     SweepConfig cfg;
     int rc = sweep_configure(g, chunk, opt ? opt->sweep_cluster : 0, opt ? opt->sweep_jsplit : 0,
                              opt ? opt->sweep_variant : 0, cfg);
@@ -111,10 +122,11 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
     a.threads = cfg.threads;
     a.resident = cfg.resident;
     a.spin_limit = opt ? opt->spin_limit : 0;
+    a.keep_costs = keep ? 1 : 0;
     cudaEvent_t *ev = opt ? reinterpret_cast<cudaEvent_t *>(opt->events) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto mark = [&](int chunk_idx, int k) {
-        return ev && ev[6 * chunk_idx + k] ? cuda_status(cudaEventRecord(ev[6 * chunk_idx + k], st), "cudaEventRecord")
+        return ev && ev[5 * chunk_idx + k] ? cuda_status(cudaEventRecord(ev[5 * chunk_idx + k], st), "cudaEventRecord")
                                            : NEST_OK;
     };
     int ci = 0;
@@ -123,10 +135,9 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
         a.records = static_cast<const unsigned char *>(records) + int64_t(first) * a.rl.record_bytes;
         a.costs_out = costs_out + first;
         a.plans_out = static_cast<unsigned char *>(plans_out) + int64_t(first) * a.plan_stride;
-        if ((rc = mark(ci, 0)) || (rc = launch_prep(a, st)) || (rc = mark(ci, 1)) || (rc = launch_cost(a, st)) ||
-            (rc = mark(ci, 2)) || (rc = launch_reduce(a, st)) || (rc = mark(ci, 3)) ||
-            (rc = launch_sweep(a, st)) || (rc = mark(ci, 4)) || (rc = launch_backtrack(a, st)) ||
-            (rc = mark(ci, 5)))
+        if ((rc = mark(ci, 0)) || (rc = launch_prep(a, st)) || (rc = mark(ci, 1)) || (rc = launch_loads(a, st)) ||
+            (rc = mark(ci, 2)) || (rc = launch_sweep(a, st)) || (rc = mark(ci, 3)) || (rc = launch_backtrack(a, st)) ||
+            (rc = mark(ci, 4)))
             return rc;
     }
     return NEST_OK;
@@ -150,6 +161,7 @@ int nest_solve_host(const nest_dims *dims, const void *records_host, int64_t *co
     if (!make_geo(*dims, g)) return NEST_E_LIMITS;
     if (dims->B == 0) return NEST_OK;
     if (!records_host || !costs_host || !plans_host || !workspace) return NEST_E_INVALID;
+    if (opt && opt->flags) return NEST_E_INVALID;   // the host entry keeps no intermediate tables
     if (reinterpret_cast<uintptr_t>(workspace) % 256) return NEST_E_WORKSPACE;
     if (ws_bytes < nest_workspace_size_host(dims, opt ? opt->chunk : 0)) return NEST_E_WORKSPACE;
     nest_layout rl;

@@ -122,7 +122,7 @@ __host__ __device__ inline PrepLayout prep_layout(const Geo &g) {
 
 // Workspace regions for passes of `ch` instances.
 struct WsLayout {
-    int64_t prep, cost, loads, dpv, dpa, total;
+    int64_t prep, loads, dpv, dpa, total, cost, total_costs;
     int64_t prep_stride, cost_stride, loads_stride, dp_stride;  // per instance (elements for tables)
 };
 
@@ -136,8 +136,6 @@ __host__ __device__ inline WsLayout ws_layout(const Geo &g, int64_t ch) {
     int64_t off = 0;
     w.prep = off;
     off = align_up(off + ch * w.prep_stride, 256);
-    w.cost = off;
-    off = align_up(off + ch * w.cost_stride * 8, 256);
     w.loads = off;
     off = align_up(off + ch * w.loads_stride * 8, 256);
     w.dpv = off;
@@ -145,6 +143,9 @@ __host__ __device__ inline WsLayout ws_layout(const Geo &g, int64_t ch) {
     w.dpa = off;
     off = align_up(off + ch * w.dp_stride * 4, 256);
     w.total = off;
+    w.cost = off;   // only with NEST_KEEP_COSTS
+    off = align_up(off + ch * w.cost_stride * 8, 256);
+    w.total_costs = off;
     return w;
 }
 
@@ -177,6 +178,8 @@ struct PassArgs {
     int32_t threads;               // sweep threads per CTA
     int32_t resident;              // sweep variant: 1 = dp rows resident in shared memory
     int64_t spin_limit;            // polls per bounded wait (negative: give up at once)
+    int32_t keep_costs;            // also write the stage-cost tensor
+    int32_t pad;
 };
 
 __host__ __device__ inline PrepHdr *prep_hdr(const PassArgs &a, int b) {
@@ -224,8 +227,7 @@ int launch_kernel(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, void
 
 // Launchers (one translation unit each).
 int launch_prep(const PassArgs &a, void *stream);
-int launch_cost(const PassArgs &a, void *stream);
-int launch_reduce(const PassArgs &a, void *stream);
+int launch_loads(const PassArgs &a, void *stream);
 int launch_sweep(const PassArgs &a, void *stream);
 int launch_backtrack(const PassArgs &a, void *stream);
 // Dynamic shared memory of the streaming and resident sweep variants.

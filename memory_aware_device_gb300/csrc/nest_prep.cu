@@ -20,10 +20,17 @@ __device__ __forceinline__ bool pow2(int64_t v) { return v > 0 && (v & (v - 1)) 
 __device__ __forceinline__ int ilog2(int64_t v) { return 63 - __clzll(v); }
 
 __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
+    extern __shared__ __align__(16) unsigned char rec_s[];   // the instance's record
     pdl_wait();   // records and the workspace may still be in use by the previous kernel
     pdl_trigger();
     const int b = blockIdx.x;
-    const unsigned char *rec = a.records + int64_t(b) * a.rl.record_bytes;
+    {   // one coalesced pass over the record; everything below reads shared memory
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.records + int64_t(b) * a.rl.record_bytes);
+        uint4 *dst = reinterpret_cast<uint4 *>(rec_s);
+        for (int q = threadIdx.x; q < int(a.rl.record_bytes / 16); q += blockDim.x) dst[q] = src[q];
+    }
+    __syncthreads();
+    const unsigned char *rec = rec_s;
     const nest_record_header h = *reinterpret_cast<const nest_record_header *>(rec);
     PrepHdr *ph = prep_hdr(a, b);
     unsigned char *pb = reinterpret_cast<unsigned char *>(ph);
@@ -215,7 +222,11 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
 }  // namespace
 
 int launch_prep(const PassArgs &a, void *stream) {
-    return launch_kernel(prep_kernel, dim3(unsigned(a.n)), dim3(256), 0, stream, 1, "prep launch", a);
+    const size_t smem = size_t(a.rl.record_bytes);
+    if (int rc = cuda_status(cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+                             "prep smem attribute"))
+        return rc;
+    return launch_kernel(prep_kernel, dim3(unsigned(a.n)), dim3(256), smem, stream, 1, "prep launch", a);
 }
 
 }  // namespace nest

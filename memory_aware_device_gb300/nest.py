@@ -24,8 +24,10 @@ ERRORS = {NEST_E_INVALID: "invalid argument", NEST_E_LIMITS: "batch dimensions b
           NEST_E_TIMEOUT: "a device wait gave up"}
 
 # Every function declared in include/nest.h.
-EXPORTS = ("nest_record_layout", "nest_plan_bytes", "nest_workspace_size", "nest_workspace_layout",
-           "nest_solve", "nest_workspace_size_host", "nest_solve_host", "nest_solve_static")
+EXPORTS = ("nest_record_layout", "nest_plan_bytes", "nest_workspace_size", "nest_workspace_size_costs",
+           "nest_workspace_layout", "nest_solve", "nest_workspace_size_host", "nest_solve_host",
+           "nest_solve_static")
+KEEP_COSTS = 1   # NEST_KEEP_COSTS
 STATIC_SCRATCH_BYTES = 64 << 20   # NEST_STATIC_SCRATCH_BYTES
 
 
@@ -45,13 +47,14 @@ class Layout(C.Structure):
 
 
 class WsLayout(C.Structure):
-    _fields_ = [(n, C.c_int64) for n in ("cost", "loads", "dpv", "dpa", "total")] + \
+    _fields_ = [(n, C.c_int64) for n in ("loads", "dpv", "dpa", "cost", "total", "total_costs")] + \
                [(n, C.c_int32) for n in ("NP", "Kmax", "Kpad", "Spad", "Dpad", "chunk")]
 
 
 class Options(C.Structure):
     _fields_ = [("chunk", C.c_int32), ("sweep_cluster", C.c_int32), ("sweep_jsplit", C.c_int32),
-                ("sweep_variant", C.c_int32), ("spin_limit", C.c_int64), ("events", C.c_void_p)]
+                ("sweep_variant", C.c_int32), ("spin_limit", C.c_int64), ("events", C.c_void_p),
+                ("flags", C.c_uint32), ("reserved", C.c_int32)]
 
 
 HEADER_DT = np.dtype([("L", "<i4"), ("D", "<i4"), ("unit", "<i4"), ("T", "<i4"), ("C", "<i4"),
@@ -78,6 +81,8 @@ def lib():
         L.nest_plan_bytes.restype = C.c_size_t
         L.nest_workspace_size.argtypes = [P(Dims), C.c_int32]
         L.nest_workspace_size.restype = C.c_size_t
+        L.nest_workspace_size_costs.argtypes = [P(Dims), C.c_int32]
+        L.nest_workspace_size_costs.restype = C.c_size_t
         L.nest_workspace_size_host.argtypes = [P(Dims), C.c_int32]
         L.nest_workspace_size_host.restype = C.c_size_t
         L.nest_workspace_layout.argtypes = [P(Dims), C.c_int32, P(WsLayout)]
@@ -114,8 +119,9 @@ def plan_bytes(dims: Dims) -> int:
     return int(lib().nest_plan_bytes(C.byref(dims)))
 
 
-def workspace_size(dims: Dims, chunk: int = 0, host: bool = False) -> int:
-    f = lib().nest_workspace_size_host if host else lib().nest_workspace_size
+def workspace_size(dims: Dims, chunk: int = 0, host: bool = False, keep_costs: bool = False) -> int:
+    f = lib().nest_workspace_size_host if host else \
+        lib().nest_workspace_size_costs if keep_costs else lib().nest_workspace_size
     return int(f(C.byref(dims), chunk))
 
 
@@ -173,9 +179,9 @@ def decode_plans(raw: np.ndarray, dims: Dims) -> List[dict]:
     return out
 
 
-def options(chunk=0, cluster=0, jsplit=0, spin_limit=0, events=None, variant=0) -> Options:
+def options(chunk=0, cluster=0, jsplit=0, spin_limit=0, events=None, variant=0, keep_costs=False) -> Options:
     o = Options(chunk=chunk, sweep_cluster=cluster, sweep_jsplit=jsplit, sweep_variant=variant,
-                spin_limit=spin_limit, events=None)
+                spin_limit=spin_limit, events=None, flags=KEEP_COSTS if keep_costs else 0)
     if events is not None:   # torch.cuda.Event entries; None entries are not recorded
         for e in events:
             if e is not None and not e.cuda_event:   # torch creates the CUDA event lazily
@@ -214,7 +220,7 @@ def solve_host_raw(dims: Dims, records_host: np.ndarray, costs_host: np.ndarray,
 class Solver:
     """Owns device buffers (via torch) for repeated solves of batches with fixed dims."""
 
-    def __init__(self, dims: Dims, chunk: int = 0, device="cuda", host_io: bool = False):
+    def __init__(self, dims: Dims, chunk: int = 0, device="cuda", host_io: bool = False, keep_costs: bool = False):
         import torch
         self.dims = dims
         self.chunk = chunk
@@ -225,7 +231,7 @@ class Solver:
         self.records = torch.empty(B * self.layout.record_bytes, dtype=torch.uint8, device=self.device)
         self.costs = torch.empty(B, dtype=torch.int64, device=self.device)
         self.plans = torch.empty(B * self.pb, dtype=torch.uint8, device=self.device)
-        ws = workspace_size(dims, chunk, host=host_io)
+        ws = workspace_size(dims, chunk, host=host_io, keep_costs=keep_costs)
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device)
 
     def load(self, records_np: np.ndarray):

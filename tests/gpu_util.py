@@ -16,14 +16,16 @@ def ensure_built():
     O.build()
 
 
-def run(instances, chunk=0, cluster=0, jsplit=0, spin_limit=0, Pcap=None, Dumax=None, variant=0):
-    """Solve on cuda:0; returns (solver, results)."""
+def run(instances, chunk=0, cluster=0, jsplit=0, spin_limit=0, Pcap=None, Dumax=None, variant=0,
+        keep_costs=True):
+    """Solve on cuda:0 (keeping the stage-cost tensor for inspection unless told
+    otherwise); returns (solver, results)."""
     import torch
     dims = nest.make_dims(instances, Pcap=Pcap, Dumax=Dumax)
-    s = nest.Solver(dims, chunk=chunk)
+    s = nest.Solver(dims, chunk=chunk, keep_costs=keep_costs)
     s.load(nest.pack_records(instances, dims))
     s.run(opt=nest.options(chunk=chunk, cluster=cluster, jsplit=jsplit, spin_limit=spin_limit,
-                           variant=variant))
+                           variant=variant, keep_costs=keep_costs))
     torch.cuda.synchronize()
     return s, s.results()
 

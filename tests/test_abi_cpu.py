@@ -99,7 +99,8 @@ def test_workspace_grows_with_chunk_and_matches_layout():
     assert 0 < a < b
     lay = nest.workspace_layout(dims, 8)
     assert lay.total == b and lay.chunk == 8
-    assert lay.cost < lay.loads < lay.dpv < lay.dpa < lay.total
+    assert lay.loads < lay.dpv < lay.dpa < lay.total == lay.cost < lay.total_costs
+    assert lay.total_costs == nest.workspace_size(dims, 8, keep_costs=True)
     assert lay.NP == 96 * 97 // 2 and lay.Kmax == 8 and lay.Dpad == 132 and lay.Spad == 36
     assert nest.workspace_size(dims, 0) == b and nest.workspace_size(dims, 99) == b
     assert nest.workspace_size(dims, 8, host=True) > b
