@@ -132,7 +132,9 @@ typedef struct {
     int32_t sweep_jsplit;   /* threads sharing one DP cell: 0 = auto, or 1, 2, 4, 8, as long as
                                the CTA stays within 512 threads (else NEST_E_INVALID) */
     int32_t sweep_variant;  /* 0 = auto; 1 = rows resident in shared memory (NEST_E_LIMITS
-                               if they do not fit); 2 = rows streamed from global memory */
+                               if they do not fit, or with sweep_cluster 1 when Pcap > 1:
+                               rows go to the next position's CTA, which must be another
+                               one); 2 = rows streamed from global memory */
     int64_t spin_limit;     /* polls before a device wait gives up (each poll suspends for at
                                most 20 us): 0 = default (2^16, about a second); a negative
                                value makes every wait give up at once, which exercises the

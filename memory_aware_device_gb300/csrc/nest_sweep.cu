@@ -393,9 +393,66 @@ __device__ __forceinline__ void relax_one(const V *Aj, const V *Hj, int Hcol, in
     }
 }
 
+// The same for exactly MT widths m < MT (every lane's excluded widths read far or
+// cap): all dp values of a c' are loaded first, then each cell takes the minimum
+// over its MT candidates with a tree that keeps the smaller m on ties, and merges it
+// into its running best.  Loads overlap and the serial depth is log2(MT).
+template <int CT, int KT, int NA, int MT, typename V>
+__device__ __forceinline__ void relax_cut_t(const V *Aj, const V *Hj, int Hcol, int d, int C, uint32_t jarg,
+                                            V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+    constexpr bool kPad = sizeof(V) == 4;   // rows padded with cap below x = 0
+#pragma unroll
+    for (int c2 = 0; c2 < CT; c2++) {
+        if (c2 >= C) break;
+        V nv[MT];
+#pragma unroll
+        for (int m = 0; m < MT; m++) {
+            const int x = kPad ? d - (1 << m) : (d - (1 << m) > 0 ? d - (1 << m) : 0);
+            nv[m] = Hj[c2 * Hcol + x];
+        }
+#pragma unroll
+        for (int c = 0; c < CT; c++) {
+            V v[MT];
+            int id[MT];
+#pragma unroll
+            for (int m = 0; m < MT; m++) {
+                const V av = Aj[(c * CT + c2) * KT + m];
+                v[m] = av > nv[m] ? av : nv[m];
+                id[m] = m;
+            }
+#pragma unroll
+            for (int w = 1; w < MT; w <<= 1)
+#pragma unroll
+                for (int q = 0; q + w < MT; q += 2 * w) {
+                    const bool r = v[q + w] < v[q];   // the left holds the smaller widths
+                    v[q] = r ? v[q + w] : v[q];
+                    id[q] = r ? id[q + w] : id[q];
+                }
+            const bool take = v[0] < bv[c][c2];
+            bv[c][c2] = take ? v[0] : bv[c][c2];
+            bi[c][c2] = take ? jarg | (uint32_t(id[0]) << 4) | uint32_t(c2) : bi[c][c2];
+        }
+    }
+}
+
 template <int CT, int KT, int NA, typename V>
 __device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, int d, int C, uint32_t jarg, int mw,
                                           V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+    if constexpr (NA > 1) {
+        // exactly mw + 1 widths, unrolled (the warp-uniform mw selects the copy)
+        switch (mw) {
+        case -1: return;
+        case 0: relax_cut_t<CT, KT, NA, 1, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return;
+        case 1: if constexpr (KT >= 2) { relax_cut_t<CT, KT, NA, 2, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
+        case 2: if constexpr (KT >= 3) { relax_cut_t<CT, KT, NA, 3, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
+        case 3: if constexpr (KT >= 4) { relax_cut_t<CT, KT, NA, 4, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
+        case 4: if constexpr (KT >= 5) { relax_cut_t<CT, KT, NA, 5, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
+        case 5: if constexpr (KT >= 6) { relax_cut_t<CT, KT, NA, 6, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
+        case 6: if constexpr (KT >= 7) { relax_cut_t<CT, KT, NA, 7, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
+        case 7: if constexpr (KT >= 8) { relax_cut_t<CT, KT, NA, 8, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
+        default: break;
+        }
+    }
     if constexpr (NA > 1) {
 #pragma unroll
         for (int c2 = 0; c2 < CT; c2++) {
@@ -454,11 +511,14 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     uint32_t *sda = reinterpret_cast<uint32_t *>(sm + sp.sda);
     constexpr V cap = Word<V>::cap, far = Word<V>::far;
 
-    // thread = (device count d, slice js), slices in adjacent lanes
+    // thread = (slot group, device count d, slice js), slices in adjacent lanes; the
+    // ngrp groups of gsize threads work on different slots at the same time
     const int tid = threadIdx.x, lane = tid & 31;
     const int jsplit = a.jsplit, lgs = __ffs(jsplit) - 1;
+    const int gsize = (g.Dumax * jsplit + 31) / 32 * 32, ngrp = a.threads / gsize;
+    const int kg = tid / gsize, gtid = tid % gsize;
     const int js = lane & (jsplit - 1);
-    const int d = (tid >> 5) * (32 >> lgs) + (lane >> lgs) + 1;
+    const int d = (gtid >> 5) * (32 >> lgs) + (lane >> lgs) + 1;
     const int jlast = jsplit - 1;   // the slice that also takes j = i + 1
     const int64_t spin = a.spin_limit == 0 ? kDefaultSpin : a.spin_limit;
     const uint32_t row_bytes = uint32_t(sizeof(V) * s.C * (s.Du + 1));   // one pushed row
@@ -546,7 +606,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         const int n = L - i - 2 > 0 ? L - i - 2 : 0;
         const int cnt = n > js ? (n - js + jsplit - 1) >> lgs : 0;
         const int items = cnt + (js == jlast ? 1 : 0);
-        for (int k = 0; k < nown_live; k++) {
+        for (int k = kg; k < nown_live; k += ngrp) {
             const int p = rank + 1 + k * cs;
             V bv[CT][NA];   // running bests
             uint32_t bi[CT][NA];
@@ -929,6 +989,7 @@ int resident_capacity_ct(const Geo &g, int cluster, int threads, size_t smem) {
 
 template <int CT, int KT>
 int launch_resident(const PassArgs &a, void *stream) {
+    if (a.cluster < 2 && a.g.Pcap > 1) return NEST_E_LIMITS;   // pushes need a peer CTA
     const size_t smem = size_t(sweep_resident_smem_bytes(a.g, a.cluster, a.jsplit, a.threads));
     return launch_cluster(sweep_resident_kernel<CT, KT>, a, stream, smem, "sweep (resident) launch");
 }
@@ -972,8 +1033,12 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
     const int NTd = (g.Dumax + 31) / 32 * 32;
 
     // resident: one thread per (device count, slice) holding every candidate, the
-    // slices of a device count in adjacent lanes; every instance's cluster resident at
-    // once if possible, then the least work per thread and step
+    // slices of a device count in adjacent lanes, and up to ngrp such groups per CTA
+    // working on different positions.  Prefer every instance's cluster resident at
+    // once, then the fewest positions per CTA (positions sharing an SM, whether in
+    // turn or in parallel groups, slow each other down about as much), then larger
+    // clusters, then groups of about 8 warps (more warps add per-step work, fewer
+    // hide less latency).
     if (variant != 2 && g.Cmax <= 4) {
         double best = 0;
         SweepConfig pick = {};
@@ -982,10 +1047,20 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
         for (int ci = 0; ci < 5; ci++) {
             const int cs = cluster_opt ? cluster_opt : cl_list[ci];
             if (cs > 1 && cs > g.Pcap && !cluster_opt) continue;
+            // rows are pushed to the owner of the next position with st.async, which
+            // must be another CTA of the cluster: one CTA per instance only when no
+            // row is pushed (a single position)
+            if (cs == 1 && g.Pcap > 1) {
+                if (cluster_opt) break;
+                continue;
+            }
             for (int ji = 0; ji < 4; ji++) {
                 const int js = jsplit_opt ? jsplit_opt : js_list[ji];
-                const int threads = (g.Dumax * js + 31) / 32 * 32;
-                if (threads > kMaxThreads) continue;
+                const int gsize = (g.Dumax * js + 31) / 32 * 32;
+                if (gsize > kMaxThreads) continue;
+                const int nown_c = (g.Pcap + cs - 1) / cs;
+                const int ngrp = nown_c < kMaxThreads / gsize ? nown_c : kMaxThreads / gsize;
+                const int threads = ngrp * gsize;
                 const int64_t smem = sweep_resident_smem_bytes(g, cs, js, threads);
                 if (smem > budget) continue;
                 const int cap = resident_capacity_ct(g, cs, threads, size_t(smem));
@@ -994,10 +1069,9 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
                                  cs, js, threads, (long long)smem, cap);
                 if (cap <= 0) continue;
                 const int waves = (n + cap - 1) / cap;
-                const int nown = (g.Pcap + cs - 1) / cs;
-                // fewer waves, then fewer positions per CTA, then about 8 warps: more
-                // warps add per-step work, fewer hide less latency
-                const double score = 1.0 / (double(waves) * nown * (1.0 + std::fabs(std::log2(threads / 256.0)) / 8));
+                const int serial = (nown_c + ngrp - 1) / ngrp;
+                const double score = 1.0 / (double(waves) * serial * ngrp * (1.0 + (16 - cs) / 64.0) *
+                                            (1.0 + std::fabs(std::log2(gsize / 256.0)) / 8));
                 if (score > best) {
                     best = score;
                     pick = {cs, js, 0, threads, 1, waves};

@@ -54,6 +54,15 @@ def test_resident_variant_rejected_when_it_does_not_fit():
     assert e.value.rc == nest.NEST_E_LIMITS
 
 
+def test_resident_variant_needs_a_peer_cta():
+    # rows go to the next position's CTA by st.async, which must be another CTA: one
+    # CTA per instance is refused before any launch when there is more than one position
+    insts = synth.config_batch(2, B=2)
+    with pytest.raises(nest.NestError) as e:
+        G.run(insts, cluster=1, jsplit=4, variant=1)
+    assert e.value.rc == nest.NEST_E_LIMITS
+
+
 @pytest.mark.parametrize("cluster,jsplit,variant", SWEEP_CONFIGS)
 def test_workload2_all_tables(cluster, jsplit, variant):
     insts = synth.config_batch(2)
