@@ -213,6 +213,25 @@ def run_reference(args, workload, instances, relax_total):
     print(json.dumps(line), flush=True)
 
 
+def rank_instances(workload_id: int, rank: int):
+    """The batch one rank solves: its own B instances (seeds 1000 w + rank B + b), so
+    ranks share nothing and need no exchange (the tiny workload is one fixed instance)."""
+    B = synth.CONFIG_BATCH[workload_id]
+    return synth.config_batch(workload_id, B=B, first=rank * B if workload_id != 1 else 0)
+
+
+def job_totals(local_units: float, local_ms: float, dist=None, device=None):
+    """Whole-job (units, ms): units summed over ranks, time the slowest rank's."""
+    if dist is None:
+        return local_units, local_ms
+    import torch
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(u.item()), float(t.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -231,7 +250,7 @@ def main():
     rank, local_rank, ws = dist_env()
     workload = f"{synth.CONFIG_NAMES[args.workload]}"
     B = synth.CONFIG_BATCH[args.workload]
-    instances = synth.config_batch(args.workload, B=B, first=rank * B if args.workload != 1 else 0)
+    instances = rank_instances(args.workload, rank)
     relax_total = sum(relaxations(x) for x in instances)
 
     if args.impl == "reference":
@@ -315,13 +334,9 @@ def main():
     torch.cuda.synchronize(dev)
     kms = kernel_ms(bd)
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    job_relax, total_ms = job_totals(relax_total, sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = relax_total * ws / (ms_per_step * 1e-3)
+    value = job_relax / (ms_per_step * 1e-3)
     solves = B * ws / (ms_per_step * 1e-3)
     launches = 5 * nchunks * args.steps
 
@@ -351,12 +366,8 @@ def main():
         t0 = time.perf_counter()
         host_step()
         e2e_ms.append(1e3 * (time.perf_counter() - t0))
-    e2e_total = sum(e2e_ms)
-    if dist is not None:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_val = relax_total * ws / (e2e_total / e2e_steps * 1e-3)
+    _, e2e_total = job_totals(relax_total, sum(e2e_ms), dist, dev)
+    e2e_val = job_relax / (e2e_total / e2e_steps * 1e-3)
     assert nest.decode_plans(plans_pin.numpy(), dims) == res, "host entry point disagrees with device path"
 
     # roofline of the dominant kernel, on its duration inside the timed steps
