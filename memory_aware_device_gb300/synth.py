@@ -53,6 +53,7 @@ class Instance:
     tierLat: np.ndarray  # int64 [T] nanoseconds
     cand: np.ndarray    # int32 [C] candidate tiers for links between stages
     strat: np.ndarray   # int16 [S, 5] strategies (t, cp, e, z, r)
+    schedule: int = 0   # pipeline schedule: 0 = 1F1B, 1 = GPipe
 
     @property
     def T(self) -> int:

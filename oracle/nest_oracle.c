@@ -10,6 +10,8 @@
  *     is the stage's position counted from the end of a 1F1B pipeline;
  *   - §3.3, recompute: only the stage input is stashed, at the price of one more
  *     forward pass;
+ *   - §3.3, schedule: the stashed count is (s - 1) under 1F1B and scales with B/d
+ *     under GPipe;
  *   - §4, Eq. 3: dp[l][D][k][s] = min over cut D' and device count a of
  *     max(dp[l'][D'][k - a][s - 1], load_l(D \ D', a, s)), solved backward over
  *     the layer suffix D, with the tier l of the (not yet placed) producer stage
@@ -33,6 +35,9 @@
  *     phi (n-1)/n of the volume per device, phi = 2 for AllReduce, else 1; a group
  *     of one device or a zero-byte volume issues no collective;
  *   - stage time per microbatch = ceil(replica time / q) + ceil(gradient sync / M);
+ *   - GPipe (B/d): each of the q data-parallel replicas runs ceil(M / q) of the M
+ *     microbatches and holds all of them at once, at every position; the bubble, and
+ *     so the time model, is the same as for 1F1B;
  *   - SYNCCOST is folded into each stage's amortised gradient sync term;
  *   - ties: smallest (v, j, m, c') per cell, smallest (tau, s) per strategy choice,
  *     smallest (t_batch, p) at the end.
@@ -47,7 +52,7 @@
 #define OR_INF UINT64_MAX
 
 typedef struct {
-    int32_t L, D, unit, T, C, S, Pmax, pad;
+    int32_t L, D, unit, T, C, S, Pmax, schedule; /* schedule: 0 = 1F1B, 1 = GPipe */
     int64_t R, M, budget, opt_factor;
     const int64_t *fl, *pd, *pe, *ao, *aw, *a2a;
     const uint8_t *moe;
@@ -114,6 +119,7 @@ int or_validate(const or_instance *x) {
         if (st[3] < 0 || st[3] > 3 || st[4] < 0 || st[4] > 1) return 2;
     }
     if (x->Pmax < 1 || x->Pmax > 31) return 2;
+    if (x->schedule < 0 || x->schedule > 1) return 2;
     if (x->M < x->Pmax || x->M > (1LL << 20)) return 2;
     if (x->R < 1 || x->R > (1LL << 40)) return 2;
     if (x->budget < 0 || x->budget > (1LL << 62)) return 2;
@@ -185,7 +191,8 @@ static void stage_terms(const or_instance *x, const or_sums *u, int m, int s, or
     r->tau = cdiv(r->comp + r->tp + r->cpc + r->ep + r->z3, q) + cdiv(r->sd + r->se, x->M);
 
     /* §3.3: weights + gradients ("2 weights"), optimizer states, activations,
-     * each sharded by the ZeRO stage; plus (position - 1) stashed microbatches */
+     * each sharded by the ZeRO stage; plus the stashed microbatches: (position - 1)
+     * under 1F1B, all ceil(M / q) of the replica's microbatches under GPipe */
     int64_t opt = x->opt_factor;
     r->w = z == 3 ? cdiv(Wd, q) + cdiv(We, qe) : Wd + We;
     r->g = z >= 2 ? cdiv(Wd, q) + cdiv(We, qe) : Wd + We;
@@ -195,6 +202,8 @@ static void stage_terms(const or_instance *x, const or_sums *u, int m, int s, or
     r->stat = r->w + r->g + r->o + r->act;
     if (r->stat > x->budget)
         r->pmax = 0;
+    else if (x->schedule == 1)
+        r->pmax = r->stash <= (x->budget - r->stat) / cdiv(x->M, q) ? x->Pmax : 0;
     else if (r->stash == 0)
         r->pmax = x->Pmax;
     else

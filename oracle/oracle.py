@@ -35,7 +35,7 @@ def build(force: bool = False) -> str:
 
 class _Inst(C.Structure):
     _fields_ = [("L", C.c_int32), ("D", C.c_int32), ("unit", C.c_int32), ("T", C.c_int32),
-                ("C", C.c_int32), ("S", C.c_int32), ("Pmax", C.c_int32), ("pad", C.c_int32),
+                ("C", C.c_int32), ("S", C.c_int32), ("Pmax", C.c_int32), ("schedule", C.c_int32),
                 ("R", C.c_int64), ("M", C.c_int64), ("budget", C.c_int64), ("opt_factor", C.c_int64),
                 ("fl", C.c_void_p), ("pd", C.c_void_p), ("pe", C.c_void_p), ("ao", C.c_void_p),
                 ("aw", C.c_void_p), ("a2a", C.c_void_p), ("moe", C.c_void_p),
@@ -91,7 +91,8 @@ class Marshalled:
         }
         k = self.keep
         self.s = _Inst(L=int(inst.L), D=int(inst.D), unit=int(inst.unit), T=len(k["G"]),
-                       C=len(k["cand"]), S=k["strat"].shape[0], Pmax=int(inst.Pmax), pad=0,
+                       C=len(k["cand"]), S=k["strat"].shape[0], Pmax=int(inst.Pmax),
+                       schedule=int(getattr(inst, "schedule", 0)),
                        R=int(inst.R), M=int(inst.M), budget=int(inst.budget),
                        opt_factor=int(inst.opt_factor),
                        **{n: v.ctypes.data for n, v in k.items()})
