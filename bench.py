@@ -243,6 +243,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps (capped at 500)")
+    ap.add_argument("--schedule", default="1f1b", choices=["1f1b", "gpipe"],
+                    help="pipeline schedule of every instance (gpipe: all microbatches of a replica stashed)")
+    ap.add_argument("--gpipe-microbatches", type=int, default=512,
+                    help="microbatches per iteration under --schedule gpipe (4096 do not fit in memory)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -251,6 +255,10 @@ def main():
     workload = f"{synth.CONFIG_NAMES[args.workload]}"
     B = synth.CONFIG_BATCH[args.workload]
     instances = rank_instances(args.workload, rank)
+    if args.schedule == "gpipe":
+        for x in instances:
+            x.schedule, x.M = 1, max(args.gpipe_microbatches, x.Pmax)
+        workload += f"-gpipe-M{args.gpipe_microbatches}"
     relax_total = sum(relaxations(x) for x in instances)
 
     if args.impl == "reference":

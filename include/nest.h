@@ -78,6 +78,7 @@ typedef struct {
  *   two with G[T-1] >= D; 1000 <= bw <= 2^40; 0 <= lat <= 2^24; 1 <= C <= Cmax;
  *   candidate tiers strictly increasing in [0, T); 1 <= S <= Smax; t, cp, e powers
  *   of two <= 8192; z in 0..3; r in 0..1; 1 <= Pmax <= Pcap; Pmax <= M <= 2^20;
+ *   schedule in {0, 1};
  *   1 <= R <= 2^40; 0 <= budget <= 2^62; 0 <= opt_factor <= 16; per layer
  *   0 <= fl <= 2^48, 0 <= pd, pe, ao, aw, a2a <= 2^38, moe in {0, 1}.       */
 typedef struct {
@@ -88,7 +89,9 @@ typedef struct {
     int32_t C;          /* candidate tiers for inter-stage links */
     int32_t S;          /* strategies */
     int32_t Pmax;       /* largest number of pipeline stages */
-    int32_t reserved;
+    int32_t schedule;   /* 0 = 1F1B (a stage at position p from the end stashes p - 1
+                           microbatches), 1 = GPipe (each of the q data-parallel replicas
+                           of a stage holds all its ceil(M / q) microbatches) */
     int64_t R;          /* device compute rate, flop per ns */
     int64_t M;          /* microbatches per iteration */
     int64_t budget;     /* bytes per device */

@@ -81,7 +81,8 @@ struct PrepHdr {
     int32_t L, D, unit, lu, Du, K, T, C, S, P;
     uint32_t maxX32;     // largest link cost X, saturated at 2^31 - 1 (prep)
     uint32_t maxload32;  // largest finite per-position load tau*, saturated (reduction)
-    int32_t pad0, pad1, pad2;
+    int32_t schedule;    // 0 = 1F1B, 1 = GPipe
+    int32_t pad1, pad2;
     int64_t R, M, budget, opt;
     int64_t G[8], bw[8], lat[8];
     int32_t cand[16];

@@ -11,11 +11,13 @@
 // amortised over the M microbatches of an iteration.  §3.3: the stage fits at
 // pipeline position p while weights + gradients + optimizer states (each sharded
 // by the ZeRO stage) + activations + (p - 1) stashed microbatches stay within the
-// budget; pmax is the largest such p.  §4 Eq. 3 takes, for each new stage, the
-// best latency over its strategies with memory-infeasible states pruned; the link
-// terms of a transition do not depend on the strategy, so that minimum is taken
-// once per (stage, width, position) - Appendix K Algorithm 1 likewise evaluates a
-// stage's load once before its inner loops.
+// budget; pmax is the largest such p.  That is the 1F1B schedule; under GPipe the
+// stash scales with B/d instead - every replica holds all of its ceil(M / q)
+// microbatches at every position - so pmax is P or 0.  §4 Eq. 3 takes, for each
+// new stage, the best latency over its strategies with memory-infeasible states
+// pruned; the link terms of a transition do not depend on the strategy, so that
+// minimum is taken once per (stage, width, position) - Appendix K Algorithm 1
+// likewise evaluates a stage's load once before its inner loops.
 //
 // Arithmetic: every group size is a power of two, so each ceil-division by a group
 // is a shift, and ceil((n - 1) phi V / n) = phi V - floor(phi V / n).  The
@@ -121,6 +123,11 @@ __device__ __forceinline__ void stage_words(const PrepHdr *ph, const unsigned ch
                 int pmax;
                 if (stat > budget) {
                     pmax = 0;
+                } else if (ph->schedule == 1) {
+                    // GPipe: ceil(M / q) stashed microbatches; exact 128-bit product
+                    const uint64_t inflight = uint64_t((M + (int64_t(1) << lq) - 1) >> lq);
+                    const uint64_t lo = uint64_t(stash) * inflight, hi = __umul64hi(uint64_t(stash), inflight);
+                    pmax = hi == 0 && lo <= uint64_t(budget - stat) ? P : 0;
                 } else if (stash == 0) {
                     pmax = P;
                 } else {

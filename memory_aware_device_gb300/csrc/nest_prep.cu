@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
         bd |= h.R < 1 || h.R > (int64_t(1) << 40);
         bd |= h.budget < 0 || h.budget > (int64_t(1) << 62);
         bd |= h.opt_factor < 0 || h.opt_factor > 16;
+        bd |= h.schedule < 0 || h.schedule > 1;
         bad = bd;
     }
     __syncthreads();
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PassArgs a) {
         ph->M = h.M;
         ph->budget = h.budget;
         ph->opt = h.opt_factor;
+        ph->schedule = h.schedule;
     }
     const int64_t *G = reinterpret_cast<const int64_t *>(rec + a.rl.G);
     const int64_t *bw = reinterpret_cast<const int64_t *>(rec + a.rl.bw);

@@ -58,7 +58,7 @@ class Options(C.Structure):
 
 
 HEADER_DT = np.dtype([("L", "<i4"), ("D", "<i4"), ("unit", "<i4"), ("T", "<i4"), ("C", "<i4"),
-                      ("S", "<i4"), ("Pmax", "<i4"), ("reserved", "<i4"), ("R", "<i8"), ("M", "<i8"),
+                      ("S", "<i4"), ("Pmax", "<i4"), ("schedule", "<i4"), ("R", "<i8"), ("M", "<i8"),
                       ("budget", "<i8"), ("opt_factor", "<i8")])
 PLAN_HDR_DT = np.dtype([("status", "<i4"), ("n_stages", "<i4"), ("t_batch", "<i8"), ("bottleneck", "<i8")])
 STAGE_DT = np.dtype([("i", "<i2"), ("j", "<i2"), ("s", "<i2"), ("c_next", "i1"), ("reserved", "i1"),
@@ -145,6 +145,7 @@ def pack_records(instances: Sequence, dims: Dims, out: np.ndarray | None = None)
         h["L"], h["D"], h["unit"], h["T"], h["C"], h["S"], h["Pmax"] = (
             x.L, x.D, x.unit, len(x.tierG), len(x.cand), len(x.strat), x.Pmax)
         h["R"], h["M"], h["budget"], h["opt_factor"] = x.R, x.M, x.budget, x.opt_factor
+        h["schedule"] = int(getattr(x, "schedule", 0))
         row[:HEADER_DT.itemsize] = h.view(np.uint8)
 
         def put(off, arr, dt):

@@ -100,6 +100,33 @@ def test_mixed_word_widths_in_one_launch():
         check_tables(s, b, insts[b])
 
 
+# GPipe stash schedule: memory at every position as for all ceil(M / q) microbatches
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_workload2_gpipe_all_tables(variant):
+    insts = synth.config_batch(2, B=8)
+    for x in insts:
+        x.schedule, x.M = 1, 512
+    s, res = G.run(insts, variant=variant)
+    oracle = G.oracle_many(insts)
+    assert sum(o["status"] == 0 for o in oracle) >= 4
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+        check_tables(s, b, insts[b])
+
+
+def test_mixed_schedules_in_one_launch():
+    insts = [synth.random_tiny(3000 + k, Lmax=7, Dmax=16) for k in range(200)]
+    for x in insts[::2]:
+        x.schedule = 1
+    s, res = G.run(insts, Pcap=6)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+    for b in range(0, 200, 23):
+        if oracle[b]["status"] != 2:
+            check_tables(s, b, insts[b])
+
+
 def test_workload3_full_batch():
     insts = synth.config_batch(3)
     s, res = G.run(insts)
