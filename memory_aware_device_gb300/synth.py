@@ -18,7 +18,7 @@ from __future__ import annotations
 
 import dataclasses
 import itertools
-from typing import List
+from typing import List, Sequence
 
 import numpy as np
 
@@ -235,3 +235,25 @@ def random_tiny(seed: int, Lmax: int = 6, Dmax: int = 8, Tmax: int = 3, Cmax: in
     return Instance(L=L, D=D, unit=unit, Pmax=Pmax, R=R, M=M, budget=budget,
                     opt_factor=int(rng.integers(0, 7)), fl=fl, pd=pd, pe=pe, ao=ao, aw=aw,
                     a2a=a2a, moe=moe, tierG=G, tierBw=bw, tierLat=lat, cand=cand, strat=strat)
+
+
+# Joint microbatch-size exploration (Nest §5.2.3: the microbatch size is explored
+# together with the placement).  The workloads above use microbatches of one
+# sample; a variant with b samples per microbatch scales every per-microbatch
+# quantity (flops, activations, all-to-all volume) by b and runs M = global batch / b
+# microbatches per iteration; parameters do not change.
+MICROBATCH_SIZES = (1, 2, 4, 8)
+GLOBAL_BATCH = 4096
+
+
+def microbatch_variant(inst: Instance, mbs: int, global_batch: int = GLOBAL_BATCH) -> Instance:
+    """The instance with `mbs` samples per microbatch (inst has one)."""
+    y = dataclasses.replace(inst)
+    y.fl, y.ao, y.aw, y.a2a = (np.asarray(a, np.int64) * mbs for a in (inst.fl, inst.ao, inst.aw, inst.a2a))
+    y.M = max(global_batch // mbs, inst.Pmax)
+    return y
+
+
+def joint_batch(problems: Sequence[Instance], sizes=MICROBATCH_SIZES) -> List[Instance]:
+    """Every problem expanded into its microbatch variants, consecutively."""
+    return [microbatch_variant(x, b) for x in problems for b in sizes]

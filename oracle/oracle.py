@@ -163,3 +163,15 @@ def solve_many(instances, threads: int | None = None) -> list:
     threads = threads or os.cpu_count() or 1
     with ThreadPoolExecutor(max_workers=threads) as ex:
         return list(ex.map(solve, instances))
+
+
+def solve_joint(variants) -> dict:
+    """Joint search over the variants of one problem (Nest §5.2.3, the microbatch size
+    explored together with the placement): the variant with the smallest t_batch, ties
+    to the earlier variant; best = -1 when no variant is solved."""
+    best, res = -1, None
+    results = [solve(v) for v in variants]
+    for q, r in enumerate(results):
+        if r["status"] == 0 and (best < 0 or r["t_batch"] < res["t_batch"]):
+            best, res = q, r
+    return {"best": best, "t_batch": res["t_batch"] if res else -1, "results": results}
