@@ -15,6 +15,7 @@ only the timing barrier and the max-over-ranks use the process group.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -247,6 +248,9 @@ def main():
                     help="pipeline schedule of every instance (gpipe: all microbatches of a replica stashed)")
     ap.add_argument("--gpipe-microbatches", type=int, default=512,
                     help="microbatches per iteration under --schedule gpipe (4096 do not fit in memory)")
+    ap.add_argument("--joint", action="store_true",
+                    help="joint microbatch-size search: every problem solved with 1, 2, 4 and 8 samples "
+                         "per microbatch, the best variant selected on the GPU")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -259,6 +263,12 @@ def main():
         for x in instances:
             x.schedule, x.M = 1, max(args.gpipe_microbatches, x.Pmax)
         workload += f"-gpipe-M{args.gpipe_microbatches}"
+    group = 1
+    if args.joint:
+        group = len(synth.MICROBATCH_SIZES)
+        instances = synth.joint_batch(instances)
+        B = len(instances)
+        workload += "-joint-mbs" + "-".join(str(b) for b in synth.MICROBATCH_SIZES)
     relax_total = sum(relaxations(x) for x in instances)
 
     if args.impl == "reference":
@@ -298,10 +308,17 @@ def main():
                         out[k] += ev[NEV * c + q].elapsed_time(ev[NEV * c + q + 1])
         return {k: v / len(opts) for k, v in out.items()}
 
+    best = torch.empty(B // group, dtype=torch.int32, device=dev)
+
     def step(opt):
         rc = nest.solve_raw(dims, solver.records, solver.costs, solver.plans, solver.workspace, stream, opt)
         if rc:
             raise nest.NestError(rc)
+        if group > 1:   # the joint search: best variant of every problem
+            rc = nest.lib().nest_select_best(solver.costs.data_ptr(), B, group, best.data_ptr(),
+                                             ctypes.c_void_p(stream.cuda_stream))
+            if rc:
+                raise nest.NestError(rc, "nest_select_best")
 
     warm = [make_opt() for _ in range(args.warmup)]
     for o in warm:
@@ -346,7 +363,7 @@ def main():
     ms_per_step = total_ms / args.steps
     value = job_relax / (ms_per_step * 1e-3)
     solves = B * ws / (ms_per_step * 1e-3)
-    launches = 5 * nchunks * args.steps
+    launches = (len(KERNELS) * nchunks + (1 if group > 1 else 0)) * args.steps
 
     # end to end through the host-buffer entry point: H2D records, solve, D2H results
     e2e_steps = args.e2e_steps or min(args.steps, 500)
@@ -356,13 +373,25 @@ def main():
     plans_pin = torch.empty(B * nest.plan_bytes(dims), dtype=torch.uint8).pin_memory()
     hopt = nest.options(chunk=args.chunk)
 
+    best_pin = torch.empty(max(B // group, 1), dtype=torch.int32).pin_memory()
+
     def host_step():
         import ctypes as C
-        rc = nest.lib().nest_solve_host(C.byref(dims), rec_pin.data_ptr(), costs_pin.data_ptr(),
-                                        plans_pin.data_ptr(), wsh.data_ptr(), wsh.numel(),
-                                        C.c_void_p(stream.cuda_stream), C.byref(hopt))
-        if rc:
-            raise nest.NestError(rc, "nest_solve_host")
+        if group == 1:
+            rc = nest.lib().nest_solve_host(C.byref(dims), rec_pin.data_ptr(), costs_pin.data_ptr(),
+                                            plans_pin.data_ptr(), wsh.data_ptr(), wsh.numel(),
+                                            C.c_void_p(stream.cuda_stream), C.byref(hopt))
+            if rc:
+                raise nest.NestError(rc, "nest_solve_host")
+            return
+        # the joint search through the device entry points: H2D records, solve, select,
+        # D2H of the choices, t_batch values and plans
+        solver.records.copy_(rec_pin, non_blocking=True)
+        step(hopt)
+        best_pin[:B // group].copy_(best, non_blocking=True)
+        costs_pin.copy_(solver.costs, non_blocking=True)
+        plans_pin.copy_(solver.plans, non_blocking=True)
+        stream.synchronize()
     for _ in range(args.warmup):
         host_step()
     if dist is not None:
@@ -409,11 +438,12 @@ def main():
                            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
                            "parallelism": f"replicas{ws}"},
                 "solves_per_s": solves,
+                **({"problems_per_s": solves / group, "variants_per_problem": group} if group > 1 else {}),
                 "kernel_ms_per_step": kms,
                 "kernel_ms_note": "separate pass, events at every kernel boundary (no launch overlap)",
                 "roofline": roof, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(records.nbytes),
-                        "d2h_bytes_per_step": int(8 * B + B * nest.plan_bytes(dims)),
+                        "d2h_bytes_per_step": int(8 * B + B * nest.plan_bytes(dims) + (4 * (B // group) if group > 1 else 0)),
                         "ms_per_step": e2e_total / e2e_steps},
                 "gpu_launches": launches, "clocks": clk}
         print(json.dumps(line), flush=True)

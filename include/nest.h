@@ -218,6 +218,20 @@ typedef struct {
 } nest_ws_layout;
 int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out);
 
+/* ---- joint search over variants -------------------------------------------------
+ * Nest §5.2.3 explores the microbatch size together with the placement.  The
+ * variants of a problem (e.g. the same model with 1, 2, 4 and 8 samples per
+ * microbatch, M scaled to keep the global batch) are solved as consecutive
+ * instances of one batch; this picks, per group of `group` consecutive instances,
+ * the index within the group of the smallest t_batch, ties to the smaller index, -1
+ * when no variant is solved.
+ *   costs     DEVICE int64 [B], as written by nest_solve (may be the same stream's
+ *             output: the call is ordered after it on `stream`)
+ *   best_out  DEVICE int32 [B / group]
+ * Returns NEST_OK once the kernel is enqueued, NEST_E_INVALID when group < 1 or B is
+ * not a multiple of group, NEST_E_CUDA if the launch fails. */
+int nest_select_best(const int64_t *costs, int32_t B, int32_t group, int32_t *best_out, void *stream);
+
 /* ---- solve without allocation ------------------------------------------------
  * No counterpart in the paper: this serves callers that cannot allocate device
  * memory - a serving or scheduling process that has handed all device memory to its

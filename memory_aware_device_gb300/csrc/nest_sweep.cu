@@ -1042,6 +1042,7 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
     if (variant != 2 && g.Cmax <= 4) {
         double best = 0;
         SweepConfig pick = {};
+        int64_t pick_ctas = 0;   // CTAs of the pick resident at once
         const int cl_list[5] = {16, 8, 4, 2, 1};
         const int js_list[4] = {8, 4, 2, 1};
         for (int ci = 0; ci < 5; ci++) {
@@ -1075,14 +1076,18 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
                 if (score > best) {
                     best = score;
                     pick = {cs, js, 0, threads, 1, waves};
+                    pick_ctas = int64_t(cap) * cs;
                 }
                 if (jsplit_opt) break;
             }
             if (cluster_opt) break;
         }
-        // resident only when every cluster of the pass is resident at once: otherwise the
-        // streaming variant, whose CTAs need no co-scheduling, keeps the GPU fuller
-        if (best > 0 && (variant == 1 || pick.resident_waves == 1)) {
+        // resident when every cluster of the pass is resident at once, or when one wave
+        // of clusters holds at least 1.5 CTAs per SM (measured: 64 16-CTA clusters of
+        // 60 KB in 4 waves beat the streaming variant 2.7x); with larger rows (one CTA
+        // per SM, many waves) the streaming variant, whose CTAs need no co-scheduling,
+        // keeps the GPU fuller
+        if (best > 0 && (variant == 1 || pick.resident_waves == 1 || 2 * pick_ctas >= 3 * int64_t(sms))) {
             out = pick;
             if (std::getenv("NEST_DEBUG"))
                 std::fprintf(stderr, "nest: sweep resident, cluster %d jsplit %d threads %d\n", pick.cluster,

@@ -26,7 +26,7 @@ ERRORS = {NEST_E_INVALID: "invalid argument", NEST_E_LIMITS: "batch dimensions b
 # Every function declared in include/nest.h.
 EXPORTS = ("nest_record_layout", "nest_plan_bytes", "nest_workspace_size", "nest_workspace_size_costs",
            "nest_workspace_layout", "nest_solve", "nest_workspace_size_host", "nest_solve_host",
-           "nest_solve_static")
+           "nest_select_best", "nest_solve_static")
 KEEP_COSTS = 1   # NEST_KEEP_COSTS
 STATIC_SCRATCH_BYTES = 64 << 20   # NEST_STATIC_SCRATCH_BYTES
 
@@ -91,6 +91,7 @@ def lib():
         L.nest_solve_host.argtypes = [P(Dims), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
                                       C.c_void_p, P(Options)]
         L.nest_solve_static.argtypes = [P(Dims), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, P(Options)]
+        L.nest_select_best.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
         _lib = L
     return _lib
 
@@ -246,6 +247,20 @@ class Solver:
 
     def results(self) -> List[dict]:
         return decode_plans(self.plans.cpu().numpy(), self.dims)
+
+
+def select_best(costs, group: int, stream=None):
+    """nest_select_best on a torch int64 CUDA tensor of t_batch values: the best index
+    within each group of `group` consecutive instances (int32 tensor, -1 = none)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(costs.device)
+    best = torch.empty(costs.numel() // group if group > 0 else 0, dtype=torch.int32, device=costs.device)
+    rc = lib().nest_select_best(costs.data_ptr(), costs.numel(), group, best.data_ptr(),
+                                C.c_void_p(stream.cuda_stream))
+    if rc:
+        raise NestError(rc, "nest_select_best")
+    return best
 
 
 def solve_instances(instances: Sequence, device="cuda", **opt_kw) -> List[dict]:

@@ -93,6 +93,16 @@ def test_bad_arguments_rejected_before_any_launch():
     assert L.nest_solve_host(C.byref(zero), None, None, None, None, 0, None, None) == nest.NEST_OK
 
 
+def test_select_best_rejects_bad_groups_before_any_launch():
+    L = nest.lib()
+    fake = 1 << 20   # never dereferenced: the checks fail first
+    assert L.nest_select_best(fake, 8, 0, fake, None) == nest.NEST_E_INVALID
+    assert L.nest_select_best(fake, 10, 4, fake, None) == nest.NEST_E_INVALID
+    assert L.nest_select_best(fake, -4, 4, fake, None) == nest.NEST_E_INVALID
+    assert L.nest_select_best(None, 0, 4, None, None) == nest.NEST_OK
+    assert L.nest_select_best(None, 8, 4, fake, None) == nest.NEST_E_INVALID
+
+
 def test_workspace_grows_with_chunk_and_matches_layout():
     dims = nest.make_dims(synth.config_batch(3, B=8))
     a, b = nest.workspace_size(dims, 2), nest.workspace_size(dims, 8)

@@ -127,6 +127,33 @@ def test_mixed_schedules_in_one_launch():
             check_tables(s, b, insts[b])
 
 
+# Joint microbatch-size search: each problem's variants are consecutive instances
+def _joint_check(problems, **kw):
+    import torch
+    insts = synth.joint_batch(problems)
+    group = len(synth.MICROBATCH_SIZES)
+    s, res = G.run(insts, **kw)
+    best = nest.select_best(s.costs, group)
+    torch.cuda.synchronize()
+    best = best.cpu().tolist()
+    for g, x in enumerate(problems):
+        j = O.solve_joint(insts[g * group:(g + 1) * group])
+        for q in range(group):
+            assert G.same_result(res[g * group + q], j["results"][q]), (g, q)
+        assert best[g] == j["best"], (g, best[g], j["best"])
+    return best
+
+
+def test_joint_microbatch_search_workload2():
+    best = _joint_check(synth.config_batch(2, B=6))
+    assert len(set(best)) >= 1
+
+
+def test_joint_microbatch_search_random_tiny():
+    best = _joint_check([synth.random_tiny(4000 + k, Lmax=7, Dmax=16) for k in range(60)], Pcap=6)
+    assert -1 in best or len(set(best)) > 1   # the sample exercises different answers
+
+
 def test_workload3_full_batch():
     insts = synth.config_batch(3)
     s, res = G.run(insts)
