@@ -248,6 +248,8 @@ def main():
                     help="pipeline schedule of every instance (gpipe: all microbatches of a replica stashed)")
     ap.add_argument("--gpipe-microbatches", type=int, default=512,
                     help="microbatches per iteration under --schedule gpipe (4096 do not fit in memory)")
+    ap.add_argument("--topology", default="tiers", choices=["tiers", "torus"],
+                    help="torus: the dense workload's problems on a 4x4x4 torus of 64 chips, tiers = hop classes")
     ap.add_argument("--joint", action="store_true",
                     help="joint microbatch-size search: every problem solved with 1, 2, 4 and 8 samples "
                          "per microbatch, the best variant selected on the GPU")
@@ -259,6 +261,11 @@ def main():
     workload = f"{synth.CONFIG_NAMES[args.workload]}"
     B = synth.CONFIG_BATCH[args.workload]
     instances = rank_instances(args.workload, rank)
+    if args.topology == "torus":
+        if args.workload != 2:
+            raise SystemExit("--topology torus applies to workload 2 (64 devices)")
+        instances = [synth.torus_instance(rank * B + b) for b in range(B)]
+        workload = synth.TORUS_NAME
     if args.schedule == "gpipe":
         for x in instances:
             x.schedule, x.M = 1, max(args.gpipe_microbatches, x.Pmax)

@@ -257,3 +257,65 @@ def microbatch_variant(inst: Instance, mbs: int, global_batch: int = GLOBAL_BATC
 def joint_batch(problems: Sequence[Instance], sizes=MICROBATCH_SIZES) -> List[Instance]:
     """Every problem expanded into its microbatch variants, consecutively."""
     return [microbatch_variant(x, b) for x in problems for b in sizes]
+
+
+# Torus and mesh clusters (Nest Appendix C, §4 "non-uniform mesh"): tiers are
+# hop-distance classes - direct neighbours, two hops, and the rest ("remote", behind
+# slower inter-mesh links).  For the DP a tier is a group size G (a power of two),
+# a bandwidth and a latency: G_t is the largest power-of-two block of chips whose
+# torus diameter is within the class's hop distance, the latency is that many hops,
+# and the remote class reaches every chip.
+
+def torus_block_diameter(shape, block) -> int:
+    """Largest hop distance between two chips of an axis-aligned block on a torus
+    (wrap-around links on every axis): along an axis of length n, a block of a chips
+    spans a - 1 hops, or floor(n / 2) when it covers the whole ring."""
+    d = 0
+    for n, a in zip(shape, block):
+        d += n // 2 if a == n else a - 1
+    return d
+
+
+def _blocks(shape, g):
+    """Axis-aligned blocks of g chips that fit in the torus (power-of-two sides)."""
+    sides = [[a for a in (1 << k for k in range(12)) if a <= n] for n in shape]
+    for block in itertools.product(*sides):
+        if int(np.prod(block)) == g:
+            yield block
+
+
+def torus_tiers(shape=(4, 4, 4), hops=(1, 2), link_gbs=50.0, hop_us=1.0, remote_gbs=12.5, remote_us=5.0):
+    """(G, bandwidth, latency) arrays for the hop classes of a torus: for each hop
+    limit h the largest power-of-two block of diameter <= h, then the whole torus."""
+    N = int(np.prod(shape))
+    best = {}   # g -> smallest diameter of a g-chip block
+    g = 1
+    while g <= N:
+        ds = [torus_block_diameter(shape, b) for b in _blocks(shape, g)]
+        if ds:
+            best[g] = min(ds)
+        g *= 2
+    G, bw, lat = [], [], []
+    for h in hops:
+        fit = [g for g, d in best.items() if d <= h and g < N]
+        if fit and (not G or max(fit) > G[-1]):
+            G.append(max(fit))
+            bw.append(link_gbs)
+            lat.append(h * hop_us)
+    G.append(N)
+    bw.append(remote_gbs)
+    lat.append(remote_us)
+    return _tiers(G, bw, lat)
+
+
+TORUS_NAME = "dense-32L-h4096-64chip-torus4x4x4"
+
+
+def torus_instance(b: int, shape=(4, 4, 4)) -> Instance:
+    """Workload 2's model and budgets on a 4x4x4 torus of 64 chips: tiers are the
+    1-hop pairs, the 2-hop 2x2 squares and the whole torus (remote)."""
+    x = config_instance(2, b)
+    G, bw, lat = torus_tiers(shape)
+    x.tierG, x.tierBw, x.tierLat = G, bw, lat
+    x.cand = np.arange(len(G), dtype=np.int32)
+    return x

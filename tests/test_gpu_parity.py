@@ -154,6 +154,17 @@ def test_joint_microbatch_search_random_tiny():
     assert -1 in best or len(set(best)) > 1   # the sample exercises different answers
 
 
+# Torus cluster: hop-distance tiers (1-hop pairs, 2-hop squares, the whole torus)
+def test_torus_workload_all_tables():
+    insts = [synth.torus_instance(b) for b in range(16)]
+    s, res = G.run(insts)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), b
+    for b in (0, 9, 15):
+        check_tables(s, b, insts[b])
+
+
 def test_workload3_full_batch():
     insts = synth.config_batch(3)
     s, res = G.run(insts)
