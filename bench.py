@@ -92,6 +92,20 @@ def alu_peak_relax_per_s(sm_mhz):
     return SMS * INT32_LANES * sm_mhz * 1e6 / OPS_PER_RELAX
 
 
+def measured_relax_peak(wide: int = 0):
+    """Relaxations/s of the relaxation arithmetic alone (one max, one compare, two
+    selects per candidate and cell, values in registers, every SM busy), from the
+    microbenchmark built next to the library; None if it cannot run."""
+    try:
+        from memory_aware_device_gb300 import build as nbuild
+        lib = ctypes.CDLL(nbuild.build_peak())
+        lib.nest_peak_relax.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+        out = ctypes.c_double()
+        return out.value if lib.nest_peak_relax(wide, 4096, ctypes.byref(out)) == 0 else None
+    except (OSError, RuntimeError):
+        return None
+
+
 def stored_traffic(kernel, workload):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -419,12 +433,19 @@ def main():
     words = sum(cost_words(x) for x in instances)
     if dom == "dp_sweep":
         mhz = (clk or {}).get("sm_mhz") or peaks["sm_max_mhz"]
-        peak = alu_peak_relax_per_s(peaks["sm_max_mhz"]) / 1e9
+        derived = alu_peak_relax_per_s(peaks["sm_max_mhz"]) / 1e9
         achieved = relax_total / (dom_ms * 1e-3) / 1e9
+        meas = measured_relax_peak(0)
+        peak = meas / 1e9 if meas else derived
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Grelax/s",
                 "frac": achieved / peak, "traffic": stored_traffic(dom, workload), "kernel": dom,
-                "peak_source": f"derived: {SMS} SMs x {INT32_LANES} INT32 lanes x {peaks['sm_max_mhz']:.0f} MHz"
-                               f" / {OPS_PER_RELAX} ops per relaxation", "sm_mhz_seen": mhz}
+                "peak_source": ("measured: register-only microbenchmark of the relaxation arithmetic on 32-bit "
+                                "words (max, compare, two selects per candidate and cell; 4 independent chains "
+                                "per thread, every SM full) - the words this batch's sweep runs on"
+                                if meas else
+                                f"derived: {SMS} SMs x {INT32_LANES} INT32 lanes x {peaks['sm_max_mhz']:.0f} MHz"
+                                f" / {OPS_PER_RELAX} ops per relaxation"),
+                "derived_64bit_peak": derived, "sm_mhz_seen": mhz}
     else:
         # the per-position loads table is what the stage-loads kernel must write
         loads_bytes = sum(8 * x.Pmax * (x.L * (x.L + 1) // 2) * (x.D // x.unit).bit_length() for x in instances)

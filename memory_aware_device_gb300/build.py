@@ -69,6 +69,23 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     return OUT
 
 
+PEAK_SRC = os.path.join(HERE, "peak", "relax_peak.cu")
+PEAK_OUT = os.path.join(HERE, "libnest_peak.so")
+
+
+def build_peak(force: bool = False) -> str:
+    """Compile (if stale) the relaxation-peak microbenchmark used by bench.py."""
+    if not force and os.path.exists(PEAK_OUT) and os.path.getmtime(PEAK_OUT) >= os.path.getmtime(PEAK_SRC):
+        return PEAK_OUT
+    tmp = PEAK_OUT + f".{os.getpid()}.tmp"
+    r = subprocess.run([nvcc(), *ARCH, *FLAGS, "-shared", PEAK_SRC, "-o", tmp], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {PEAK_SRC}:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, PEAK_OUT)
+    return PEAK_OUT
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
                 extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else []))
+    print(build_peak(force="--force" in sys.argv))
