@@ -591,6 +591,13 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         }
     };
     a_rows(L - 1, tid);
+    // the next position's row and barrier base in its owner's shared memory, for this
+    // thread's first slot (the common case has one slot per CTA); rows of step i sit
+    // i * Hrow values and i barriers further on
+    const int p0 = rank + 1 + kg * cs;
+    const bool has0 = kg < nown_live && p0 < s.P;
+    const uint32_t rrow0 = has0 ? cluster_map(H + (p0 / cs) * sp.Hslot + sp.Hpad, uint32_t(p0 % cs)) : 0;
+    const uint32_t bar0 = has0 ? cluster_map(&rowbar[(p0 / cs) * g.Lmax], uint32_t(p0 % cs)) : 0;
     cluster_sync();  // first A rows built, pads and barriers set, every CTA started: pushes may begin
 
     int64_t ro = row_offset(L - 1, L);   // row_offset(i, L) of the current step
@@ -606,6 +613,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         const int n = L - i - 2 > 0 ? L - i - 2 : 0;
         const int cnt = n > js ? (n - js + jsplit - 1) >> lgs : 0;
         const int items = cnt + (js == jlast ? 1 : 0);
+
         for (int k = kg; k < nown_live; k += ngrp) {
             const int p = rank + 1 + k * cs;
             V bv[CT][NA];   // running bests
@@ -686,14 +694,21 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
             // owner of position p + 1 (its slot p / cs, row i), value and argument to the
             // staged dp row that is copied to global memory after the step
             const bool push = p < s.P && i > 0;
-            const uint32_t crank = uint32_t(p % cs);
-            const uint32_t rrow = push ? cluster_map(H + (p / cs) * sp.Hslot + i * sp.Hrow + sp.Hpad, crank) : 0;
-            const uint32_t bar = push ? cluster_map(&rowbar[(p / cs) * g.Lmax + i], crank) : 0;
+            uint32_t rrow = 0, bar = 0;
+            if (push && k == kg) {
+                rrow = rrow0 + uint32_t(i * sp.Hrow * int(sizeof(V)));
+                bar = bar0 + uint32_t(8 * i);
+            } else if (push) {
+                const uint32_t crank = uint32_t(p % cs);
+                rrow = cluster_map(H + (p / cs) * sp.Hslot + i * sp.Hrow + sp.Hpad, crank);
+                bar = cluster_map(&rowbar[(p / cs) * g.Lmax + i], crank);
+            }
             const int so = ((i & 1) * nown + k) * sp.Srow;
+            const bool aborted = abort_flag;
 #pragma unroll
             for (int c = 0; c < CT; c++) {
                 if (c >= C || (c & (jsplit - 1)) != js) continue;
-                const uint64_t kc = abort_flag ? kInf : key[c];
+                const uint64_t kc = aborted ? kInf : key[c];
                 const int at = c * g.Dpad + d, ht = c * sp.Hcol + d;
                 if (dlive) {
                     sdv[so + at] = int64_t(kc >> 24);
@@ -707,7 +722,8 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
                 }
             }
         }
-        // the A rows of step i - 1, into the other buffer (last read at step i + 1)
+        // the A rows of step i - 1, into the other buffer (last read at step i + 1), after
+        // this step's pushes (which the neighbour is waiting for)
         if (a_mine) a_entry(a_dst + ((i - 1) & 1) * sp.Abuf + i * sp.Aj, i - 1, i + a_r, a_m, pre);
         if (i > 0 && a_total > int(blockDim.x)) a_rows(i - 1, tid + blockDim.x);
         // the staged rows of step i go to global memory by bulk copies; those of step
