@@ -1,0 +1,511 @@
+// Device bodies shared by the pass kernels: the prep of one instance, the stage
+// loads of a range of its stages, and its backtrack.  The standalone kernels
+// (nest_prep.cu, nest_loads.cu, nest_backtrack.cu) run them one after the other;
+// the fused resident sweep (nest_sweep.cu) runs all of them inside one launch.
+//
+// Nest (Network- and Memory-Aware Device Placement): §3.2 (per-layer metadata), §3.3
+// (memory model, stash by schedule), §4 load() and Eq. 3 (stage latency, link terms,
+// strategy minimum per stage), Appendix K Algorithm 1 (final batch-time loop and
+// stage reconstruction); see the three kernel files for the details of each step.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "nest_internal.cuh"
+
+namespace nest {
+
+// Shared scratch of prep_instance: two flags, the record, the layer values and the
+// sparse table (byte offsets).
+struct PrepScratch {
+    int64_t flags, rec, sv, sst, bytes;
+};
+
+__host__ __device__ inline PrepScratch prep_scratch(const Geo &g, const nest_layout &rl) {
+    PrepScratch s;
+    s.flags = 0;
+    s.rec = 128;
+    s.sv = s.rec + align_up(rl.record_bytes, 128);
+    s.sst = s.sv + align_up(8 * int64_t(kNumPfx) * g.Lmax, 128);
+    s.bytes = s.sst + align_up(8 * int64_t(kLogL) * g.Lmax, 128);
+    return s;
+}
+
+__device__ __forceinline__ bool pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+__device__ __forceinline__ int ilog2(int64_t v) { return 63 - __clzll(v); }
+
+// The prep of instance b (validation, prefix sums, sparse table, link table,
+// strategy codes, invariant divisors) into its prep block in the workspace, using
+// `scr` (prep_scratch bytes of shared memory).  Every thread of the block calls it.
+static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsigned char *scr) {
+    const PrepScratch ps = prep_scratch(a.g, a.rl);
+    int &bad = *reinterpret_cast<int *>(scr + ps.flags);
+    uint32_t &xmax = *reinterpret_cast<uint32_t *>(scr + ps.flags + 4);
+    unsigned char *rec_s = scr + ps.rec;
+    int64_t *sv = reinterpret_cast<int64_t *>(scr + ps.sv);     // [kNumPfx][Lmax], scanned in place
+    int64_t *sst = reinterpret_cast<int64_t *>(scr + ps.sst);   // [kLogL][Lmax], sparse table of max(aw)
+    const int LM = a.g.Lmax;
+    {   // one coalesced pass over the record; everything below reads shared memory
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.records + int64_t(b) * a.rl.record_bytes);
+        uint4 *dst = reinterpret_cast<uint4 *>(rec_s);
+        for (int q = threadIdx.x; q < int(a.rl.record_bytes / 16); q += blockDim.x) dst[q] = src[q];
+    }
+    __syncthreads();
+    const unsigned char *rec = rec_s;
+    const nest_record_header h = *reinterpret_cast<const nest_record_header *>(rec);
+    PrepHdr *ph = prep_hdr(a, b);
+    unsigned char *pb = reinterpret_cast<unsigned char *>(ph);
+    const Geo &g = a.g;
+    if (threadIdx.x == 0) {
+        int bd = 0;
+        bd |= h.L < 1 || h.L > g.Lmax;
+        bd |= !pow2(h.unit) || h.D < h.unit || h.D > 8192 || (h.unit > 0 && h.D % h.unit);
+        bd |= h.unit > 0 && h.D / h.unit > g.Dumax;
+        bd |= h.T < 1 || h.T > g.Tmax;
+        bd |= h.C < 1 || h.C > g.Cmax;
+        bd |= h.S < 1 || h.S > g.Smax;
+        bd |= h.Pmax < 1 || h.Pmax > g.Pcap;
+        bd |= h.M < h.Pmax || h.M > (int64_t(1) << 20);
+        bd |= h.R < 1 || h.R > (int64_t(1) << 40);
+        bd |= h.budget < 0 || h.budget > (int64_t(1) << 62);
+        bd |= h.opt_factor < 0 || h.opt_factor > 16;
+        bd |= h.schedule < 0 || h.schedule > 1;
+        bad = bd;
+    }
+    __syncthreads();
+    if (!bad) {
+        const int64_t *G = reinterpret_cast<const int64_t *>(rec + a.rl.G);
+        const int64_t *bw = reinterpret_cast<const int64_t *>(rec + a.rl.bw);
+        const int64_t *lat = reinterpret_cast<const int64_t *>(rec + a.rl.lat);
+        const int32_t *cand = reinterpret_cast<const int32_t *>(rec + a.rl.cand);
+        const int16_t *st = reinterpret_cast<const int16_t *>(rec + a.rl.strat);
+        int bd = 0;
+        for (int l = threadIdx.x; l < h.L; l += blockDim.x) {
+            const int64_t *arr[5] = {
+                reinterpret_cast<const int64_t *>(rec + a.rl.pd), reinterpret_cast<const int64_t *>(rec + a.rl.pe),
+                reinterpret_cast<const int64_t *>(rec + a.rl.ao), reinterpret_cast<const int64_t *>(rec + a.rl.aw),
+                reinterpret_cast<const int64_t *>(rec + a.rl.a2a)};
+            const int64_t f = reinterpret_cast<const int64_t *>(rec + a.rl.fl)[l];
+            bd |= f < 0 || f > (int64_t(1) << 48);
+            for (int q = 0; q < 5; q++) bd |= arr[q][l] < 0 || arr[q][l] > (int64_t(1) << 38);
+            bd |= rec[a.rl.moe + l] > 1;
+        }
+        for (int t = threadIdx.x; t < h.T; t += blockDim.x) {
+            bd |= !pow2(G[t]) || (t > 0 && G[t] <= G[t - 1]);
+            bd |= bw[t] < 1000 || bw[t] > (int64_t(1) << 40);
+            bd |= lat[t] < 0 || lat[t] > (int64_t(1) << 24);
+        }
+        if (threadIdx.x == 0) bd |= G[h.T - 1] < h.D;
+        for (int c = threadIdx.x; c < h.C; c += blockDim.x) {
+            bd |= cand[c] < 0 || cand[c] >= h.T || (c > 0 && cand[c] <= cand[c - 1]);
+        }
+        for (int s = threadIdx.x; s < h.S; s += blockDim.x) {
+            const int16_t *x = st + 8 * s;
+            for (int f = 0; f < 3; f++) bd |= !pow2(x[f]) || x[f] > 8192;
+            bd |= x[3] < 0 || x[3] > 3 || x[4] < 0 || x[4] > 1;
+        }
+        bd = __syncthreads_or(bd);
+        if (threadIdx.x == 0) bad = bd;
+        __syncthreads();
+    }
+    if (bad) {
+        if (threadIdx.x == 0) ph->status = NEST_BAD_INPUT;
+        return;
+    }
+
+    const int L = h.L;
+    const int64_t Du = h.D / h.unit;
+    if (threadIdx.x == 0) {
+        ph->L = L;
+        ph->D = h.D;
+        ph->unit = h.unit;
+        ph->lu = ilog2(h.unit);
+        ph->Du = int32_t(Du);
+        ph->K = ilog2(Du) + 1;
+        ph->T = h.T;
+        ph->C = h.C;
+        ph->S = h.S;
+        ph->P = h.Pmax;
+        ph->R = h.R;
+        ph->M = h.M;
+        ph->budget = h.budget;
+        ph->opt = h.opt_factor;
+        ph->schedule = h.schedule;
+    }
+    const int64_t *G = reinterpret_cast<const int64_t *>(rec + a.rl.G);
+    const int64_t *bw = reinterpret_cast<const int64_t *>(rec + a.rl.bw);
+    const int64_t *lat = reinterpret_cast<const int64_t *>(rec + a.rl.lat);
+    const int32_t *cand = reinterpret_cast<const int32_t *>(rec + a.rl.cand);
+    for (int t = threadIdx.x; t < 8; t += blockDim.x) {
+        ph->G[t] = t < h.T ? G[t] : 0;
+        ph->bw[t] = t < h.T ? bw[t] : 1;
+        ph->lat[t] = t < h.T ? lat[t] : 0;
+        ph->bwdiv[t] = make_divisor(uint64_t(t < h.T ? bw[t] : 1));
+    }
+    if (threadIdx.x == 8) ph->Mdiv = make_divisor(uint64_t(h.M));
+    if (threadIdx.x == 9) ph->Rdiv = make_divisor(uint64_t(h.R));
+    for (int x = threadIdx.x; x < 16; x += blockDim.x) {
+        int t = 0;
+        while (t < h.T - 1 && G[t] < (int64_t(1) << x)) t++;
+        ph->tier_log[x] = int8_t(t);
+    }
+    for (int c = threadIdx.x; c < 16; c += blockDim.x) {
+        int ml = -1;
+        if (c < h.C) {
+            const int64_t cap = G[cand[c]];
+            for (int m = 0; m < 16; m++)
+                if (2 * (int64_t(h.unit) << m) <= cap) ml = m;
+        }
+        ph->cand[c] = c < h.C ? cand[c] : 0;
+        ph->mlim[c] = ml;
+    }
+
+    // prefix sums and the sparse table, built in shared memory: the layer arrays are
+    // read once with coalesced loads, each array is scanned by one warp, and the
+    // results are written back with coalesced stores
+    int64_t *pfx = reinterpret_cast<int64_t *>(pb + a.pl.pfx);
+    int64_t *ao = reinterpret_cast<int64_t *>(pb + a.pl.ao);
+    int64_t *awst = reinterpret_cast<int64_t *>(pb + a.pl.awst);
+    {
+        const int64_t off[6] = {a.rl.fl, a.rl.pd, a.rl.pe, a.rl.ao, a.rl.aw, a.rl.a2a};
+        for (int e = threadIdx.x; e < kNumPfx * L; e += blockDim.x) {
+            const int q = e / L, l = e % L;
+            const int64_t v = q == kNm ? int64_t(rec[a.rl.moe + l]) : reinterpret_cast<const int64_t *>(rec + off[q])[l];
+            sv[q * LM + l] = v;
+            if (q == kAw) sst[l] = v;
+            if (q == kAo) ao[l] = v;
+        }
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int q = warp; q < kNumPfx; q += int(blockDim.x >> 5)) {
+        int64_t carry = 0;
+        for (int base = 0; base < L; base += 32) {
+            int64_t x = base + lane < L ? sv[q * LM + base + lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            x += carry;
+            if (base + lane < L) sv[q * LM + base + lane] = x;
+            carry = __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
+    }
+    for (int lv = 1; lv < kLogL; lv++) {
+        const int span = 1 << (lv - 1);
+        for (int l = threadIdx.x; l < L; l += blockDim.x) {
+            const int64_t x = sst[(lv - 1) * LM + l];
+            const int64_t y = l + span < L ? sst[(lv - 1) * LM + l + span] : x;
+            sst[lv * LM + l] = x > y ? x : y;
+        }
+        __syncthreads();
+    }
+    for (int e = threadIdx.x; e < kNumPfx * (L + 1); e += blockDim.x) {
+        const int q = e / (L + 1), l = e % (L + 1);
+        pfx[int64_t(q) * (g.Lmax + 1) + l] = l == 0 ? 0 : sv[q * LM + l - 1];
+    }
+    for (int e = threadIdx.x; e < kLogL * L; e += blockDim.x) {
+        const int lv = e / L, l = e % L;
+        awst[int64_t(lv) * g.Lmax + l] = sst[lv * LM + l];
+    }
+    const int64_t *ao_in = reinterpret_cast<const int64_t *>(rec + a.rl.ao);
+    int64_t *X = reinterpret_cast<int64_t *>(pb + a.pl.X);
+    if (threadIdx.x == 0) xmax = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < (L + 1) * h.C; e += blockDim.x) {
+        const int bnd = e / h.C, c = e % h.C;
+        int64_t v = 0;
+        if (bnd > 0 && bnd < L) {
+            const int tr = cand[c];
+            v = lat[tr] + cdiv(ao_in[bnd - 1] * 1000, bw[tr]);
+        }
+        X[int64_t(bnd) * g.Cmax + c] = v;
+        atomicMax(&xmax, v < 0x7FFFFFFF ? uint32_t(v) : 0x7FFFFFFFu);
+    }
+    uint32_t *sp = reinterpret_cast<uint32_t *>(pb + a.pl.strat);
+    const int16_t *st = reinterpret_cast<const int16_t *>(rec + a.rl.strat);
+    for (int s = threadIdx.x; s < h.S; s += blockDim.x) {
+        const int16_t *x = st + 8 * s;
+        sp[s] = uint32_t(ilog2(x[0])) | uint32_t(ilog2(x[1])) << 4 | uint32_t(ilog2(x[2])) << 8 |
+                uint32_t(x[3]) << 12 | uint32_t(x[4]) << 14;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ph->maxX32 = xmax;
+        ph->maxload32 = 0;   // raised by the strategy reduction
+        ph->status = NEST_SOLVED;
+    }
+}
+
+
+__device__ __forceinline__ int64_t up_shift(int64_t x, int l) { return (x + (int64_t(1) << l) - 1) >> l; }
+
+struct Net {
+    const PrepHdr *ph;
+    // Ring-model cost of cnt collectives moving V bytes in total over 2^ln devices on
+    // tier tr; phi = 2 for AllReduce, 1 for AllGather / ReduceScatter / AllToAll.
+    __device__ __forceinline__ int64_t coll(int64_t phi, int ln, int tr, int64_t V, int64_t cnt) const {
+        if (ln == 0 || V == 0) return 0;
+        const int64_t pv = phi * V;
+        const int64_t per_device = pv - (pv >> ln);  // ceil(phi (n - 1) V / n)
+        const int64_t steps = cnt * phi * ((int64_t(1) << ln) - 1) * ph->lat[tr];
+        return steps + int64_t(divide_up(uint64_t(per_device) * 1000, uint64_t(ph->bw[tr]), ph->bwdiv[tr]));
+    }
+};
+
+// The K width words (tau << 8) | pmax of stage [i, j) under strategy s, handed to
+// emit(m, word); all ones where the strategy does not apply at that width.
+template <typename Emit>
+__device__ __forceinline__ void stage_words(const PrepHdr *ph, const unsigned char *pb, const PrepLayout &pl,
+                                            const Geo &g, int i, int j, int s, Emit emit) {
+    const int K = ph->K, lu = ph->lu;
+    const uint32_t code = reinterpret_cast<const uint32_t *>(pb + pl.strat)[s];
+    const int lt = code & 15, lcp = (code >> 4) & 15, le = (code >> 8) & 15;
+    const int z = (code >> 12) & 3, r = (code >> 14) & 1;
+    const int64_t *pfx = reinterpret_cast<const int64_t *>(pb + pl.pfx);
+    const int64_t ld = g.Lmax + 1;
+    const int64_t nM = pfx[kNm * ld + j] - pfx[kNm * ld + i];
+    // valid for some width iff t cp e <= the widest stage, and e > 1 only over MoE layers
+    const int lmin = lt + lcp + le - lu;  // smallest m that admits the strategy
+    if (lmin > K - 1 || (le > 0 && nM == 0)) {
+        for (int m = 0; m < K; m++) emit(m, kInf);
+        return;
+    }
+    auto sum = [&](int q) { return pfx[q * ld + j] - pfx[q * ld + i]; };
+    const int64_t Fl = sum(kFl), Pd = sum(kPd), Pe = sum(kPe), Ao = sum(kAo), Aw = sum(kAw), A2 = sum(kA2);
+    const int64_t nL = j - i;
+    const Net net{ph};
+
+    // width-independent terms: groups inside one replica
+    const int64_t comp = int64_t(divide_up(uint64_t(up_shift(Fl * (3 + r), lt + lcp)), uint64_t(ph->R), ph->Rdiv));
+    const int64_t rep = comp + net.coll(2, lt, ph->tier_log[lt], 4 * up_shift(Ao, lcp), 4 * nL) +
+                        net.coll(1, lcp, ph->tier_log[lt + lcp], 4 * up_shift(Ao, lt), 4 * nL) +
+                        net.coll(1, le, ph->tier_log[lt + lcp + le], 4 * up_shift(A2, lt + lcp), 4 * nM);
+    const int64_t Wd = up_shift(Pd, lt), We = up_shift(Pe, lt + le);
+    int64_t act, stash;
+    if (r) {
+        const int64_t *ao = reinterpret_cast<const int64_t *>(pb + pl.ao);
+        const int64_t *awst = reinterpret_cast<const int64_t *>(pb + pl.awst);
+        const int lv = 31 - __clz(j - i);
+        const int64_t m1 = awst[int64_t(lv) * g.Lmax + i], m2 = awst[int64_t(lv) * g.Lmax + j - (1 << lv)];
+        act = up_shift(m1 > m2 ? m1 : m2, lt + lcp);
+        stash = up_shift(i > 0 ? ao[i - 1] : ao[0], lt + lcp);
+    } else {
+        act = up_shift(Aw, lt + lcp);
+        stash = act;
+    }
+    const int64_t opt = ph->opt, budget = ph->budget, M = ph->M;
+    const int P = ph->P;
+    const float inv_stash = stash > 0 ? 1.0f / float(stash) : 0.0f;
+    const int64_t mult = z == 0 ? 1 : (z < 3 ? 2 : 1);
+    const int64_t phi_s = z == 0 ? 2 : 1;
+    for (int m = 0; m < K; m++) {
+        uint64_t word = kInf;
+        if (m >= lmin) {
+            const int lq = lu + m - lt - lcp, lqe = lq - le;
+            const int tk = ph->tier_log[lu + m];
+            const int64_t z3 =
+                z == 3 ? net.coll(1, lq, tk, 2 * Wd, 2 * nL) + net.coll(1, lqe, tk, 2 * We, 2 * nM) : 0;
+            const int64_t sync = mult * (net.coll(phi_s, lq, tk, Wd, nL) + net.coll(phi_s, lqe, tk, We, nM));
+            const int64_t tau = up_shift(rep + z3, lq) + int64_t(divide_up(uint64_t(sync), uint64_t(M), ph->Mdiv));
+            if (tau < kCap) {
+                const int64_t sh = up_shift(Wd, lq) + up_shift(We, lqe);
+                const int64_t w = z == 3 ? sh : Wd + We;
+                const int64_t gr = z >= 2 ? sh : Wd + We;
+                const int64_t o = z >= 1 ? up_shift(opt * Wd, lq) + up_shift(opt * We, lqe) : opt * (Wd + We);
+                const int64_t stat = w + gr + o + act;
+                int pmax;
+                if (stat > budget) {
+                    pmax = 0;
+                } else if (ph->schedule == 1) {
+                    // GPipe: ceil(M / q) stashed microbatches; exact 128-bit product
+                    const uint64_t inflight = uint64_t((M + (int64_t(1) << lq) - 1) >> lq);
+                    const uint64_t lo = uint64_t(stash) * inflight, hi = __umul64hi(uint64_t(stash), inflight);
+                    pmax = hi == 0 && lo <= uint64_t(budget - stat) ? P : 0;
+                } else if (stash == 0) {
+                    pmax = P;
+                } else {
+                    // largest p <= P with (p - 1) stash <= budget - stat
+                    const int64_t rem = budget - stat;
+                    int p = 1 + int(fminf(float(rem) * inv_stash, 64.0f));
+                    p = p > P ? P : p;
+                    while (p > 1 && int64_t(p - 1) * stash > rem) p--;
+                    while (p < P && int64_t(p) * stash <= rem) p++;
+                    pmax = p;
+                }
+                word = (uint64_t(tau) << 8) | uint64_t(pmax);
+            }
+        }
+        emit(m, word);
+    }
+}
+
+// The per-position loads of stages pair0 .. pair0 + ppc - 1 of instance b, from a
+// copy of its prep block in shared memory (`smem`, status solved), with `bucket`
+// ([ppc][Kmax][Pcap + 1] uint64) and one word `bmax` of shared scratch.  spt threads
+// per stage run over its strategies (ppc * spt <= blockDim.x).  Every thread of the
+// block calls it.
+static __device__ __noinline__ void loads_slice(const PassArgs &a, int b, const unsigned char *smem, int64_t pair0, int ppc,
+                                         int spt, uint64_t *bucket, uint32_t *bmax_s) {
+    const Geo &g = a.g;
+    const PrepLayout &pl = a.pl;
+    const PrepHdr *ph = reinterpret_cast<const PrepHdr *>(smem);
+    const int L = ph->L, S = ph->S, K = ph->K, P = ph->P;
+    const int64_t npairs = int64_t(L) * (L + 1) / 2;
+    if (pair0 >= npairs) return;             // uniform over the CTA
+    const int rowp = g.Pcap + 1;
+    for (int q = threadIdx.x; q < ppc * g.Kmax * rowp; q += blockDim.x) bucket[q] = kInf;
+    __syncthreads();
+
+    const int lp = threadIdx.x / spt, s0 = threadIdx.x % spt;
+    const int64_t pair = pair0 + lp;
+    if (lp < ppc && pair < npairs) {
+        // invert pair = row_offset(i) + (j - i - 1)
+        int i = int((2.0f * L + 1.0f - sqrtf((2.0f * L + 1.0f) * (2.0f * L + 1.0f) - 8.0f * float(pair))) * 0.5f);
+        if (i < 0) i = 0;
+        if (i > L - 1) i = L - 1;
+        while (i > 0 && row_offset(i, L) > pair) i--;
+        while (i < L - 1 && row_offset(i + 1, L) <= pair) i++;
+        const int j = i + 1 + int(pair - row_offset(i, L));
+        uint64_t *bk = bucket + lp * g.Kmax * rowp;
+        uint64_t *cout = a.keep_costs ? reinterpret_cast<uint64_t *>(a.ws + a.w.cost) + int64_t(b) * a.w.cost_stride +
+                                            pair * g.Kmax * g.Spad
+                                      : nullptr;
+        for (int s = s0; s < S; s += spt) {
+            stage_words(ph, smem, pl, g, i, j, s, [&](int m, uint64_t w) {
+                if (cout) cout[int64_t(m) * g.Spad + s] = w;
+                const int pm = w == kInf ? 0 : int(w & 0xFF);
+                if (pm == 0) return;
+                const uint64_t key = ((w >> 8) << 16) | uint64_t(s);
+                uint64_t *slot = bk + m * rowp + pm;
+                if (key < *slot) atomicMin(reinterpret_cast<unsigned long long *>(slot), key);
+            });
+        }
+    }
+    __syncthreads();
+    // suffix minimum over pmax: position p takes the strategies with pmax >= p
+    uint64_t *out = reinterpret_cast<uint64_t *>(a.ws + a.w.loads) + int64_t(b) * a.w.loads_stride;
+    const int64_t pos_stride = int64_t(g.NP) * g.Kpad;
+    uint32_t tmax = 0;   // largest finite tau written, saturated at 2^31 - 1
+    for (int r = threadIdx.x; r < ppc * K; r += blockDim.x) {
+        const int q = r / K, m = r % K;
+        const int64_t pr = pair0 + q;
+        if (pr >= npairs) continue;
+        const uint64_t *bq = bucket + (q * g.Kmax + m) * rowp;
+        uint64_t cur = kInf;
+        for (int p = P; p >= 1; p--) {
+            cur = bq[p] < cur ? bq[p] : cur;
+            out[int64_t(p - 1) * pos_stride + pr * g.Kpad + m] = cur;
+            if (cur != kInf) {
+                const uint64_t tau = cur >> 16;
+                const uint32_t t32 = tau < 0x7FFFFFFFu ? uint32_t(tau) : 0x7FFFFFFFu;
+                tmax = t32 > tmax ? t32 : tmax;
+            }
+        }
+    }
+    // one atomic per CTA: the sweep keeps 32-bit words when every value is small
+    if (threadIdx.x == 0) *bmax_s = 0;
+    __syncthreads();
+    tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
+    if ((threadIdx.x & 31) == 0 && tmax) atomicMax(bmax_s, tmax);
+    __syncthreads();
+    if (threadIdx.x == 0 && *bmax_s) atomicMax(&prep_hdr(a, b)->maxload32, *bmax_s);
+    __syncthreads();   // the buckets and bmax may be reused
+}
+
+
+// The final batch-time loop and the plan of instance b, by one whole warp; `walk`
+// is 64 ints of shared scratch for the warp (stage q -> (i | j << 8 | m << 16 |
+// c' << 20, p)).
+static __device__ __noinline__ void backtrack_warp(const PassArgs &a, int b, int *walk) {
+    const int lane = threadIdx.x & 31;
+    const PrepHdr *ph = prep_hdr(a, b);
+    nest_plan_header *hdr = reinterpret_cast<nest_plan_header *>(a.plans_out + int64_t(b) * a.plan_stride);
+    nest_stage *st = reinterpret_cast<nest_stage *>(hdr + 1);
+    int status = ph->status;
+    const Geo &g = a.g;
+    const int64_t row_cells = int64_t(g.Cmax) * g.Dpad;
+    const int64_t pos_cells = int64_t(g.Lmax) * row_cells;
+    const int64_t *dpv = reinterpret_cast<const int64_t *>(a.ws + a.w.dpv) + int64_t(b) * a.w.dp_stride;
+    const uint32_t *dpa = reinterpret_cast<const uint32_t *>(a.ws + a.w.dpa) + int64_t(b) * a.w.dp_stride;
+    const uint64_t *loads = reinterpret_cast<const uint64_t *>(a.ws + a.w.loads) + int64_t(b) * a.w.loads_stride;
+
+    // smallest (t_batch, p); t_batch < 2^61
+    long long bt = -1;
+    int bp = 0;
+    if (status == NEST_SOLVED) {
+        const int L = ph->L, P = ph->P, Du = ph->Du;
+        for (int p = lane + 1; p <= P && p <= L; p += 32) {
+            const int64_t v = dpv[int64_t(p - 1) * pos_cells + Du];  // (i = 0, c = 0, d = Du)
+            if (v < kCap) {
+                const long long t = (long long)(v) * (long long)(ph->M + p - 1);
+                if (bp == 0 || t < bt) {
+                    bt = t;
+                    bp = p;
+                }
+            }
+        }
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        const long long ot = __shfl_xor_sync(0xffffffffu, bt, off);
+        const int op = __shfl_xor_sync(0xffffffffu, bp, off);
+        if (op != 0 && (bp == 0 || ot < bt || (ot == bt && op < bp))) {
+            bt = ot;
+            bp = op;
+        }
+    }
+    if (status == NEST_SOLVED && bp == 0) status = NEST_INFEASIBLE;
+    if (status != NEST_SOLVED) {
+        if (lane == 0) {
+            hdr->status = status;
+            hdr->n_stages = 0;
+            hdr->t_batch = -1;
+            hdr->bottleneck = -1;
+            a.costs_out[b] = -1;
+        }
+        return;
+    }
+    // lane 0 follows the argument fields (a chain of dependent reads); the stages'
+    // strategies are looked up afterwards by one lane each
+    const int L = ph->L;
+    int n = 0;
+    if (lane == 0) {
+        int i = 0, p = bp, c = 0, d = ph->Du;
+        while (i < L && p >= 1 && n < g.Pcap) {
+            const uint32_t arg = dpa[int64_t(p - 1) * pos_cells + int64_t(i) * row_cells + int64_t(c) * g.Dpad + d];
+            const int j = int((arg >> 8) & 0xFF), m = int((arg >> 4) & 0xF), c2 = int(arg & 0xF);
+            if (j <= i || j > L || m >= ph->K || (1 << m) > d || c2 >= ph->C) break;  // not for a solved cell
+            walk[2 * n] = i | j << 8 | m << 16 | c2 << 20;
+            walk[2 * n + 1] = p;
+            n++;
+            d -= 1 << m;
+            p -= 1;
+            c = c2;
+            i = j;
+        }
+    }
+    n = __shfl_sync(0xffffffffu, n, 0);
+    __syncwarp();
+    if (lane < n) {
+        const int w = walk[2 * lane], p = walk[2 * lane + 1];
+        const int i = w & 0xFF, j = (w >> 8) & 0xFF, m = (w >> 16) & 0xF, c2 = (w >> 20) & 0xF;
+        const uint64_t lw = loads[int64_t(p - 1) * g.NP * g.Kpad + (row_offset(i, L) + (j - i - 1)) * g.Kpad + m];
+        st[lane].i = int16_t(i);
+        st[lane].j = int16_t(j);
+        st[lane].s = int16_t(lw & 0xFFFF);
+        st[lane].c_next = int8_t(j < L ? c2 : -1);
+        st[lane].reserved = 0;
+        st[lane].k = ph->unit << m;
+    }
+    if (lane == 0) {
+        hdr->status = NEST_SOLVED;
+        hdr->n_stages = n;
+        hdr->t_batch = bt;
+        hdr->bottleneck = dpv[int64_t(bp - 1) * pos_cells + ph->Du];
+        a.costs_out[b] = bt;
+    }
+}
+
+
+}  // namespace nest
