@@ -319,3 +319,49 @@ def torus_instance(b: int, shape=(4, 4, 4)) -> Instance:
     x.tierG, x.tierBw, x.tierLat = G, bw, lat
     x.cand = np.arange(len(G), dtype=np.int32)
     return x
+
+
+# ----------------------------------------------------------------------------------
+# Layer DAGs (Nest §4 states Eq. 3 over downsets of the operator graph).  A graph is
+# given by successor masks: bit v of succ[l] is set for each edge l -> v, and the
+# layers are numbered topologically (v > l).
+# ----------------------------------------------------------------------------------
+
+def chain_succ(L: int) -> np.ndarray:
+    """The successor masks of the chain 0 -> 1 -> ... -> L-1."""
+    return np.asarray([(1 << (l + 1)) if l + 1 < L else 0 for l in range(L)], dtype=np.uint64)
+
+
+def random_dag(seed: int, L: int, density: float) -> np.ndarray:
+    """Each forward edge u -> v (u < v) present with probability `density`."""
+    rng = np.random.default_rng(2 * 10**6 + seed)
+    succ = np.zeros(L, dtype=np.uint64)
+    for u in range(L):
+        for v in range(u + 1, L):
+            if rng.random() < density:
+                succ[u] |= np.uint64(1 << v)
+    return succ
+
+
+def two_tower_succ(branch: int = 8, trunk: int = 16) -> np.ndarray:
+    """Two encoder branches of `branch` blocks each feeding a shared trunk of `trunk`
+    blocks: branch A is layers [0, branch), branch B [branch, 2 branch), the trunk
+    the rest; both branch ends feed the first trunk block."""
+    L = 2 * branch + trunk
+    succ = np.zeros(L, dtype=np.uint64)
+    for base in (0, branch):
+        for l in range(base, base + branch - 1):
+            succ[l] = np.uint64(1 << (l + 1))
+        succ[base + branch - 1] = np.uint64(1 << (2 * branch))
+    for l in range(2 * branch, L - 1):
+        succ[l] = np.uint64(1 << (l + 1))
+    return succ
+
+
+TWO_TOWER_NAME = "two-tower-32L-h4096-64dev"
+
+
+def two_tower_instance(b: int) -> Instance:
+    """Workload 2's blocks, tiers and budgets arranged as two 8-block encoder branches
+    feeding a 16-block trunk (97 up-sets)."""
+    return config_instance(2, b)

@@ -40,7 +40,12 @@
  *     so the time model, is the same as for 1F1B;
  *   - SYNCCOST is folded into each stage's amortised gradient sync term;
  *   - ties: smallest (v, j, m, c') per cell, smallest (tau, s) per strategy choice,
- *     smallest (t_batch, p) at the end.
+ *     smallest (t_batch, p) at the end;
+ *   - a layer DAG numbered topologically: D an up-set (closed under successors), the
+ *     cut D' an up-set strictly inside D; states ordered by size descending, then
+ *     by mask, so a chain gets the suffix indices; the bytes entering D are the
+ *     outputs of the layers outside D that feed it (for the whole graph, the
+ *     source layers' outputs) and are both the link volume and the stashed input.
  * Every function below is pinned by the CPU tests (closed forms, brute force,
  * textbook special cases and invariants).
  */
@@ -402,4 +407,270 @@ int or_solve(const or_instance *x, uint64_t *dp_out, int64_t *t_batch, int64_t *
     if (!dp_out) free(keys);
 #undef KEY
     return status;
+}
+
+/* ---------------------------------------------------------------------------------
+ * Non-chain layer graphs.  Nest §4 states Eq. 3 over downsets of the operator
+ * graph: the DP state is the set of layers not yet placed, a stage is the
+ * difference of two such sets.  Reading for a DAG whose layers are numbered
+ * topologically (every edge u -> v has u < v): the states are the up-sets (closed
+ * under successors), ordered by size descending and then by mask; a transition
+ * goes from D to any up-set D' strictly inside D and places the stage D \ D'.  For
+ * a chain the up-sets are the suffixes [i, L) with the same indices, so everything
+ * below reduces to the chain solver above.
+ * ------------------------------------------------------------------------------- */
+
+#define OR_MAX_STATES 256
+
+static int popc(uint64_t v) { return __builtin_popcountll(v); }
+
+/* Up-sets of the DAG given by succ[l] (bit v set for each edge l -> v, v > l):
+ * grown from the empty set by adding a layer whose successors are all present.
+ * Returns the count, or -1 when the graph is not topologically numbered, has more
+ * than 63 layers, or more than OR_MAX_STATES up-sets. */
+int or_lattice_states(const or_instance *x, const uint64_t *succ, uint64_t *states) {
+    const int L = x->L;
+    if (L < 1 || L > 63) return -1;
+    for (int l = 0; l < L; l++)
+        if (succ[l] & (((uint64_t)2 << l) - 1)) return -1;   /* edges go forward */
+    int n = 1;
+    states[0] = 0;
+    for (int q = 0; q < n; q++) {
+        const uint64_t D = states[q];
+        for (int l = 0; l < L; l++) {
+            const uint64_t bit = (uint64_t)1 << l;
+            if ((D & bit) || (succ[l] & ~D)) continue;
+            const uint64_t E = D | bit;
+            int seen = 0;
+            for (int r = 0; r < n && !seen; r++) seen = states[r] == E;
+            if (seen) continue;
+            if (n == OR_MAX_STATES) return -1;
+            states[n++] = E;
+        }
+    }
+    /* size descending, then mask ascending */
+    for (int a = 1; a < n; a++) {
+        const uint64_t v = states[a];
+        int b = a;
+        while (b > 0 && (popc(states[b - 1]) < popc(v) || (popc(states[b - 1]) == popc(v) && states[b - 1] > v))) {
+            states[b] = states[b - 1];
+            b--;
+        }
+        states[b] = v;
+    }
+    return n;
+}
+
+/* Bytes entering up-set D: the outputs of the layers outside D that feed it; for
+ * the whole graph, the outputs of its source layers. */
+static int64_t bytes_in(const or_instance *x, const uint64_t *succ, uint64_t D, uint64_t all) {
+    int64_t b = 0;
+    for (int l = 0; l < x->L; l++) {
+        const uint64_t bit = (uint64_t)1 << l;
+        if (D == all) {
+            int src = 1;
+            for (int u = 0; u < l; u++)
+                if (succ[u] & bit) src = 0;
+            if (src) b += x->ao[l];
+        } else if (!(D & bit) && (succ[l] & D)) {
+            b += x->ao[l];
+        }
+    }
+    return b;
+}
+
+static void mask_sums(const or_instance *x, uint64_t S, int64_t ain, or_sums *u) {
+    memset(u, 0, sizeof *u);
+    for (int l = 0; l < x->L; l++) {
+        if (!(S >> l & 1)) continue;
+        u->Fl += x->fl[l];
+        u->Pd += x->pd[l];
+        u->Pe += x->pe[l];
+        u->Ao += x->ao[l];
+        u->Aw += x->aw[l];
+        u->A2 += x->a2a[l];
+        u->nM += x->moe[l];
+        u->AwMax = imax(u->AwMax, x->aw[l]);
+        u->nL++;
+    }
+    u->ain = ain;
+}
+
+/* Link cost into each state over each candidate: out[state][c], zero for the whole
+ * graph and for the empty set. */
+static void lattice_links(const or_instance *x, const uint64_t *succ, const uint64_t *st, int ns, int64_t *X) {
+    const uint64_t all = st[0];
+    for (int q = 0; q < ns; q++)
+        for (int c = 0; c < x->C; c++) {
+            int64_t v = 0;
+            if (q > 0 && q < ns - 1) {
+                const int tr = x->cand[c];
+                v = x->lat[tr] + cdiv(bytes_in(x, succ, st[q], all) * 1000, x->bw[tr]);
+            }
+            X[q * x->C + c] = v;
+        }
+}
+
+static void lattice_stage_loads(const or_instance *x, const uint64_t *succ, uint64_t D, uint64_t Dp, uint64_t all,
+                                int K, uint64_t *out) {
+    or_sums u;
+    mask_sums(x, D & ~Dp, bytes_in(x, succ, D, all), &u);
+    for (int m = 0; m < K; m++) {
+        for (int p = 1; p <= x->Pmax; p++) out[m * x->Pmax + p - 1] = OR_INF;
+        for (int s = 0; s < x->S; s++) {
+            or_terms r;
+            stage_terms(x, &u, m, s, &r);
+            uint64_t w = word_of(&r);
+            if (w == OR_INF) continue;
+            uint64_t key = ((w >> 8) << 16) | (uint64_t)s;
+            int pm = (int)(w & 0xFF);
+            for (int p = 1; p <= pm; p++)
+                if (key < out[m * x->Pmax + p - 1]) out[m * x->Pmax + p - 1] = key;
+        }
+    }
+}
+
+/* Loads of every transition (i, j), i < j, states[j] strictly inside states[i],
+ * in that order: out[(t * K + m) * Pmax + p - 1].  Returns the transition count. */
+int64_t or_lattice_loads(const or_instance *x, const uint64_t *succ, const uint64_t *st, int ns, uint64_t *out) {
+    const int K = widths(x);
+    int64_t t = 0;
+    for (int i = 0; i < ns; i++)
+        for (int j = i + 1; j < ns; j++) {
+            if ((st[j] & ~st[i]) || st[j] == st[i]) continue;
+            if (out) lattice_stage_loads(x, succ, st[i], st[j], st[0], K, out + t * K * x->Pmax);
+            t++;
+        }
+    return t;
+}
+
+/* Eq. 3 over the up-sets of the DAG (the chain solver with j ranging over the
+ * states inside state i), the batch-time loop and the stage reconstruction; stage
+ * i and j fields are state indices.  dp_out (optional): [ns][Du+1][Pmax+1][C].
+ * Returns 0 solved, 1 infeasible, 2 invalid input (also a graph beyond the
+ * lattice limits). */
+int or_solve_lattice(const or_instance *x, const uint64_t *succ, uint64_t *dp_out, int64_t *t_batch,
+                     int64_t *bottleneck, int32_t *n_stages, or_stage *stages) {
+    *t_batch = -1;
+    *bottleneck = -1;
+    *n_stages = 0;
+    if (or_validate(x)) return 2;
+    uint64_t st[OR_MAX_STATES];
+    const int ns = or_lattice_states(x, succ, st);
+    if (ns < 2) return 2;
+    const int C = x->C, P = x->Pmax, K = widths(x);
+    const int64_t Du = x->D / x->unit;
+    const int64_t nd = Du + 1, np = P + 1;
+    const int E = ns - 1; /* the empty set */
+#define KEY(i, d, p, c) keys[(((int64_t)(i) * nd + (d)) * np + (p)) * C + (c)]
+    const int64_t words = (int64_t)ns * nd * np * C;
+    uint64_t *keys = dp_out ? dp_out : malloc(sizeof(uint64_t) * words);
+    int64_t *X = malloc(sizeof(int64_t) * ns * C);
+    uint64_t *ld = malloc(sizeof(uint64_t) * K * P);
+    for (int64_t w = 0; w < words; w++) keys[w] = OR_INF;
+    for (int64_t d = 0; d <= Du; d++)
+        for (int c = 0; c < C; c++) KEY(E, d, 0, c) = 0;
+    lattice_links(x, succ, st, ns, X);
+
+    for (int i = E - 1; i >= 0; i--) {
+        const int ncell = i == 0 ? 1 : C;
+        const int layers = popc(st[i]);
+        for (int j = i + 1; j <= E; j++) {
+            if ((st[j] & ~st[i]) || st[j] == st[i]) continue;
+            lattice_stage_loads(x, succ, st[i], st[j], st[0], K, ld);
+            for (int p = 1; p <= P && p <= layers; p++) {
+                if ((j == E) != (p == 1)) continue;
+                for (int64_t d = 1; d <= Du; d++)
+                    for (int m = 0; ((int64_t)1 << m) <= d; m++) {
+                        const int64_t k = (int64_t)x->unit << m;
+                        const uint64_t load = ld[m * P + p - 1];
+                        if (load == OR_INF) continue;
+                        const int64_t tstar = (int64_t)(load >> 16);
+                        for (int c = 0; c < ncell; c++) {
+                            if (i > 0 && 2 * k > x->G[x->cand[c]]) continue;
+                            const int64_t base = tstar + (i > 0 ? X[i * C + c] : 0);
+                            uint64_t best = KEY(i, d, p, c);
+                            if (j == E) {
+                                if (base < OR_CAP) {
+                                    const uint64_t cand_key = pack_key(base, j, m, 0);
+                                    if (cand_key < best) best = cand_key;
+                                }
+                            } else {
+                                for (int c2 = 0; c2 < C; c2++) {
+                                    if (2 * k > x->G[x->cand[c2]]) continue;
+                                    const uint64_t prev = KEY(j, d - ((int64_t)1 << m), p - 1, c2);
+                                    if (prev == OR_INF) continue;
+                                    const int64_t v = imax(base + X[j * C + c2], (int64_t)(prev >> 24));
+                                    if (v >= OR_CAP) continue;
+                                    const uint64_t cand_key = pack_key(v, j, m, c2);
+                                    if (cand_key < best) best = cand_key;
+                                }
+                            }
+                            KEY(i, d, p, c) = best;
+                        }
+                    }
+            }
+        }
+    }
+
+    int bp = -1;
+    int64_t bt = 0;
+    for (int p = 1; p <= P && p <= popc(st[0]); p++) {
+        const uint64_t key = KEY(0, Du, p, 0);
+        if (key == OR_INF) continue;
+        const int64_t t = (int64_t)(key >> 24) * (x->M + p - 1);
+        if (bp < 0 || t < bt) {
+            bt = t;
+            bp = p;
+        }
+    }
+    int status = 1;
+    if (bp > 0) {
+        status = 0;
+        *t_batch = bt;
+        *bottleneck = (int64_t)(KEY(0, Du, bp, 0) >> 24);
+        int i = 0, p = bp, c = 0, n = 0;
+        int64_t d = Du;
+        while (i < E) {
+            const uint64_t key = KEY(i, d, p, c);
+            const int j = (int)((key >> 8) & 0xFF), m = (int)((key >> 4) & 0xF), c2 = (int)(key & 0xF);
+            lattice_stage_loads(x, succ, st[i], st[j], st[0], K, ld);
+            stages[n].i = i;
+            stages[n].j = j;
+            stages[n].k = x->unit << m;
+            stages[n].s = (int32_t)(ld[m * P + p - 1] & 0xFFFF);
+            stages[n].c_next = j < E ? c2 : -1;
+            n++;
+            d -= (int64_t)1 << m;
+            p -= 1;
+            c = c2;
+            i = j;
+        }
+        *n_stages = n;
+    }
+    free(ld);
+    free(X);
+    if (!dp_out) free(keys);
+#undef KEY
+    return status;
+}
+
+/* The terms of the stage D \ D' of a layer DAG (exposed for the pins). */
+void or_lattice_terms(const or_instance *x, const uint64_t *succ, uint64_t D, uint64_t Dp, int m, int s,
+                      or_terms *r) {
+    uint64_t all = 0;
+    for (int l = 0; l < x->L; l++) all |= (uint64_t)1 << l;
+    or_sums u;
+    mask_sums(x, D & ~Dp, bytes_in(x, succ, D, all), &u);
+    stage_terms(x, &u, m, s, r);
+}
+
+/* Link cost into up-set D over candidate c (zero for the whole graph and the empty
+ * set), exposed for the pins. */
+int64_t or_lattice_link(const or_instance *x, const uint64_t *succ, uint64_t D, int c) {
+    uint64_t all = 0;
+    for (int l = 0; l < x->L; l++) all |= (uint64_t)1 << l;
+    if (D == all || D == 0) return 0;
+    const int tr = x->cand[c];
+    return x->lat[tr] + cdiv(bytes_in(x, succ, D, all) * 1000, x->bw[tr]);
 }

@@ -72,6 +72,15 @@ def lib():
             L.or_dp_table_words.restype = C.c_int64
             L.or_solve.argtypes = [P(_Inst), C.c_void_p, P(C.c_int64), P(C.c_int64),
                                    P(C.c_int32), P(_Stage)]
+            L.or_lattice_states.argtypes = [P(_Inst), C.c_void_p, C.c_void_p]
+            L.or_lattice_loads.argtypes = [P(_Inst), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p]
+            L.or_lattice_loads.restype = C.c_int64
+            L.or_lattice_terms.argtypes = [P(_Inst), C.c_void_p, C.c_uint64, C.c_uint64, C.c_int, C.c_int,
+                                           P(_Terms)]
+            L.or_lattice_link.argtypes = [P(_Inst), C.c_void_p, C.c_uint64, C.c_int]
+            L.or_lattice_link.restype = C.c_int64
+            L.or_solve_lattice.argtypes = [P(_Inst), C.c_void_p, C.c_void_p, P(C.c_int64), P(C.c_int64),
+                                           P(C.c_int32), P(_Stage)]
             _lib = L
     return _lib
 
@@ -175,3 +184,64 @@ def solve_joint(variants) -> dict:
         if r["status"] == 0 and (best < 0 or r["t_batch"] < res["t_batch"]):
             best, res = q, r
     return {"best": best, "t_batch": res["t_batch"] if res else -1, "results": results}
+
+
+# ---------------------------------------------------------------------------------
+# Layer DAGs: succ[l] is the bit mask of the successors of layer l (layers numbered
+# topologically); the states of Eq. 3 are the up-sets of the graph.
+
+
+def _succ(succ) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(succ, dtype=np.uint64))
+
+
+def lattice_states(inst, succ) -> np.ndarray | None:
+    """The up-sets as layer masks in DP order, or None beyond the lattice limits."""
+    m, sc = Marshalled(inst), _succ(succ)
+    out = np.zeros(256, dtype=np.uint64)
+    n = lib().or_lattice_states(C.byref(m.s), sc.ctypes.data, out.ctypes.data)
+    return None if n < 0 else out[:n].copy()
+
+
+def lattice_loads(inst, succ) -> tuple[list, np.ndarray]:
+    """Transitions [(i, j)] in the oracle's order and their loads [T, K, Pmax]."""
+    m, sc = Marshalled(inst), _succ(succ)
+    st = lattice_states(inst, succ)
+    n = lib().or_lattice_loads(C.byref(m.s), sc.ctypes.data, st.ctypes.data, len(st), None)
+    out = np.empty((n, m.K, inst.Pmax), dtype=np.uint64)
+    lib().or_lattice_loads(C.byref(m.s), sc.ctypes.data, st.ctypes.data, len(st), out.ctypes.data)
+    pairs = [(i, j) for i in range(len(st)) for j in range(i + 1, len(st))
+             if not (int(st[j]) & ~int(st[i])) and st[j] != st[i]]
+    return pairs, out
+
+
+def lattice_terms(inst, succ, D: int, Dp: int, m: int, s: int) -> dict:
+    mm, sc = Marshalled(inst), _succ(succ)
+    t = _Terms()
+    lib().or_lattice_terms(C.byref(mm.s), sc.ctypes.data, D, Dp, m, s, C.byref(t))
+    return {n: int(getattr(t, n)) for n in TERM_NAMES}
+
+
+def lattice_link(inst, succ, D: int, c: int) -> int:
+    mm, sc = Marshalled(inst), _succ(succ)
+    return int(lib().or_lattice_link(C.byref(mm.s), sc.ctypes.data, D, c))
+
+
+def solve_lattice(inst, succ, want_dp: bool = False) -> dict:
+    """Eq. 3 over the up-sets of a layer DAG; plan stage i/j are state indices into
+    `states`."""
+    m, sc = Marshalled(inst), _succ(succ)
+    st = lattice_states(inst, succ)
+    dp = None
+    dp_ptr = None
+    if want_dp and st is not None:
+        Du = inst.D // inst.unit
+        dp = np.empty((len(st), Du + 1, inst.Pmax + 1, m.s.C), dtype=np.uint64)
+        dp_ptr = dp.ctypes.data
+    t, v, n = C.c_int64(), C.c_int64(), C.c_int32()
+    stages = (_Stage * 64)()
+    rc = lib().or_solve_lattice(C.byref(m.s), sc.ctypes.data, dp_ptr, C.byref(t), C.byref(v), C.byref(n), stages)
+    plan = [(stages[q].i, stages[q].j, stages[q].k, stages[q].s, stages[q].c_next)
+            for q in range(n.value)]
+    return {"status": rc, "t_batch": t.value, "bottleneck": v.value, "plan": plan, "dp": dp,
+            "states": st}
