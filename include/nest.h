@@ -12,12 +12,25 @@
  *   Appendix K Algorithm 1      backward sweep, t_batch = t_stage (mbs + s - 1),
  *                               stage reconstruction.
  *
- * One problem ("instance") is a chain of L layers, a cluster of D devices grouped
- * in tiers, C candidate tiers for links between pipeline stages, S parallel
- * strategies (TP t, context-parallel cp, expert-parallel e, ZeRO stage z,
- * recompute r) and a per-device memory budget.  The solver returns, per instance,
- * the smallest iteration time and a plan of contiguous stages, each with a device
- * count unit * 2^m, a strategy and the candidate tier of its outgoing link.
+ * One problem ("instance") is a chain of L layers, or a DAG of L layers (graph
+ * instances, below), a cluster of D devices grouped in tiers, C candidate tiers for
+ * links between pipeline stages, S parallel strategies (TP t, context-parallel cp,
+ * expert-parallel e, ZeRO stage z, recompute r) and a per-device memory budget.
+ * The solver returns, per instance, the smallest iteration time and a plan of
+ * stages, each with a device count unit * 2^m, a strategy and the candidate tier
+ * of its outgoing link.
+ *
+ * Graph instances (Nest §4 states Eq. 3 over downsets of the operator graph): the
+ * layers are numbered topologically and succ[l] has bit v set for each edge
+ * l -> v.  The DP states are the up-sets of the graph (sets closed under
+ * successors: the layers not yet placed), ordered by size descending and then by
+ * mask ascending - state 0 is the whole graph, the last state the empty set; a
+ * chain gets its suffixes [i, L) as states i.  A stage goes from state i to a
+ * state j strictly inside it and holds the layers states[i] \ states[j].  The
+ * bytes entering a state (outputs of the layers outside it that feed it; for the
+ * whole graph, the source layers' outputs) are its link volume and the stashed
+ * input of the stage that starts there; for a chain that is ao[i - 1] (ao[0] at
+ * i = 0), as in the chain model.
  * All times are int64 nanoseconds and every result is exact: the CUDA path and
  * the plain CPU definition agree bit for bit.
  *
@@ -55,7 +68,8 @@ extern "C" {
  * on the host before any launch, NEST_E_LIMITS otherwise):
  *   1 <= Lmax <= 255 layers, 1 <= Tmax <= 8 tiers, 1 <= Cmax <= 15 candidates,
  *   1 <= Smax <= 4095 strategies, 1 <= Pcap <= 31 stages,
- *   1 <= Dumax <= 512 device units.                                          */
+ *   1 <= Dumax <= 512 device units, 0 <= Vmax <= 255.
+ * The DP runs over states 0 .. N per instance, N = max(Lmax, Vmax).          */
 typedef struct {
     int32_t B;      /* instances in the batch (0 is a no-op) */
     int32_t Lmax;
@@ -64,7 +78,9 @@ typedef struct {
     int32_t Smax;
     int32_t Pcap;
     int32_t Dumax;  /* largest D / unit of any instance */
-    int32_t reserved;
+    int32_t Vmax;   /* at least the number of non-empty up-sets of every graph instance's
+                       layer graph (its DP states less the empty set); 0 when every
+                       instance is a chain */
 } nest_dims;
 
 /* ---- instance record ---------------------------------------------------------
@@ -78,7 +94,9 @@ typedef struct {
  *   two with G[T-1] >= D; 1000 <= bw <= 2^40; 0 <= lat <= 2^24; 1 <= C <= Cmax;
  *   candidate tiers strictly increasing in [0, T); 1 <= S <= Smax; t, cp, e powers
  *   of two <= 8192; z in 0..3; r in 0..1; 1 <= Pmax <= Pcap; Pmax <= M <= 2^20;
- *   schedule in {0, 1};
+ *   schedule in {0, 1}; graph in {0, 1};
+ *   graph instances: L <= 63, every succ[l] has bits only in (l, L), and the graph
+ *   has at most Vmax non-empty up-sets;
  *   1 <= R <= 2^40; 0 <= budget <= 2^62; 0 <= opt_factor <= 16; per layer
  *   0 <= fl <= 2^48, 0 <= pd, pe, ao, aw, a2a <= 2^38, moe in {0, 1}.       */
 typedef struct {
@@ -96,6 +114,8 @@ typedef struct {
     int64_t M;          /* microbatches per iteration */
     int64_t budget;     /* bytes per device */
     int64_t opt_factor; /* optimizer-state bytes per bf16 weight byte */
+    int32_t graph;      /* 0 = chain 0 -> 1 -> ... -> L-1 (succ ignored), 1 = the DAG in succ */
+    int32_t reserved;
 } nest_record_header;
 
 /* Byte offsets inside one record (from its start). */
@@ -106,17 +126,22 @@ typedef struct {
     int64_t G, bw, lat;              /* int64 [Tmax] each */
     int64_t cand;                    /* int32 [Cmax] */
     int64_t strat;                   /* int16 [Smax][8]: t, cp, e, z, r, 0, 0, 0 */
+    int64_t succ;                    /* uint64 [Lmax]: successor masks (graph instances) */
 } nest_layout;
 
 /* ---- output plan --------------------------------------------------------------
  * B plan records back to back, each nest_plan_bytes() long: a nest_plan_header
  * followed by Pcap nest_stage entries (n_stages of them used).               */
 typedef struct {
-    int16_t i, j;    /* the stage holds layers [i, j) */
+    int16_t i, j;    /* the stage goes from DP state i to state j: layers [i, j) of a chain,
+                        states[i] \ states[j] of a graph (state order above) */
     int16_t s;       /* strategy index into the instance's strategy table */
     int8_t c_next;   /* candidate of the link to the next stage, -1 for the last stage */
     int8_t reserved;
     int32_t k;       /* devices of the stage */
+    int32_t reserved2;
+    uint64_t layers; /* bit l set for each layer of the stage (0 for chains of more than
+                        64 layers) */
 } nest_stage;
 
 typedef struct {
@@ -204,17 +229,19 @@ int nest_solve_host(const nest_dims *dims, const void *records_host, int64_t *co
 /* Offsets (bytes from the workspace start) of the intermediate tables of the
  * LAST chunk a nest_solve call processed, for inspection after the stream syncs:
  *   loads uint64 [chunk][Pcap][NP][Kpad]  (tau* << 16) | s* per position p (index p-1)
- *   dpv   int64  [chunk][Pcap][Lmax][Cmax][Dpad]  DP value per (p, i, c, d), 2^40-1 = none
- *   dpa   uint32 [chunk][Pcap][Lmax][Cmax][Dpad]  (j << 8) | (m << 4) | c'
+ *   dpv   int64  [chunk][Pcap][N][Cmax][Dpad]  DP value per (p, i, c, d), 2^40-1 = none
+ *   dpa   uint32 [chunk][Pcap][N][Cmax][Dpad]  (j << 8) | (m << 4) | c'
  *   cost  uint64 [chunk][NP][Kmax][Spad]  (tau << 8) | pmax, all ones = not applicable;
  *         written only with NEST_KEEP_COSTS, after the end of the plain workspace
- * where NP = Lmax (Lmax + 1) / 2 pairs (i, j) ordered by i then j, Kmax =
+ * where NP = N (N + 1) / 2 pairs of states (i, j) ordered by i then j (for a graph
+ * instance the pairs whose state j is not inside state i hold all
+ * ones), Kmax =
  * floor(log2 Dumax) + 1, Kpad = Kmax rounded up to even, Spad = Smax rounded up
  * to even, Dpad = Dumax + 1 rounded up to a multiple of 4.  total and total_costs
  * are nest_workspace_size and nest_workspace_size_costs. */
 typedef struct {
     int64_t loads, dpv, dpa, cost, total, total_costs;
-    int32_t NP, Kmax, Kpad, Spad, Dpad, chunk;
+    int32_t NP, Kmax, Kpad, Spad, Dpad, chunk, N, reserved;
 } nest_ws_layout;
 int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out);
 

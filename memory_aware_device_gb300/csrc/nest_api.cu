@@ -84,6 +84,8 @@ int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *
     out->Spad = g.Spad;
     out->Dpad = g.Dpad;
     out->chunk = ch;
+    out->N = g.Nmax;
+    out->reserved = 0;
     return NEST_OK;
 }
 

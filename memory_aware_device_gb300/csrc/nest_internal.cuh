@@ -16,13 +16,15 @@ constexpr int64_t kCap = (int64_t(1) << 40) - 1;   // stage times >= kCap are in
 constexpr uint64_t kInf = ~uint64_t(0);             // "no value" word / key
 constexpr uint32_t kNoArg = 0xFFFFFFu;              // argument field of an empty DP cell
 constexpr int kLogL = 8;                            // sparse-table levels: 2^8 > 255 layers
+constexpr int kMaxStates = 256;                     // DP states per instance (8-bit state index)
 
 __host__ __device__ inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 // Batch geometry derived from nest_dims.
 struct Geo {
-    int32_t B, Lmax, Tmax, Cmax, Smax, Pcap, Dumax;
-    int32_t NP;    // pairs (i, j), 0 <= i < j <= Lmax
+    int32_t B, Lmax, Tmax, Cmax, Smax, Pcap, Dumax, Vmax;
+    int32_t Nmax;  // last DP state index of any instance: max(Lmax, Vmax)
+    int32_t NP;    // pairs of states (i, j), 0 <= i < j <= Nmax
     int32_t Kmax;  // widths unit * 2^m, m < Kmax
     int32_t Kpad;  // Kmax rounded up to even (16-byte rows)
     int32_t Spad;  // Smax rounded up to even
@@ -32,7 +34,7 @@ struct Geo {
 inline bool make_geo(const nest_dims &d, Geo &g) {
     if (d.B < 0 || d.Lmax < 1 || d.Lmax > 255 || d.Tmax < 1 || d.Tmax > 8 || d.Cmax < 1 ||
         d.Cmax > 15 || d.Smax < 1 || d.Smax > 4095 || d.Pcap < 1 || d.Pcap > 31 || d.Dumax < 1 ||
-        d.Dumax > 512)
+        d.Dumax > 512 || d.Vmax < 0 || d.Vmax >= kMaxStates)
         return false;
     g.B = d.B;
     g.Lmax = d.Lmax;
@@ -41,7 +43,9 @@ inline bool make_geo(const nest_dims &d, Geo &g) {
     g.Smax = d.Smax;
     g.Pcap = d.Pcap;
     g.Dumax = d.Dumax;
-    g.NP = d.Lmax * (d.Lmax + 1) / 2;
+    g.Vmax = d.Vmax;
+    g.Nmax = d.Lmax > d.Vmax ? d.Lmax : d.Vmax;
+    g.NP = g.Nmax * (g.Nmax + 1) / 2;
     int K = 0;
     while ((1 << K) <= d.Dumax) K++;
     g.Kmax = K;
@@ -53,7 +57,7 @@ inline bool make_geo(const nest_dims &d, Geo &g) {
 
 // Offsets inside one instance record (public layout, see nest.h).
 inline void record_layout(const Geo &g, nest_layout &o) {
-    int64_t off = sizeof(nest_record_header);
+    int64_t off = align_up(sizeof(nest_record_header), 16);
     auto take = [&](int64_t bytes) {
         int64_t at = off;
         off = align_up(off + bytes, 16);
@@ -71,6 +75,7 @@ inline void record_layout(const Geo &g, nest_layout &o) {
     o.lat = take(8 * g.Tmax);
     o.cand = take(4 * g.Cmax);
     o.strat = take(16 * g.Smax);
+    o.succ = take(8 * g.Lmax);
     o.record_bytes = align_up(off, 256);
 }
 
@@ -78,11 +83,13 @@ inline void record_layout(const Geo &g, nest_layout &o) {
 struct PrepHdr {
     int32_t status;  // NEST_SOLVED (0) when the instance is valid, NEST_BAD_INPUT otherwise;
                      // the sweep raises it to NEST_TIMED_OUT when a wait gives up
-    int32_t L, D, unit, lu, Du, K, T, C, S, P;
+    int32_t L;       // last DP state: the empty set (layers of a chain, up-sets - 1 of a graph)
+    int32_t D, unit, lu, Du, K, T, C, S, P;
     uint32_t maxX32;     // largest link cost X, saturated at 2^31 - 1 (prep)
     uint32_t maxload32;  // largest finite per-position load tau*, saturated (reduction)
     int32_t schedule;    // 0 = 1F1B, 1 = GPipe
-    int32_t pad1, pad2;
+    int32_t graph;       // 0 = chain, 1 = states are the up-sets of a layer DAG
+    int32_t layers;      // layers of the instance
     int64_t R, M, budget, opt;
     int64_t G[8], bw[8], lat[8];
     int32_t cand[16];
@@ -96,10 +103,11 @@ static_assert(sizeof(PrepHdr) % 16 == 0, "PrepHdr alignment");
 enum { kFl = 0, kPd, kPe, kAo, kAw, kA2, kNm, kNumPfx };
 
 struct PrepLayout {
-    int64_t pfx;    // int64 [kNumPfx][Lmax + 1] prefix sums
-    int64_t ao;     // int64 [Lmax] raw output activation bytes
+    int64_t pfx;    // int64 [kNumPfx][Lmax + 1] prefix sums over layers
+    int64_t ain;    // int64 [Nmax + 1] bytes entering each state (link volume, stashed input)
+    int64_t umask;  // uint64 [Nmax + 1] layers of each state (chains of <= 64 layers, graphs)
     int64_t awst;   // int64 [kLogL][Lmax] sparse table of max(aw)
-    int64_t X;      // int64 [Lmax + 1][Cmax] link cost per boundary and candidate
+    int64_t X;      // int64 [Nmax + 1][Cmax] link cost into each state per candidate
     int64_t strat;  // uint32 [Smax] packed log2 t | log2 cp << 4 | log2 e << 8 | z << 12 | r << 14
     int64_t bytes;
 };
@@ -109,12 +117,14 @@ __host__ __device__ inline PrepLayout prep_layout(const Geo &g) {
     int64_t off = sizeof(PrepHdr);
     p.pfx = off;
     off += 8 * int64_t(kNumPfx) * (g.Lmax + 1);
-    p.ao = off;
-    off += 8 * int64_t(g.Lmax);
+    p.ain = off;
+    off += 8 * int64_t(g.Nmax + 1);
+    p.umask = off;
+    off += 8 * int64_t(g.Nmax + 1);
     p.awst = off;
     off += 8 * int64_t(kLogL) * g.Lmax;
     p.X = off;
-    off += 8 * int64_t(g.Lmax + 1) * g.Cmax;
+    off += 8 * int64_t(g.Nmax + 1) * g.Cmax;
     p.strat = off;
     off += 4 * int64_t(g.Smax);
     p.bytes = align_up(off, 256);
@@ -133,7 +143,7 @@ __host__ __device__ inline WsLayout ws_layout(const Geo &g, int64_t ch) {
     w.prep_stride = p.bytes;
     w.cost_stride = int64_t(g.NP) * g.Kmax * g.Spad;            // uint64 words
     w.loads_stride = int64_t(g.Pcap) * g.NP * g.Kpad;           // uint64 words
-    w.dp_stride = int64_t(g.Pcap) * g.Lmax * g.Cmax * g.Dpad;   // cells
+    w.dp_stride = int64_t(g.Pcap) * g.Nmax * g.Cmax * g.Dpad;   // cells
     int64_t off = 0;
     w.prep = off;
     off = align_up(off + ch * w.prep_stride, 256);
@@ -154,7 +164,7 @@ __host__ __device__ inline int64_t plan_bytes(const Geo &g) {
     return align_up(int64_t(sizeof(nest_plan_header)) + int64_t(sizeof(nest_stage)) * g.Pcap, 8);
 }
 
-// Row offset of pair (i, i+1) among the pairs of an L-layer chain.
+// Row offset of pair (i, i+1) among the pairs of states 0 .. L.
 __host__ __device__ inline int64_t row_offset(int i, int L) {
     return int64_t(i) * L - int64_t(i) * (i - 1) / 2;
 }

@@ -15,10 +15,10 @@
 
 namespace nest {
 
-// Shared scratch of prep_instance: two flags, the record, the layer values and the
-// sparse table (byte offsets).
+// Shared scratch of prep_instance: flags and counters, the record, the layer values,
+// the sparse table and the up-set lists of a graph instance (byte offsets).
 struct PrepScratch {
-    int64_t flags, rec, sv, sst, bytes;
+    int64_t flags, rec, sv, sst, gen, lev, bytes;
 };
 
 __host__ __device__ inline PrepScratch prep_scratch(const Geo &g, const nest_layout &rl) {
@@ -27,12 +27,15 @@ __host__ __device__ inline PrepScratch prep_scratch(const Geo &g, const nest_lay
     s.rec = 128;
     s.sv = s.rec + align_up(rl.record_bytes, 128);
     s.sst = s.sv + align_up(8 * int64_t(kNumPfx) * g.Lmax, 128);
-    s.bytes = s.sst + align_up(8 * int64_t(kLogL) * g.Lmax, 128);
+    s.gen = s.sst + align_up(8 * int64_t(kLogL) * g.Lmax, 128);
+    s.lev = s.gen + 8 * kMaxStates;
+    s.bytes = s.lev + 4 * 72;
     return s;
 }
 
 __device__ __forceinline__ bool pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
 __device__ __forceinline__ int ilog2(int64_t v) { return 63 - __clzll(v); }
+__device__ __forceinline__ uint64_t low_bits(int n) { return n >= 64 ? ~uint64_t(0) : (uint64_t(1) << n) - 1; }
 
 // The prep of instance b (validation, prefix sums, sparse table, link table,
 // strategy codes, invariant divisors) into its prep block in the workspace, using
@@ -70,6 +73,8 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
         bd |= h.budget < 0 || h.budget > (int64_t(1) << 62);
         bd |= h.opt_factor < 0 || h.opt_factor > 16;
         bd |= h.schedule < 0 || h.schedule > 1;
+        bd |= h.graph < 0 || h.graph > 1;
+        bd |= h.graph == 1 && (h.L > 63 || g.Vmax < 1);
         bad = bd;
     }
     __syncthreads();
@@ -89,6 +94,8 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
             bd |= f < 0 || f > (int64_t(1) << 48);
             for (int q = 0; q < 5; q++) bd |= arr[q][l] < 0 || arr[q][l] > (int64_t(1) << 38);
             bd |= rec[a.rl.moe + l] > 1;
+            if (h.graph)   // edges go forward, to layers of the instance
+                bd |= (reinterpret_cast<const uint64_t *>(rec + a.rl.succ)[l] & ~(low_bits(h.L) & ~low_bits(l + 1))) != 0;
         }
         for (int t = threadIdx.x; t < h.T; t += blockDim.x) {
             bd |= !pow2(G[t]) || (t > 0 && G[t] <= G[t - 1]);
@@ -116,7 +123,8 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
     const int L = h.L;
     const int64_t Du = h.D / h.unit;
     if (threadIdx.x == 0) {
-        ph->L = L;
+        ph->layers = L;
+        ph->graph = h.graph;
         ph->D = h.D;
         ph->unit = h.unit;
         ph->lu = ilog2(h.unit);
@@ -164,7 +172,6 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
     // read once with coalesced loads, each array is scanned by one warp, and the
     // results are written back with coalesced stores
     int64_t *pfx = reinterpret_cast<int64_t *>(pb + a.pl.pfx);
-    int64_t *ao = reinterpret_cast<int64_t *>(pb + a.pl.ao);
     int64_t *awst = reinterpret_cast<int64_t *>(pb + a.pl.awst);
     {
         const int64_t off[6] = {a.rl.fl, a.rl.pd, a.rl.pe, a.rl.ao, a.rl.aw, a.rl.a2a};
@@ -173,7 +180,6 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
             const int64_t v = q == kNm ? int64_t(rec[a.rl.moe + l]) : reinterpret_cast<const int64_t *>(rec + off[q])[l];
             sv[q * LM + l] = v;
             if (q == kAw) sst[l] = v;
-            if (q == kAo) ao[l] = v;
         }
     }
     __syncthreads();
@@ -209,18 +215,90 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
         const int lv = e / L, l = e % L;
         awst[int64_t(lv) * g.Lmax + l] = sst[lv * LM + l];
     }
+    // the DP states: suffixes [b, L) of a chain, the up-sets of a graph; per state its
+    // layer mask, the bytes entering it and the link cost into it per candidate
     const int64_t *ao_in = reinterpret_cast<const int64_t *>(rec + a.rl.ao);
+    int64_t *ain = reinterpret_cast<int64_t *>(pb + a.pl.ain);
+    uint64_t *um = reinterpret_cast<uint64_t *>(pb + a.pl.umask);
+    int E = L;   // the last state, the empty set
+    if (!h.graph) {
+        for (int q = threadIdx.x; q <= L; q += blockDim.x) {
+            ain[q] = q > 0 ? ao_in[q - 1] : ao_in[0];
+            um[q] = L <= 64 ? low_bits(L) & ~low_bits(q) : 0;
+        }
+    } else {
+        // Up-sets grown by size: the children of D are D + {l} for each layer l below
+        // the lowest layer of D whose successors all lie in D.  The lowest layer of an
+        // up-set has no predecessor inside it (the numbering is topological), so
+        // every up-set has exactly one parent and each is generated once.
+        const uint64_t *succ = reinterpret_cast<const uint64_t *>(rec + a.rl.succ);
+        uint64_t *gen = reinterpret_cast<uint64_t *>(scr + ps.gen);
+        int *lev = reinterpret_cast<int *>(scr + ps.lev);   // level k is gen[lev[k] .. lev[k + 1])
+        int &ngen = *reinterpret_cast<int *>(scr + ps.flags + 8);
+        const int cap = g.Vmax + 1;   // <= kMaxStates
+        if (threadIdx.x == 0) {
+            gen[0] = 0;
+            lev[0] = 0;
+            lev[1] = 1;
+            ngen = 1;
+        }
+        __syncthreads();
+        for (int k = 0; k <= L; k++) {
+            const int lo = lev[k], hi = lev[k + 1];
+            if (lo == hi) break;   // uniform: shared values after a barrier
+            for (int q = lo + int(threadIdx.x); q < hi; q += blockDim.x) {
+                const uint64_t D = gen[q];
+                const int top = D ? __ffsll((long long)D) - 1 : L;
+                for (int l = 0; l < top; l++)
+                    if ((succ[l] & ~D) == 0) {
+                        const int at = atomicAdd(&ngen, 1);
+                        if (at < cap) gen[at] = D | (uint64_t(1) << l);
+                    }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) lev[k + 2] = ngen < cap ? ngen : cap;
+            __syncthreads();
+        }
+        const int n = ngen;
+        if (n > cap) {   // more up-sets than the batch was sized for
+            if (threadIdx.x == 0) ph->status = NEST_BAD_INPUT;
+            return;
+        }
+        // state order: size descending, then mask ascending
+        for (int e = threadIdx.x; e < n; e += blockDim.x) {
+            int k = 0;
+            while (lev[k + 1] <= e) k++;
+            const uint64_t D = gen[e];
+            int r = 0;
+            for (int q = lev[k]; q < lev[k + 1]; q++) r += gen[q] < D;
+            um[n - lev[k + 1] + r] = D;
+        }
+        __syncthreads();
+        uint64_t fed = 0;   // layers with a predecessor
+        for (int l = 0; l < L; l++) fed |= succ[l];
+        const uint64_t full = low_bits(L);
+        for (int q = threadIdx.x; q < n; q += blockDim.x) {
+            const uint64_t D = um[q];
+            int64_t v = 0;
+            for (int l = 0; l < L; l++) {
+                const uint64_t bit = uint64_t(1) << l;
+                if (D == full ? !(fed & bit) : (!(D & bit) && (succ[l] & D))) v += ao_in[l];
+            }
+            ain[q] = v;
+        }
+        E = n - 1;
+    }
     int64_t *X = reinterpret_cast<int64_t *>(pb + a.pl.X);
     if (threadIdx.x == 0) xmax = 0;
     __syncthreads();
-    for (int e = threadIdx.x; e < (L + 1) * h.C; e += blockDim.x) {
-        const int bnd = e / h.C, c = e % h.C;
+    for (int e = threadIdx.x; e < (E + 1) * h.C; e += blockDim.x) {
+        const int q = e / h.C, c = e % h.C;
         int64_t v = 0;
-        if (bnd > 0 && bnd < L) {
+        if (q > 0 && q < E) {
             const int tr = cand[c];
-            v = lat[tr] + cdiv(ao_in[bnd - 1] * 1000, bw[tr]);
+            v = lat[tr] + cdiv(ain[q] * 1000, bw[tr]);
         }
-        X[int64_t(bnd) * g.Cmax + c] = v;
+        X[int64_t(q) * g.Cmax + c] = v;
         atomicMax(&xmax, v < 0x7FFFFFFF ? uint32_t(v) : 0x7FFFFFFFu);
     }
     uint32_t *sp = reinterpret_cast<uint32_t *>(pb + a.pl.strat);
@@ -232,6 +310,7 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        ph->L = E;
         ph->maxX32 = xmax;
         ph->maxload32 = 0;   // raised by the strategy reduction
         ph->status = NEST_SOLVED;
@@ -254,8 +333,41 @@ struct Net {
     }
 };
 
-// The K width words (tau << 8) | pmax of stage [i, j) under strategy s, handed to
-// emit(m, word); all ones where the strategy does not apply at that width.
+// Largest aw over layers [x, y), x < y, from the sparse table.
+__device__ __forceinline__ int64_t aw_max(const int64_t *awst, const Geo &g, int x, int y) {
+    const int lv = 31 - __clz(y - x);
+    const int64_t m1 = awst[int64_t(lv) * g.Lmax + x], m2 = awst[int64_t(lv) * g.Lmax + y - (1 << lv)];
+    return m1 > m2 ? m1 : m2;
+}
+
+// Per-layer metadata summed over a stage (§3.2), with its largest working activation.
+struct StageSums {
+    int64_t v[kNumPfx];   // kFl .. kNm
+    int64_t nL, awmax;
+};
+
+// The sums of the layers in `S`: one prefix-sum difference and one sparse-table
+// query per run of consecutive layers.  S < 2^63.
+__device__ __forceinline__ void mask_sums(const int64_t *pfx, const int64_t *awst, const Geo &g, uint64_t S,
+                                          StageSums &u) {
+    const int64_t ld = g.Lmax + 1;
+    for (int q = 0; q < kNumPfx; q++) u.v[q] = 0;
+    u.nL = __popcll(S);
+    u.awmax = 0;
+    while (S) {
+        const int x = __ffsll((long long)S) - 1;
+        const int run = __ffsll((long long)~(S >> x)) - 1;   // bit 63 of S is clear, so run <= 63
+        const int y = x + run;
+        for (int q = 0; q < kNumPfx; q++) u.v[q] += pfx[q * ld + y] - pfx[q * ld + x];
+        const int64_t mx = aw_max(awst, g, x, y);
+        u.awmax = mx > u.awmax ? mx : u.awmax;
+        S &= ~(low_bits(run) << x);
+    }
+}
+
+// The K width words (tau << 8) | pmax of the stage from state i to state j under
+// strategy s, handed to emit(m, word); all ones where the strategy does not apply at
+// that width, and for a graph instance when state j is not inside state i.
 template <typename Emit>
 __device__ __forceinline__ void stage_words(const PrepHdr *ph, const unsigned char *pb, const PrepLayout &pl,
                                             const Geo &g, int i, int j, int s, Emit emit) {
@@ -264,17 +376,35 @@ __device__ __forceinline__ void stage_words(const PrepHdr *ph, const unsigned ch
     const int lt = code & 15, lcp = (code >> 4) & 15, le = (code >> 8) & 15;
     const int z = (code >> 12) & 3, r = (code >> 14) & 1;
     const int64_t *pfx = reinterpret_cast<const int64_t *>(pb + pl.pfx);
+    const int64_t *awst = reinterpret_cast<const int64_t *>(pb + pl.awst);
     const int64_t ld = g.Lmax + 1;
-    const int64_t nM = pfx[kNm * ld + j] - pfx[kNm * ld + i];
     // valid for some width iff t cp e <= the widest stage, and e > 1 only over MoE layers
     const int lmin = lt + lcp + le - lu;  // smallest m that admits the strategy
-    if (lmin > K - 1 || (le > 0 && nM == 0)) {
-        for (int m = 0; m < K; m++) emit(m, kInf);
-        return;
+    StageSums u;
+    if (ph->graph) {
+        const uint64_t *um = reinterpret_cast<const uint64_t *>(pb + pl.umask);
+        const uint64_t Di = um[i], Dj = um[j];
+        if ((Dj & ~Di) || lmin > K - 1) {
+            for (int m = 0; m < K; m++) emit(m, kInf);
+            return;
+        }
+        mask_sums(pfx, awst, g, Di & ~Dj, u);
+        if (le > 0 && u.v[kNm] == 0) {
+            for (int m = 0; m < K; m++) emit(m, kInf);
+            return;
+        }
+    } else {
+        u.v[kNm] = pfx[kNm * ld + j] - pfx[kNm * ld + i];
+        if (lmin > K - 1 || (le > 0 && u.v[kNm] == 0)) {
+            for (int m = 0; m < K; m++) emit(m, kInf);
+            return;
+        }
+        for (int q = 0; q < kNm; q++) u.v[q] = pfx[q * ld + j] - pfx[q * ld + i];
+        u.nL = j - i;
+        u.awmax = r ? aw_max(awst, g, i, j) : 0;
     }
-    auto sum = [&](int q) { return pfx[q * ld + j] - pfx[q * ld + i]; };
-    const int64_t Fl = sum(kFl), Pd = sum(kPd), Pe = sum(kPe), Ao = sum(kAo), Aw = sum(kAw), A2 = sum(kA2);
-    const int64_t nL = j - i;
+    const int64_t Fl = u.v[kFl], Pd = u.v[kPd], Pe = u.v[kPe], Ao = u.v[kAo], Aw = u.v[kAw], A2 = u.v[kA2];
+    const int64_t nM = u.v[kNm], nL = u.nL;
     const Net net{ph};
 
     // width-independent terms: groups inside one replica
@@ -285,12 +415,8 @@ __device__ __forceinline__ void stage_words(const PrepHdr *ph, const unsigned ch
     const int64_t Wd = up_shift(Pd, lt), We = up_shift(Pe, lt + le);
     int64_t act, stash;
     if (r) {
-        const int64_t *ao = reinterpret_cast<const int64_t *>(pb + pl.ao);
-        const int64_t *awst = reinterpret_cast<const int64_t *>(pb + pl.awst);
-        const int lv = 31 - __clz(j - i);
-        const int64_t m1 = awst[int64_t(lv) * g.Lmax + i], m2 = awst[int64_t(lv) * g.Lmax + j - (1 << lv)];
-        act = up_shift(m1 > m2 ? m1 : m2, lt + lcp);
-        stash = up_shift(i > 0 ? ao[i - 1] : ao[0], lt + lcp);
+        act = up_shift(u.awmax, lt + lcp);
+        stash = up_shift(reinterpret_cast<const int64_t *>(pb + pl.ain)[i], lt + lcp);
     } else {
         act = up_shift(Aw, lt + lcp);
         stash = act;
@@ -426,7 +552,7 @@ static __device__ __noinline__ void backtrack_warp(const PassArgs &a, int b, int
     int status = ph->status;
     const Geo &g = a.g;
     const int64_t row_cells = int64_t(g.Cmax) * g.Dpad;
-    const int64_t pos_cells = int64_t(g.Lmax) * row_cells;
+    const int64_t pos_cells = int64_t(g.Nmax) * row_cells;
     const int64_t *dpv = reinterpret_cast<const int64_t *>(a.ws + a.w.dpv) + int64_t(b) * a.w.dp_stride;
     const uint32_t *dpa = reinterpret_cast<const uint32_t *>(a.ws + a.w.dpa) + int64_t(b) * a.w.dp_stride;
     const uint64_t *loads = reinterpret_cast<const uint64_t *>(a.ws + a.w.loads) + int64_t(b) * a.w.loads_stride;
@@ -497,6 +623,9 @@ static __device__ __noinline__ void backtrack_warp(const PassArgs &a, int b, int
         st[lane].c_next = int8_t(j < L ? c2 : -1);
         st[lane].reserved = 0;
         st[lane].k = ph->unit << m;
+        st[lane].reserved2 = 0;
+        const uint64_t *um = reinterpret_cast<const uint64_t *>(reinterpret_cast<const unsigned char *>(ph) + a.pl.umask);
+        st[lane].layers = um[i] & ~um[j];
     }
     if (lane == 0) {
         hdr->status = NEST_SOLVED;

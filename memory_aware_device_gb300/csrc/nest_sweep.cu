@@ -221,7 +221,7 @@ __device__ __forceinline__ Inst load_inst(const PassArgs &a, const PrepHdr *ph, 
     s.C = ph->C;
     s.P = ph->P;
     s.row_cells = int64_t(a.g.Cmax) * a.g.Dpad;
-    s.pos_cells = int64_t(a.g.Lmax) * s.row_cells;
+    s.pos_cells = int64_t(a.g.Nmax) * s.row_cells;
     s.pos_loads = int64_t(a.g.NP) * a.g.Kpad;
     s.dpv = reinterpret_cast<int64_t *>(a.ws + a.w.dpv) + int64_t(b) * a.w.dp_stride;
     s.dpa = reinterpret_cast<uint32_t *>(a.ws + a.w.dpa) + int64_t(b) * a.w.dp_stride;
@@ -344,18 +344,18 @@ __host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, 
     auto up = [](int w) { return (w + 15) / 16 * 16; };   // 128-byte alignment
     int off = 0;
     s.rowbar = off;                                       // one mbarrier per (owned slot, row j)
-    off = up(off + nown * g.Lmax);
+    off = up(off + nown * g.Nmax);
     s.X = off;
-    off = up(off + (g.Lmax + 1) * g.Cmax);
+    off = up(off + (g.Nmax + 1) * g.Cmax);
     s.Hpad = res_hpad(g, vbytes);
     s.Hcol = s.Hpad + g.Dpad;
     s.Hrow = res_hrow(g, jsplit, vbytes);
-    s.Hslot = g.Lmax * s.Hrow;
-    const int h4 = (nown * g.Lmax * res_hrow(g, jsplit, 4) + 1) / 2, h8 = nown * g.Lmax * res_hrow(g, jsplit, 8);
+    s.Hslot = g.Nmax * s.Hrow;
+    const int h4 = (nown * g.Nmax * res_hrow(g, jsplit, 4) + 1) / 2, h8 = nown * g.Nmax * res_hrow(g, jsplit, 8);
     s.H = off;
     off = up(off + (h4 > h8 ? h4 : h8));
     s.Aj = CT * CT * KT + 1;
-    s.Aslot = (g.Lmax + 1) * s.Aj;
+    s.Aslot = (g.Nmax + 1) * s.Aj;
     s.Abuf = nown * s.Aslot;
     s.A = off;
     off = up(off + 2 * s.Abuf);
@@ -504,7 +504,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     const Inst s = load_inst(a, ph, b);
     const int nown = (g.Pcap + cs - 1) / cs;
     const ResPlan sp = res_plan(g, nown, a.jsplit, CT, KT, int(sizeof(V)));
-    uint64_t *rowbar = reinterpret_cast<uint64_t *>(sm + sp.rowbar);   // [nown][Lmax]
+    uint64_t *rowbar = reinterpret_cast<uint64_t *>(sm + sp.rowbar);   // [nown][Nmax]
     V *H = reinterpret_cast<V *>(sm + sp.H);
     V *A = reinterpret_cast<V *>(sm + sp.A);
     int64_t *sdv = sm + sp.sdv;
@@ -539,19 +539,19 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     const int mw_0 = __reduce_max_sync(0xFFFFFFFFu, dlive ? mlog : -1);
     const int nown_live = rank + 1 > s.P ? 0 : (s.P - rank - 1) / cs + 1;
 
-    // A entries (slot k, cut point j = i + 1 + r, width m) at e = (k * Lmax + r) * K + m:
+    // A entries (slot k, cut point j = i + 1 + r, width m) at e = (k * Nmax + r) * K + m:
     // a fixed numbering, so a thread's first entry is decoded once
-    const int a_total = nown_live * g.Lmax * K;
-    const int a_m = tid % K, a_r = (tid / K) % g.Lmax, a_k = tid / (K * g.Lmax);
+    const int a_total = nown_live * g.Nmax * K;
+    const int a_m = tid % K, a_r = (tid / K) % g.Nmax, a_k = tid / (K * g.Nmax);
     const bool a_have = tid < a_total;
     const uint64_t *a_src = s.loads + int64_t(a_have ? rank + a_k * cs : 0) * s.pos_loads + int64_t(a_r) * g.Kpad + a_m;
     V *a_dst = A + a_k * sp.Aslot + a_r * sp.Aj + a_m;
 
     const int64_t *Xg = reinterpret_cast<const int64_t *>(reinterpret_cast<const unsigned char *>(ph) + a.pl.X);
     for (int e = tid; e < (L + 1) * g.Cmax; e += blockDim.x) sm[sp.X + e] = Xg[e];
-    for (int q = tid; q < nown * g.Lmax; q += blockDim.x) mbar_init(&rowbar[q], 1);
+    for (int q = tid; q < nown * g.Nmax; q += blockDim.x) mbar_init(&rowbar[q], 1);
     // the padding in front of every row: cap (never written again)
-    for (int e = tid; e < nown * g.Lmax * g.Cmax * sp.Hpad; e += blockDim.x) {
+    for (int e = tid; e < nown * g.Nmax * g.Cmax * sp.Hpad; e += blockDim.x) {
         const int row = e / sp.Hpad;   // (slot, j, c') in order
         H[(row / g.Cmax) * sp.Hrow + (row % g.Cmax) * sp.Hcol + e % sp.Hpad] = cap;
     }
@@ -559,8 +559,8 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
     // arm the row barriers this CTA will receive: rows 1 .. L-1 of positions p_k - 1 >= 1
-    for (int q = tid; q < nown * g.Lmax; q += blockDim.x) {
-        const int k = q / g.Lmax, j = q % g.Lmax;
+    for (int q = tid; q < nown * g.Nmax; q += blockDim.x) {
+        const int k = q / g.Nmax, j = q % g.Nmax;
         const int p = rank + 1 + k * cs;
         if (p >= 2 && p <= s.P && j >= 1 && j < L) mbar_expect_tx(&rowbar[q], row_bytes);
     }
@@ -583,7 +583,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     };
     auto a_rows = [&](int i, int e0) {   // entries e0, e0 + blockDim.x, .. (decoded here)
         for (int e = e0; e < a_total; e += blockDim.x) {
-            const int m = e % K, r = (e / K) % g.Lmax, k = e / (K * g.Lmax);
+            const int m = e % K, r = (e / K) % g.Nmax, k = e / (K * g.Nmax);
             if (r >= L - i) continue;
             const int p = rank + 1 + k * cs, j = i + 1 + r;
             const uint64_t lw = s.loads[int64_t(p - 1) * s.pos_loads + (row_offset(i, L) + r) * g.Kpad + m];
@@ -597,7 +597,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     const int p0 = rank + 1 + kg * cs;
     const bool has0 = kg < nown_live && p0 < s.P;
     const uint32_t rrow0 = has0 ? cluster_map(H + (p0 / cs) * sp.Hslot + sp.Hpad, uint32_t(p0 % cs)) : 0;
-    const uint32_t bar0 = has0 ? cluster_map(&rowbar[(p0 / cs) * g.Lmax], uint32_t(p0 % cs)) : 0;
+    const uint32_t bar0 = has0 ? cluster_map(&rowbar[(p0 / cs) * g.Nmax], uint32_t(p0 % cs)) : 0;
     cluster_sync();  // first A rows built, pads and barriers set, every CTA started: pushes may begin
 
     int64_t ro = row_offset(L - 1, L);   // row_offset(i, L) of the current step
@@ -647,7 +647,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
                 // position p - 1 arrived during earlier steps but were not waited for yet
                 if (p == L - i)
                     for (int j = L - 1; j >= i + 2; j--)
-                        if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + j], 0, spin)) abort_flag = 1;
+                        if (!abort_flag && !mbar_wait(&rowbar[k * g.Nmax + j], 0, spin)) abort_flag = 1;
                 for (int t = 0; t < items; t++) {
                     const bool last = t == cnt;
                     const int j = last ? i + 1 : i + 2 + js + (t << lgs);
@@ -655,7 +655,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
                         // row i + 1 is the one the neighbour pushed last (bounded wait); it
                         // is the smallest cut point and wins ties, so compare against bv + 1
                         // until it has improved a running best
-                        if (!abort_flag && !mbar_wait(&rowbar[k * g.Lmax + i + 1], 0, spin)) abort_flag = 1;
+                        if (!abort_flag && !mbar_wait(&rowbar[k * g.Nmax + i + 1], 0, spin)) abort_flag = 1;
 #pragma unroll
                         for (int c = 0; c < CT; c++)
 #pragma unroll
@@ -701,7 +701,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
             } else if (push) {
                 const uint32_t crank = uint32_t(p % cs);
                 rrow = cluster_map(H + (p / cs) * sp.Hslot + i * sp.Hrow + sp.Hpad, crank);
-                bar = cluster_map(&rowbar[(p / cs) * g.Lmax + i], crank);
+                bar = cluster_map(&rowbar[(p / cs) * g.Nmax + i], crank);
             }
             const int so = ((i & 1) * nown + k) * sp.Srow;
             const bool aborted = abort_flag;
@@ -748,7 +748,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         for (int k = 0; k < nown; k++) {
             const int p = rank + 1 + k * cs;
             if (p < 2 || p > s.P) continue;
-            for (int j = 1; j < L; j++) mbar_wait(&rowbar[k * g.Lmax + j], 0, kDefaultSpin);
+            for (int j = 1; j < L; j++) mbar_wait(&rowbar[k * g.Nmax + j], 0, kDefaultSpin);
         }
     }
     cluster_sync();
@@ -787,7 +787,7 @@ __host__ __device__ inline StreamPlan stream_plan(const Geo &g, int jc, int jspl
     s.mbar = off;
     off += 16;
     s.X = off;
-    off = align_up(off + 8 * int64_t(g.Lmax + 1) * g.Cmax, 128);
+    off = align_up(off + 8 * int64_t(g.Nmax + 1) * g.Cmax, 128);
     s.dp_tile = 8 * int64_t(jc) * g.Cmax * g.Dpad;
     s.bs_tile = 8 * int64_t(jc) * g.Kpad;
     s.dp = off;
@@ -1125,7 +1125,7 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
         while (cluster < 8 && cluster * 2 <= g.Pcap && int64_t(n) * cluster * 2 <= sms) cluster *= 2;
     }
     const int threads = NTd * jsplit;
-    int jc = g.Lmax > 1 ? g.Lmax - 1 : 1;
+    int jc = g.Nmax > 1 ? g.Nmax - 1 : 1;
     while (jc > 1 && sweep_smem_bytes(g, jc, jsplit, threads) > budget) jc--;
     if (sweep_smem_bytes(g, jc, jsplit, threads) > budget) return NEST_E_LIMITS;
     out = {cluster, jsplit, jc, threads, 0, 1};

@@ -38,17 +38,17 @@ class NestError(RuntimeError):
 
 
 class Dims(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("B", "Lmax", "Tmax", "Cmax", "Smax", "Pcap", "Dumax", "reserved")]
+    _fields_ = [(n, C.c_int32) for n in ("B", "Lmax", "Tmax", "Cmax", "Smax", "Pcap", "Dumax", "Vmax")]
 
 
 class Layout(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("record_bytes", "fl", "pd", "pe", "ao", "aw", "a2a", "moe",
-                                         "G", "bw", "lat", "cand", "strat")]
+                                         "G", "bw", "lat", "cand", "strat", "succ")]
 
 
 class WsLayout(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("loads", "dpv", "dpa", "cost", "total", "total_costs")] + \
-               [(n, C.c_int32) for n in ("NP", "Kmax", "Kpad", "Spad", "Dpad", "chunk")]
+               [(n, C.c_int32) for n in ("NP", "Kmax", "Kpad", "Spad", "Dpad", "chunk", "N", "reserved")]
 
 
 class Options(C.Structure):
@@ -59,10 +59,10 @@ class Options(C.Structure):
 
 HEADER_DT = np.dtype([("L", "<i4"), ("D", "<i4"), ("unit", "<i4"), ("T", "<i4"), ("C", "<i4"),
                       ("S", "<i4"), ("Pmax", "<i4"), ("schedule", "<i4"), ("R", "<i8"), ("M", "<i8"),
-                      ("budget", "<i8"), ("opt_factor", "<i8")])
+                      ("budget", "<i8"), ("opt_factor", "<i8"), ("graph", "<i4"), ("reserved", "<i4")])
 PLAN_HDR_DT = np.dtype([("status", "<i4"), ("n_stages", "<i4"), ("t_batch", "<i8"), ("bottleneck", "<i8")])
 STAGE_DT = np.dtype([("i", "<i2"), ("j", "<i2"), ("s", "<i2"), ("c_next", "i1"), ("reserved", "i1"),
-                     ("k", "<i4")])
+                     ("k", "<i4"), ("reserved2", "<i4"), ("layers", "<u8")])
 
 _lib = None
 
@@ -100,12 +100,37 @@ def lib():
 # Geometry and packing
 # ---------------------------------------------------------------------------------
 
-def make_dims(instances: Sequence, Pcap: int | None = None, Dumax: int | None = None) -> Dims:
+def upset_count(succ, limit: int = 256) -> int:
+    """Number of up-sets of the layer DAG given by successor masks (the empty set
+    included), counted up to `limit` + 1: sizes the batch (nest_dims.Vmax); the
+    library enumerates and checks the states itself."""
+    L = len(succ)
+    sc = [int(v) for v in succ]
+    n = 0
+    stack = [(L - 1, 0)]          # decide layers from the last one down
+    while stack and n <= limit:
+        l, D = stack.pop()
+        if l < 0:
+            n += 1
+            continue
+        stack.append((l - 1, D))
+        if sc[l] & ~D == 0:
+            stack.append((l - 1, D | (1 << l)))
+    return n
+
+
+def make_dims(instances: Sequence, Pcap: int | None = None, Dumax: int | None = None,
+              Vmax: int | None = None) -> Dims:
+    """Batch dims covering `instances`; an instance with a `succ` attribute (not None)
+    is a graph instance, and Vmax defaults to its largest up-set count less one."""
+    if Vmax is None:
+        Vmax = max([upset_count(x.succ) - 1 for x in instances if getattr(x, "succ", None) is not None],
+                   default=0)
     return Dims(B=len(instances), Lmax=max(int(x.L) for x in instances),
                 Tmax=max(len(x.tierG) for x in instances), Cmax=max(len(x.cand) for x in instances),
                 Smax=max(len(x.strat) for x in instances),
                 Pcap=Pcap or max(int(x.Pmax) for x in instances),
-                Dumax=Dumax or max(int(x.D) // int(x.unit) for x in instances), reserved=0)
+                Dumax=Dumax or max(int(x.D) // int(x.unit) for x in instances), Vmax=Vmax)
 
 
 def record_layout(dims: Dims) -> Layout:
@@ -147,6 +172,8 @@ def pack_records(instances: Sequence, dims: Dims, out: np.ndarray | None = None)
             x.L, x.D, x.unit, len(x.tierG), len(x.cand), len(x.strat), x.Pmax)
         h["R"], h["M"], h["budget"], h["opt_factor"] = x.R, x.M, x.budget, x.opt_factor
         h["schedule"] = int(getattr(x, "schedule", 0))
+        succ = getattr(x, "succ", None)
+        h["graph"] = 0 if succ is None else 1
         row[:HEADER_DT.itemsize] = h.view(np.uint8)
 
         def put(off, arr, dt):
@@ -162,11 +189,14 @@ def pack_records(instances: Sequence, dims: Dims, out: np.ndarray | None = None)
         st = np.zeros((len(x.strat), 8), dtype="<i2")
         st[:, :5] = np.asarray(x.strat, dtype=np.int16).reshape(-1, 5)
         put(lay.strat, st, "<i2")
+        if succ is not None:
+            put(lay.succ, succ, "<u8")
     return buf
 
 
 def decode_plans(raw: np.ndarray, dims: Dims) -> List[dict]:
-    """Plan records -> [{status, t_batch, bottleneck, plan: [(i, j, k, s, c_next)]}]."""
+    """Plan records -> [{status, t_batch, bottleneck, plan: [(i, j, k, s, c_next)],
+    layers: [layer mask of each stage]}]."""
     pb = plan_bytes(dims)
     raw = np.ascontiguousarray(raw).view(np.uint8).reshape(dims.B, pb)
     out = []
@@ -177,7 +207,8 @@ def decode_plans(raw: np.ndarray, dims: Dims) -> List[dict]:
         out.append({"status": int(h["status"]), "t_batch": int(h["t_batch"]),
                     "bottleneck": int(h["bottleneck"]),
                     "plan": [(int(s["i"]), int(s["j"]), int(s["k"]), int(s["s"]), int(s["c_next"]))
-                             for s in st]})
+                             for s in st],
+                    "layers": [int(s["layers"]) for s in st]})
     return out
 
 

@@ -32,7 +32,7 @@ AW_FACTOR = 17      # working activation bytes = 17 x the block's output activat
 
 @dataclasses.dataclass
 class Instance:
-    """One placement problem: a layer chain, a tiered cluster and a strategy list."""
+    """One placement problem: a layer chain (or DAG), a tiered cluster and a strategy list."""
     L: int
     D: int
     unit: int
@@ -54,6 +54,7 @@ class Instance:
     cand: np.ndarray    # int32 [C] candidate tiers for links between stages
     strat: np.ndarray   # int16 [S, 5] strategies (t, cp, e, z, r)
     schedule: int = 0   # pipeline schedule: 0 = 1F1B, 1 = GPipe
+    succ: np.ndarray | None = None   # uint64 [L] successor masks of a layer DAG; None = chain
 
     @property
     def T(self) -> int:
@@ -364,4 +365,6 @@ TWO_TOWER_NAME = "two-tower-32L-h4096-64dev"
 def two_tower_instance(b: int) -> Instance:
     """Workload 2's blocks, tiers and budgets arranged as two 8-block encoder branches
     feeding a 16-block trunk (97 up-sets)."""
-    return config_instance(2, b)
+    x = config_instance(2, b)
+    x.succ = two_tower_succ()
+    return x

@@ -674,3 +674,22 @@ int64_t or_lattice_link(const or_instance *x, const uint64_t *succ, uint64_t D, 
     const int tr = x->cand[c];
     return x->lat[tr] + cdiv(bytes_in(x, succ, D, all) * 1000, x->bw[tr]);
 }
+
+/* Stage-cost words of every pair of states (i, j), i < j, in pair order (i, then j),
+ * all ones where state j is not inside state i: out[pair][m][s]. */
+void or_lattice_cost_tensor(const or_instance *x, const uint64_t *succ, const uint64_t *st, int ns, uint64_t *out) {
+    const int K = widths(x);
+    int64_t pair = 0;
+    for (int i = 0; i < ns; i++)
+        for (int j = i + 1; j < ns; j++, pair++)
+            for (int m = 0; m < K; m++)
+                for (int s = 0; s < x->S; s++) {
+                    uint64_t w = OR_INF;
+                    if (!(st[j] & ~st[i])) {
+                        or_terms r;
+                        or_lattice_terms(x, succ, st[i], st[j], m, s, &r);
+                        w = word_of(&r);
+                    }
+                    out[(pair * K + m) * x->S + s] = w;
+                }
+}

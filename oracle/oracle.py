@@ -79,6 +79,7 @@ def lib():
                                            P(_Terms)]
             L.or_lattice_link.argtypes = [P(_Inst), C.c_void_p, C.c_uint64, C.c_int]
             L.or_lattice_link.restype = C.c_int64
+            L.or_lattice_cost_tensor.argtypes = [P(_Inst), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p]
             L.or_solve_lattice.argtypes = [P(_Inst), C.c_void_p, C.c_void_p, P(C.c_int64), P(C.c_int64),
                                            P(C.c_int32), P(_Stage)]
             _lib = L
@@ -245,3 +246,20 @@ def solve_lattice(inst, succ, want_dp: bool = False) -> dict:
             for q in range(n.value)]
     return {"status": rc, "t_batch": t.value, "bottleneck": v.value, "plan": plan, "dp": dp,
             "states": st}
+
+
+def lattice_pair_tables(inst, succ) -> tuple[np.ndarray, np.ndarray]:
+    """Over every pair of states (i, j), i < j, in pair order: the stage-cost words
+    [NP, K, S] and the per-position loads [NP, K, Pmax], all ones where state j is
+    not inside state i."""
+    m, sc = Marshalled(inst), _succ(succ)
+    st = lattice_states(inst, succ)
+    ns = len(st)
+    npairs = ns * (ns - 1) // 2
+    cost = np.empty((npairs, m.K, m.s.S), dtype=np.uint64)
+    lib().or_lattice_cost_tensor(C.byref(m.s), sc.ctypes.data, st.ctypes.data, ns, cost.ctypes.data)
+    pairs, ld = lattice_loads(inst, succ)
+    loads = np.full((npairs, m.K, inst.Pmax), INF, dtype=np.uint64)
+    for t, (i, j) in enumerate(pairs):
+        loads[i * (ns - 1) - i * (i - 1) // 2 + (j - i - 1)] = ld[t]
+    return cost, loads

@@ -17,17 +17,23 @@ def ensure_built():
 
 
 def run(instances, chunk=0, cluster=0, jsplit=0, spin_limit=0, Pcap=None, Dumax=None, variant=0,
-        keep_costs=True):
+        keep_costs=True, Vmax=None):
     """Solve on cuda:0 (keeping the stage-cost tensor for inspection unless told
     otherwise); returns (solver, results)."""
     import torch
-    dims = nest.make_dims(instances, Pcap=Pcap, Dumax=Dumax)
+    dims = nest.make_dims(instances, Pcap=Pcap, Dumax=Dumax, Vmax=Vmax)
     s = nest.Solver(dims, chunk=chunk, keep_costs=keep_costs)
     s.load(nest.pack_records(instances, dims))
     s.run(opt=nest.options(chunk=chunk, cluster=cluster, jsplit=jsplit, spin_limit=spin_limit,
                            variant=variant, keep_costs=keep_costs))
     torch.cuda.synchronize()
     return s, s.results()
+
+
+def last_state(inst):
+    """Index of the empty state: L for a chain, the up-set count less one for a graph."""
+    succ = getattr(inst, "succ", None)
+    return int(inst.L) if succ is None else nest.upset_count(succ) - 1
 
 
 def _slice(ws, off, count, dtype):
@@ -40,8 +46,8 @@ def cost_table(s, b, inst):
     per = lay.NP * lay.Kmax * lay.Spad
     t = _slice(s.workspace, lay.cost + 8 * per * b, per, U64).reshape(lay.NP, lay.Kmax, lay.Spad)
     K = (inst.D // inst.unit).bit_length()
-    npi = inst.L * (inst.L + 1) // 2
-    return t[:npi, :K, :len(inst.strat)]
+    E = last_state(inst)
+    return t[:E * (E + 1) // 2, :K, :len(inst.strat)]
 
 
 def loads_table(s, b, inst):
@@ -49,26 +55,26 @@ def loads_table(s, b, inst):
     per = s.dims.Pcap * lay.NP * lay.Kpad
     t = _slice(s.workspace, lay.loads + 8 * per * b, per, U64).reshape(s.dims.Pcap, lay.NP, lay.Kpad)
     K = (inst.D // inst.unit).bit_length()
-    npi = inst.L * (inst.L + 1) // 2
-    return np.transpose(t[:inst.Pmax, :npi, :K], (1, 2, 0))   # [pair][m][p-1] like the oracle
+    E = last_state(inst)
+    return np.transpose(t[:inst.Pmax, :E * (E + 1) // 2, :K], (1, 2, 0))   # [pair][m][p-1] like the oracle
 
 
 def dp_keys(s, b, inst):
     """GPU DP table as packed keys in the oracle's [i][d][p][c] order (p >= 1, i < L)."""
     lay = nest.workspace_layout(s.dims, s.chunk)
-    shape = (s.dims.Pcap, s.dims.Lmax, s.dims.Cmax, lay.Dpad)
+    shape = (s.dims.Pcap, lay.N, s.dims.Cmax, lay.Dpad)
     per = int(np.prod(shape))
     v = _slice(s.workspace, lay.dpv + 8 * per * b, per, np.int64).reshape(shape)
     a = _slice(s.workspace, lay.dpa + 4 * per * b, per, np.uint32).reshape(shape)
-    Du, C = inst.D // inst.unit, len(inst.cand)
-    v = v[:inst.Pmax, :inst.L, :C, :Du + 1].astype(U64)
-    a = a[:inst.Pmax, :inst.L, :C, :Du + 1].astype(U64)
+    Du, C, E = inst.D // inst.unit, len(inst.cand), last_state(inst)
+    v = v[:inst.Pmax, :E, :C, :Du + 1].astype(U64)
+    a = a[:inst.Pmax, :E, :C, :Du + 1].astype(U64)
     keys = (v << U64(24)) | a
     return np.transpose(keys, (1, 3, 0, 2))   # [i][d][p-1][c]
 
 
 def oracle_dp_keys(inst, dp):
-    return dp[:inst.L, :, 1:, :]
+    return dp[:last_state(inst), :, 1:, :]
 
 
 def oracle_many(instances, fn=O.solve, threads=None):
@@ -99,3 +105,26 @@ def scaled(inst, factor):
 def same_result(g, o):
     return (g["status"] == o["status"] and g["t_batch"] == o["t_batch"] and
             (g["status"] != 0 or (g["bottleneck"] == o["bottleneck"] and g["plan"] == o["plan"])))
+
+
+def solve_graph(inst):
+    return O.solve_lattice(inst, inst.succ)
+
+
+def check_graph_tables(s, b, inst):
+    """Every table of graph instance b against the oracle over up-sets; returns the
+    oracle's result."""
+    cost, loads = O.lattice_pair_tables(inst, inst.succ)
+    np.testing.assert_array_equal(cost_table(s, b, inst), cost)
+    np.testing.assert_array_equal(loads_table(s, b, inst), loads)
+    o = O.solve_lattice(inst, inst.succ, want_dp=True)
+    np.testing.assert_array_equal(dp_keys(s, b, inst), oracle_dp_keys(inst, o["dp"]))
+    return o
+
+
+def same_graph_result(g, o):
+    """Results equal, and each stage's layer mask is states[i] minus states[j]."""
+    if not same_result(g, o):
+        return False
+    st = o["states"]
+    return g["status"] != 0 or g["layers"] == [int(st[i]) & ~int(st[j]) for i, j, *_ in o["plan"]]

@@ -63,7 +63,8 @@ def test_pack_roundtrip():
 
 
 @pytest.mark.parametrize("field,value", [("Lmax", 256), ("Lmax", 0), ("Tmax", 9), ("Cmax", 16),
-                                         ("Smax", 4096), ("Pcap", 32), ("Dumax", 513), ("Dumax", 0)])
+                                         ("Smax", 4096), ("Pcap", 32), ("Dumax", 513), ("Dumax", 0),
+                                         ("Vmax", 256), ("Vmax", -1)])
 def test_limits_rejected_on_host(field, value):
     dims = nest.make_dims(synth.config_batch(2, B=2))
     setattr(dims, field, value)
@@ -74,8 +75,28 @@ def test_limits_rejected_on_host(field, value):
 
 
 def test_largest_dims_accepted():
-    dims = nest.Dims(B=1, Lmax=255, Tmax=8, Cmax=15, Smax=4095, Pcap=31, Dumax=512)
-    assert nest.workspace_size(dims) > 0 and nest.plan_bytes(dims) == 24 + 12 * 31 + 4
+    dims = nest.Dims(B=1, Lmax=255, Tmax=8, Cmax=15, Smax=4095, Pcap=31, Dumax=512, Vmax=255)
+    assert nest.workspace_size(dims) > 0 and nest.plan_bytes(dims) == 24 + 24 * 31
+    assert nest.STAGE_DT.itemsize == 24 and nest.HEADER_DT.itemsize == 72
+
+
+def test_state_dimension_follows_the_larger_of_layers_and_up_sets():
+    base = dict(B=1, Lmax=32, Tmax=3, Cmax=2, Smax=12, Pcap=16, Dumax=64)
+    chain = nest.workspace_layout(nest.Dims(**base, Vmax=0))
+    graph = nest.workspace_layout(nest.Dims(**base, Vmax=96))
+    assert (chain.N, chain.NP) == (32, 32 * 33 // 2)
+    assert (graph.N, graph.NP) == (96, 96 * 97 // 2)
+    assert nest.workspace_layout(nest.Dims(**base, Vmax=20)).N == 32
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_upset_count_sizes_the_batch(seed):
+    O = pytest.importorskip("oracle.oracle")
+    x = synth.random_tiny(seed, Lmax=8)
+    succ = synth.random_dag(seed, x.L, (0.1, 0.4, 0.8)[seed % 3])
+    assert nest.upset_count(succ) == len(O.lattice_states(x, succ))
+    assert nest.upset_count(synth.two_tower_succ()) == 97
+    assert nest.upset_count(synth.chain_succ(12)) == 13
 
 
 def test_bad_arguments_rejected_before_any_launch():

@@ -422,3 +422,33 @@ def test_every_table_cell_matches_enumeration(chunk):
         assert np.array_equal(r["dp"], want), seed
         nonempty += int(np.count_nonzero(want[:-1] != INF))
     assert nonempty > 1000
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_pair_tables_cover_every_pair_of_states(seed):
+    x, succ = tiny(seed + 1500, Lmax=6)
+    st = [int(v) for v in O.lattice_states(x, succ)]
+    cost, loads = O.lattice_pair_tables(x, succ)
+    K = (x.D // x.unit).bit_length()
+    pairs, ld = O.lattice_loads(x, succ)
+    want = dict(zip(pairs, ld))
+    q = 0
+    for i in range(len(st)):
+        for j in range(i + 1, len(st)):
+            nested = not (st[j] & ~st[i])
+            assert nested == ((i, j) in want)
+            if nested:
+                np.testing.assert_array_equal(loads[q], want[(i, j)])
+                for m in range(K):
+                    for s in range(len(x.strat)):
+                        t = O.lattice_terms(x, succ, st[i], st[j], m, s)
+                        w = INF if not t["valid"] or t["tau"] >= CAP else (t["tau"] << 8) | t["pmax"]
+                        assert int(cost[q, m, s]) == w
+            else:
+                assert (cost[q] == INF).all() and (loads[q] == INF).all()
+            q += 1
+    # a chain's tables are the chain oracle's
+    y = synth.random_tiny(seed + 1600, Lmax=7)
+    c2, l2 = O.lattice_pair_tables(y, synth.chain_succ(y.L))
+    np.testing.assert_array_equal(c2, O.cost_tensor(y))
+    np.testing.assert_array_equal(l2, O.loads(y))
