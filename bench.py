@@ -41,16 +41,38 @@ KERNEL_SRC = {"prep": "nest_prep.cu", "stage_loads": "nest_loads.cu", "dp_sweep"
 L2_FLUSH_BYTES = 256 << 20
 
 
+def states(x) -> list:
+    """The DP states of an instance as layer masks, in DP order: the suffixes of a
+    chain, or the up-sets of a layer DAG by size descending then mask ascending."""
+    if getattr(x, "succ", None) is None:
+        return [((1 << x.L) - 1) ^ ((1 << i) - 1) for i in range(x.L + 1)]
+    succ = [int(v) for v in x.succ]
+    out, stack = [], [(x.L - 1, 0)]
+    while stack:
+        l, D = stack.pop()
+        if l < 0:
+            out.append(D)
+            continue
+        stack.append((l - 1, D))
+        if succ[l] & ~D == 0:
+            stack.append((l - 1, D | (1 << l)))
+    return sorted(out, key=lambda D: (-bin(D).count("1"), D))
+
+
 def relaxations(x) -> int:
     """Min-max transitions (j, m, c') the recurrence evaluates for one instance:
-    every cell (i, d, p, c) times its cut points j, widths m <= log2 d allowed by
-    the link tier, and next-link candidates c' allowed for that width."""
-    L, Du, P, C, u = x.L, x.D // x.unit, x.Pmax, len(x.cand), x.unit
+    every cell (i, d, p, c) times its cut points j (states inside state i), widths
+    m <= log2 d allowed by the link tier, and next-link candidates c' allowed for
+    that width."""
+    Du, P, C, u = x.D // x.unit, x.Pmax, len(x.cand), x.unit
     G = [int(x.tierG[c]) for c in x.cand]
     K = Du.bit_length()
+    st = states(x)
+    E = len(st) - 1
     tot = 0
-    for i in range(L):
-        Pi = min(P, L - i)
+    for i in range(E):
+        Pi = min(P, bin(st[i]).count("1"))
+        inner = sum(1 for j in range(i + 1, E) if st[j] & ~st[i] == 0)   # cut points before the end
         for c in range(1 if i == 0 else C):
             for m in range(K):
                 k = u << m
@@ -58,12 +80,22 @@ def relaxations(x) -> int:
                     continue
                 nd = Du - (1 << m) + 1
                 ncp = sum(1 for g in G if 2 * k <= g)
-                tot += nd * (1 + (Pi - 1) * (L - 1 - i) * ncp)
+                tot += nd * (1 + (Pi - 1) * inner * ncp)
     return tot
 
 
+def state_pairs(x) -> int:
+    E = len(states(x)) - 1
+    return E * (E + 1) // 2
+
+
 def cost_words(x) -> int:
-    return x.L * (x.L + 1) // 2 * (x.D // x.unit).bit_length() * len(x.strat)
+    return state_pairs(x) * (x.D // x.unit).bit_length() * len(x.strat)
+
+
+def oracle_solve(x):
+    from oracle import oracle as O
+    return O.solve(x) if getattr(x, "succ", None) is None else O.solve_lattice(x, x.succ)
 
 
 def src_hash(kernel: str) -> str:
@@ -177,7 +209,7 @@ def cpu_baseline(instances, relax_total, seconds=12.0):
     passes = 0
     with ThreadPoolExecutor(max_workers=cores) as ex:
         while True:
-            list(ex.map(O.solve, instances))
+            list(ex.map(oracle_solve, instances))
             passes += 1
             if time.perf_counter() - t0 >= seconds:
                 break
@@ -210,7 +242,7 @@ def run_reference(args, workload, instances, relax_total):
         for step in range(args.warmup + args.steps):
             idx = [(step * n + q) % len(instances) for q in range(n)]
             t0 = time.perf_counter()
-            list(ex.map(O.solve, [instances[q] for q in idx]))
+            list(ex.map(oracle_solve, [instances[q] for q in idx]))
             dt = time.perf_counter() - t0
             if step >= args.warmup:
                 times.append(dt)
@@ -264,6 +296,9 @@ def main():
                     help="microbatches per iteration under --schedule gpipe (4096 do not fit in memory)")
     ap.add_argument("--topology", default="tiers", choices=["tiers", "torus"],
                     help="torus: the dense workload's problems on a 4x4x4 torus of 64 chips, tiers = hop classes")
+    ap.add_argument("--graph", default="chain", choices=["chain", "two-tower"],
+                    help="two-tower: the dense workload's blocks as two 8-block encoder branches feeding a "
+                         "16-block trunk, solved over the up-sets of that layer DAG")
     ap.add_argument("--joint", action="store_true",
                     help="joint microbatch-size search: every problem solved with 1, 2, 4 and 8 samples "
                          "per microbatch, the best variant selected on the GPU")
@@ -280,6 +315,11 @@ def main():
             raise SystemExit("--topology torus applies to workload 2 (64 devices)")
         instances = [synth.torus_instance(rank * B + b) for b in range(B)]
         workload = synth.TORUS_NAME
+    if args.graph == "two-tower":
+        if args.workload != 2 or args.topology != "tiers":
+            raise SystemExit("--graph two-tower applies to workload 2 on its tiers")
+        instances = [synth.two_tower_instance(rank * B + b) for b in range(B)]
+        workload = synth.TWO_TOWER_NAME
     if args.schedule == "gpipe":
         for x in instances:
             x.schedule, x.M = 1, max(args.gpipe_microbatches, x.Pmax)
@@ -384,7 +424,8 @@ def main():
     ms_per_step = total_ms / args.steps
     value = job_relax / (ms_per_step * 1e-3)
     solves = B * ws / (ms_per_step * 1e-3)
-    launches = (len(KERNELS) * nchunks + (1 if group > 1 else 0)) * args.steps
+    plan = nest.describe_launch(dims, nest.options(chunk=args.chunk))
+    launches = (plan["kernels_per_chunk"] * plan["chunks"] + (1 if group > 1 else 0)) * args.steps
 
     # end to end through the host-buffer entry point: H2D records, solve, D2H results
     e2e_steps = args.e2e_steps or min(args.steps, 500)
@@ -448,7 +489,7 @@ def main():
                 "derived_64bit_peak": derived, "sm_mhz_seen": mhz}
     else:
         # the per-position loads table is what the stage-loads kernel must write
-        loads_bytes = sum(8 * x.Pmax * (x.L * (x.L + 1) // 2) * (x.D // x.unit).bit_length() for x in instances)
+        loads_bytes = sum(8 * x.Pmax * state_pairs(x) * (x.D // x.unit).bit_length() for x in instances)
         algo = {"stage_loads": loads_bytes, "prep": 0, "backtrack": 0}[dom]
         achieved = algo / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -464,7 +505,7 @@ def main():
                 "config": {"workload": workload, "batch_per_gpu": B, "chunk": chunk,
                            "relaxations_per_batch": relax_total, "cost_words_per_batch": words,
                            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
-                           "parallelism": f"replicas{ws}"},
+                           "parallelism": f"replicas{ws}", "launch": plan},
                 "solves_per_s": solves,
                 **({"problems_per_s": solves / group, "variants_per_problem": group} if group > 1 else {}),
                 "kernel_ms_per_step": kms,

@@ -245,6 +245,28 @@ typedef struct {
 } nest_ws_layout;
 int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *out);
 
+/* ---- launch description ----------------------------------------------------------
+ * What nest_solve launches for these dims and options on the current device, without
+ * launching anything: the passes, the kernels of a pass and the DP-sweep shape.  The
+ * sweep shape follows the device's shared memory and occupancy, so call it with the
+ * device current that will run the solve.  When the resident sweep sized for 32-bit
+ * value words alone (instances whose largest load plus two link costs stays below
+ * 2^30 ns) needs fewer waves than one sized for both widths, the sweep is split:
+ * that launch takes the 32-bit instances and a second launch the others.
+ * Returns NEST_OK, NEST_E_INVALID (null pointer, bad option) or NEST_E_LIMITS. */
+typedef struct {
+    int32_t chunks;             /* passes through the kernels */
+    int32_t kernels_per_chunk;  /* launches per pass: prep, stage loads, sweep (1 or 2), backtrack */
+    int32_t sweep_variant;      /* 1 = rows resident in shared memory, 2 = streamed from global memory */
+    int32_t sweep_cluster;      /* CTAs per instance */
+    int32_t sweep_jsplit;       /* threads per DP cell */
+    int32_t sweep_threads;      /* threads per CTA */
+    int32_t sweep_split;        /* 1: a second sweep launch (wide_*) takes the 64-bit-word instances */
+    int32_t wide_variant, wide_cluster, wide_jsplit, wide_threads;
+    int32_t reserved;
+} nest_launch_desc;
+int nest_describe_launch(const nest_dims *dims, const nest_options *opt, nest_launch_desc *out);
+
 /* ---- joint search over variants -------------------------------------------------
  * Nest §5.2.3 explores the microbatch size together with the placement.  The
  * variants of a problem (e.g. the same model with 1, 2, 4 and 8 samples per

@@ -89,6 +89,51 @@ int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *
     return NEST_OK;
 }
 
+int nest_describe_launch(const nest_dims *dims, const nest_options *opt, nest_launch_desc *out) {
+    if (!dims || !out) return NEST_E_INVALID;
+    Geo g;
+    if (dims->B < 0) return NEST_E_INVALID;
+    if (!make_geo(*dims, g)) return NEST_E_LIMITS;
+    const int32_t chunk = chunk_of(dims, opt ? opt->chunk : 0);
+    SweepConfig cfg;
+    const int rc = sweep_configure(g, chunk < 1 ? 1 : chunk, opt ? opt->sweep_cluster : 0,
+                                   opt ? opt->sweep_jsplit : 0, opt ? opt->sweep_variant : 0, cfg);
+    if (rc != NEST_OK) return rc;
+    std::memset(out, 0, sizeof *out);
+    out->chunks = dims->B == 0 ? 0 : (dims->B + chunk - 1) / chunk;
+    out->kernels_per_chunk = cfg.split ? 5 : 4;
+    out->sweep_variant = cfg.resident ? 1 : 2;
+    out->sweep_cluster = cfg.cluster;
+    out->sweep_jsplit = cfg.jsplit;
+    out->sweep_threads = cfg.threads;
+    out->sweep_split = cfg.split;
+    if (cfg.split) {
+        out->wide_variant = cfg.wide.resident ? 1 : 2;
+        out->wide_cluster = cfg.wide.cluster;
+        out->wide_jsplit = cfg.wide.jsplit;
+        out->wide_threads = cfg.wide.threads;
+    }
+    return NEST_OK;
+}
+
+// The DP sweep of one pass: one launch, or the 32-bit-word launch followed by the
+// 64-bit-word one (each leaves the other's instances alone).
+static int sweep_pass(PassArgs a, const SweepConfig &cfg, void *stream) {
+    if (!cfg.split) {
+        a.word_mode = 0;
+        return launch_sweep(a, stream);
+    }
+    a.word_mode = 1;
+    if (int rc = launch_sweep(a, stream)) return rc;
+    a.word_mode = 2;
+    a.cluster = cfg.wide.cluster;
+    a.jsplit = cfg.wide.jsplit;
+    a.jc = cfg.wide.jc;
+    a.threads = cfg.wide.threads;
+    a.resident = cfg.wide.resident;
+    return launch_sweep(a, stream);
+}
+
 int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, void *plans_out,
                void *workspace, size_t ws_bytes, void *stream, const nest_options *opt) {
     if (!dims) return NEST_E_INVALID;
@@ -138,8 +183,8 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
         a.costs_out = costs_out + first;
         a.plans_out = static_cast<unsigned char *>(plans_out) + int64_t(first) * a.plan_stride;
         if ((rc = mark(ci, 0)) || (rc = launch_prep(a, st)) || (rc = mark(ci, 1)) || (rc = launch_loads(a, st)) ||
-            (rc = mark(ci, 2)) || (rc = launch_sweep(a, st)) || (rc = mark(ci, 3)) || (rc = launch_backtrack(a, st)) ||
-            (rc = mark(ci, 4)))
+            (rc = mark(ci, 2)) || (rc = sweep_pass(a, cfg, st)) || (rc = mark(ci, 3)) ||
+            (rc = launch_backtrack(a, st)) || (rc = mark(ci, 4)))
             return rc;
     }
     return NEST_OK;

@@ -190,7 +190,8 @@ struct PassArgs {
     int32_t resident;              // sweep variant: 1 = dp rows resident in shared memory
     int64_t spin_limit;            // polls per bounded wait (negative: give up at once)
     int32_t keep_costs;            // also write the stage-cost tensor
-    int32_t pad;
+    int32_t word_mode;             // sweep launch takes: 0 every instance, 1 those on 32-bit
+                                   // words only, 2 those on 64-bit words only
 };
 
 __host__ __device__ inline PrepHdr *prep_hdr(const PassArgs &a, int b) {
@@ -243,13 +244,20 @@ int launch_sweep(const PassArgs &a, void *stream);
 int launch_backtrack(const PassArgs &a, void *stream);
 // Dynamic shared memory of the streaming and resident sweep variants.
 int64_t sweep_smem_bytes(const Geo &g, int jc, int jsplit, int threads);
-int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads);
+int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads, int mode);
 
 // Launch shape of the DP sweep for passes of n instances.  cluster_opt / jsplit_opt
 // (0 = choose) and variant (0 = choose, 1 = resident, 2 = streaming) come from
-// nest_options.  Returns NEST_OK, NEST_E_INVALID or NEST_E_LIMITS.
+// nest_options.  With split set, the sweep is two launches: the resident shape above
+// sized for the instances on 32-bit words alone (word_mode 1), then `wide` for those
+// on 64-bit words (word_mode 2).  Returns NEST_OK, NEST_E_INVALID or NEST_E_LIMITS.
+struct SweepShape {
+    int cluster, jsplit, jc, threads, resident, resident_waves;
+};
 struct SweepConfig {
     int cluster, jsplit, jc, threads, resident, resident_waves;
+    int split;
+    SweepShape wide;
 };
 int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int variant, SweepConfig &out);
 

@@ -320,7 +320,9 @@ __device__ __forceinline__ bool narrow_words(const PrepHdr *ph) {
 //  - A[buf][slot][j][c][c'][m] = load*(i, j, m, p) + X[i][c] + X[j][c'] when both
 //    links admit the width, else `far`; A[j] holds an odd number of values (banks).
 //  - staged dp rows [2][slot][Cmax][Dpad] (int64 values, uint32 arguments).
-// The H region is sized for whichever word width needs more.
+// The H and A regions are sized for whichever word width needs more, or, for a launch
+// that takes only the instances of one word width (`mode` 1: 32-bit, 2: 64-bit), for
+// that width alone.
 struct ResPlan {
     int rowbar, X, H, A, sdv, sda, total;  // word offsets; total = words
     int Hpad, Hcol, Hrow, Hslot;           // H strides in values of the chosen width
@@ -328,18 +330,23 @@ struct ResPlan {
     int Srow;                              // values per staged dp row: Cmax * Dpad
 };
 
-__host__ __device__ inline int res_hpad(const Geo &g, int vbytes) {
-    return vbytes == 4 ? ((1 << (g.Kmax - 1)) + 3) & ~3 : 0;
+// Cap columns in front of a 32-bit row.  A warp covers 32 / jsplit consecutive device
+// counts d_lo .. d_hi and reads widths up to 2^mw <= d_hi, so no lane reads further
+// than 32 / jsplit - 1 columns below x = 0 (nor than 2^(Kmax-1) - 1).
+__host__ __device__ inline int res_hpad(const Geo &g, int jsplit, int vbytes) {
+    const int reach = (1 << (g.Kmax - 1)) < 32 / jsplit ? (1 << (g.Kmax - 1)) : 32 / jsplit;
+    return vbytes == 4 ? (reach + 3) & ~3 : 0;
 }
 
 __host__ __device__ inline int res_hrow(const Geo &g, int jsplit, int vbytes) {
     const int s = vbytes / 4, mod = 32 / s, want = (32 / jsplit / s) % mod;
-    int h = g.Cmax * (res_hpad(g, vbytes) + g.Dpad);
+    int h = g.Cmax * (res_hpad(g, jsplit, vbytes) + g.Dpad);
     while (h % mod != want) h++;
     return h;
 }
 
-__host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, int CT, int KT, int vbytes) {
+__host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, int CT, int KT, int vbytes,
+                                            int mode) {
     ResPlan s;
     auto up = [](int w) { return (w + 15) / 16 * 16; };   // 128-byte alignment
     int off = 0;
@@ -347,18 +354,18 @@ __host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, 
     off = up(off + nown * g.Nmax);
     s.X = off;
     off = up(off + (g.Nmax + 1) * g.Cmax);
-    s.Hpad = res_hpad(g, vbytes);
+    s.Hpad = res_hpad(g, jsplit, vbytes);
     s.Hcol = s.Hpad + g.Dpad;
     s.Hrow = res_hrow(g, jsplit, vbytes);
     s.Hslot = g.Nmax * s.Hrow;
     const int h4 = (nown * g.Nmax * res_hrow(g, jsplit, 4) + 1) / 2, h8 = nown * g.Nmax * res_hrow(g, jsplit, 8);
     s.H = off;
-    off = up(off + (h4 > h8 ? h4 : h8));
+    off = up(off + (mode == 1 ? h4 : mode == 2 ? h8 : h4 > h8 ? h4 : h8));
     s.Aj = CT * CT * KT + 1;
     s.Aslot = (g.Nmax + 1) * s.Aj;
     s.Abuf = nown * s.Aslot;
     s.A = off;
-    off = up(off + 2 * s.Abuf);
+    off = up(off + (mode == 1 ? s.Abuf : 2 * s.Abuf));   // two buffers of 4- or 8-byte values
     s.Srow = g.Cmax * g.Dpad;
     s.sdv = off;
     off = up(off + 2 * nown * s.Srow);
@@ -503,7 +510,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     const int cs = a.cluster;
     const Inst s = load_inst(a, ph, b);
     const int nown = (g.Pcap + cs - 1) / cs;
-    const ResPlan sp = res_plan(g, nown, a.jsplit, CT, KT, int(sizeof(V)));
+    const ResPlan sp = res_plan(g, nown, a.jsplit, CT, KT, int(sizeof(V)), a.word_mode);
     uint64_t *rowbar = reinterpret_cast<uint64_t *>(sm + sp.rowbar);   // [nown][Nmax]
     V *H = reinterpret_cast<V *>(sm + sp.H);
     V *A = reinterpret_cast<V *>(sm + sp.A);
@@ -765,8 +772,11 @@ __global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs
     const int rank = int(cluster_rank());
     PrepHdr *ph = prep_hdr(a, b);
     if (ph->status != NEST_SOLVED) return;  // uniform over the cluster
-    // the word width is uniform over the cluster too: every CTA reads the same header
-    if (narrow_words(ph))
+    // the word width is uniform over the cluster too: every CTA reads the same header;
+    // a launch for one width leaves the other width's instances to its companion launch
+    const bool narrow = narrow_words(ph);
+    if ((a.word_mode == 1 && !narrow) || (a.word_mode == 2 && narrow)) return;
+    if (narrow)
         resident_body<CT, KT, uint32_t>(a, ph, b, rank, sm, abort_flag);
     else
         resident_body<CT, KT, int64_t>(a, ph, b, rank, sm, abort_flag);
@@ -813,6 +823,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) sweep_stream_kernel(PassArgs a
     const int rank = int(cluster_rank());
     PrepHdr *ph = prep_hdr(a, b);
     if (ph->status != NEST_SOLVED) return;  // uniform over the cluster
+    if (a.word_mode == 2 && narrow_words(ph)) return;   // taken by the resident launch
     const Inst s = load_inst(a, ph, b);
     const StreamPlan sp = stream_plan(g, a.jc, a.jsplit, a.threads);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + sp.mbar);
@@ -1006,7 +1017,7 @@ int resident_capacity_ct(const Geo &g, int cluster, int threads, size_t smem) {
 template <int CT, int KT>
 int launch_resident(const PassArgs &a, void *stream) {
     if (a.cluster < 2 && a.g.Pcap > 1) return NEST_E_LIMITS;   // pushes need a peer CTA
-    const size_t smem = size_t(sweep_resident_smem_bytes(a.g, a.cluster, a.jsplit, a.threads));
+    const size_t smem = size_t(sweep_resident_smem_bytes(a.g, a.cluster, a.jsplit, a.threads, a.word_mode));
     return launch_cluster(sweep_resident_kernel<CT, KT>, a, stream, smem, "sweep (resident) launch");
 }
 
@@ -1030,10 +1041,32 @@ int64_t sweep_smem_bytes(const Geo &g, int jc, int jsplit, int threads) {
     return stream_plan(g, jc, jsplit, threads).total;
 }
 
-int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads) {
+int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads, int mode) {
     const int nown = (g.Pcap + cluster - 1) / cluster;
     (void)threads;
-    return 8 * int64_t(res_plan(g, nown, jsplit, ct_of(g.Cmax), kt_of(g.Kmax), 8).total);
+    return 8 * int64_t(res_plan(g, nown, jsplit, ct_of(g.Cmax), kt_of(g.Kmax), 8, mode).total);
+}
+
+// Streaming shape: one thread per (slice, device count) holding every candidate.
+static int stream_shape(const Geo &g, int n, int cluster_opt, int jsplit_opt, int sms, int64_t budget, SweepShape &out) {
+    const int NTd = (g.Dumax + 31) / 32 * 32;
+    int jsplit = jsplit_opt;
+    if (jsplit == 0) {
+        jsplit = 1;
+        while (jsplit < 8 && NTd * jsplit * 2 <= kMaxThreads) jsplit *= 2;
+    }
+    if (NTd * jsplit > kMaxThreads) return NEST_E_INVALID;
+    int cluster = cluster_opt;
+    if (cluster == 0) {
+        cluster = 1;
+        while (cluster < 8 && cluster * 2 <= g.Pcap && int64_t(n) * cluster * 2 <= sms) cluster *= 2;
+    }
+    const int threads = NTd * jsplit;
+    int jc = g.Nmax > 1 ? g.Nmax - 1 : 1;
+    while (jc > 1 && sweep_smem_bytes(g, jc, jsplit, threads) > budget) jc--;
+    if (sweep_smem_bytes(g, jc, jsplit, threads) > budget) return NEST_E_LIMITS;
+    out = {cluster, jsplit, jc, threads, 0, 1};
+    return NEST_OK;
 }
 
 int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int variant, SweepConfig &out) {
@@ -1046,19 +1079,23 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
     auto ok_cluster = [](int c) { return c == 1 || c == 2 || c == 4 || c == 8 || c == 16; };
     auto ok_jsplit = [](int j) { return j == 1 || j == 2 || j == 4 || j == 8; };
     if ((cluster_opt && !ok_cluster(cluster_opt)) || (jsplit_opt && !ok_jsplit(jsplit_opt))) return NEST_E_INVALID;
-    const int NTd = (g.Dumax + 31) / 32 * 32;
 
     // resident: one thread per (device count, slice) holding every candidate, the
     // slices of a device count in adjacent lanes, and up to ngrp such groups per CTA
     // working on different positions.  Prefer every instance's cluster resident at
     // once, then the fewest positions per CTA (positions sharing an SM, whether in
     // turn or in parallel groups, slow each other down about as much), then larger
-    // clusters, then groups of about 8 warps (more warps add per-step work, fewer
-    // hide less latency).
-    if (variant != 2 && g.Cmax <= 4) {
-        double best = 0;
-        SweepConfig pick = {};
-        int64_t pick_ctas = 0;   // CTAs of the pick resident at once
+    // clusters, then groups of about 8 warps per 32 states, 16 at most (more warps
+    // add per-step work, fewer hide less latency; a step relaxes up to one cut point
+    // per later state).  `mode` sizes shared memory for both word widths (0), or for
+    // a launch that takes the instances of one width only (1: 32-bit, 2: 64-bit).
+    struct Pick {
+        double best;
+        SweepShape shape;
+        int64_t ctas;   // CTAs resident at once
+    };
+    auto search = [&](int mode) {
+        Pick r = {0.0, {}, 0};
         const int cl_list[5] = {16, 8, 4, 2, 1};
         const int js_list[4] = {8, 4, 2, 1};
         for (int ci = 0; ci < 5; ci++) {
@@ -1078,57 +1115,82 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
                 const int nown_c = (g.Pcap + cs - 1) / cs;
                 const int ngrp = nown_c < kMaxThreads / gsize ? nown_c : kMaxThreads / gsize;
                 const int threads = ngrp * gsize;
-                const int64_t smem = sweep_resident_smem_bytes(g, cs, js, threads);
+                const int64_t smem = sweep_resident_smem_bytes(g, cs, js, threads, mode);
                 if (smem > budget) continue;
                 const int cap = resident_capacity_ct(g, cs, threads, size_t(smem));
                 if (std::getenv("NEST_DEBUG"))
-                    std::fprintf(stderr, "nest: resident sweep cluster %d jsplit %d threads %d smem %lld: %d clusters at once\n",
-                                 cs, js, threads, (long long)smem, cap);
+                    std::fprintf(stderr,
+                                 "nest: resident sweep words %d cluster %d jsplit %d threads %d smem %lld: %d clusters at once\n",
+                                 mode, cs, js, threads, (long long)smem, cap);
                 if (cap <= 0) continue;
                 const int waves = (n + cap - 1) / cap;
                 const int serial = (nown_c + ngrp - 1) / ngrp;
+                const double ideal = g.Nmax >= 64 ? 512.0 : g.Nmax > 32 ? 8.0 * g.Nmax : 256.0;
                 const double score = 1.0 / (double(waves) * serial * ngrp * (1.0 + (16 - cs) / 64.0) *
-                                            (1.0 + std::fabs(std::log2(gsize / 256.0)) / 8));
-                if (score > best) {
-                    best = score;
-                    pick = {cs, js, 0, threads, 1, waves};
-                    pick_ctas = int64_t(cap) * cs;
+                                            (1.0 + std::fabs(std::log2(gsize / ideal)) / 8));
+                if (score > r.best) {
+                    r.best = score;
+                    r.shape = {cs, js, 0, threads, 1, waves};
+                    r.ctas = int64_t(cap) * cs;
                 }
                 if (jsplit_opt) break;
             }
             if (cluster_opt) break;
         }
-        // resident when every cluster of the pass is resident at once, or when one wave
-        // of clusters holds at least 1.5 CTAs per SM (measured: 64 16-CTA clusters of
-        // 60 KB in 4 waves beat the streaming variant 2.7x); with larger rows (one CTA
-        // per SM, many waves) the streaming variant, whose CTAs need no co-scheduling,
-        // keeps the GPU fuller
-        if (best > 0 && (variant == 1 || pick.resident_waves == 1 || 2 * pick_ctas >= 3 * int64_t(sms))) {
-            out = pick;
+        return r;
+    };
+    // resident when every cluster of the pass is resident at once, or when one wave
+    // of clusters holds at least one CTA per SM (measured on GB300, 16-CTA clusters:
+    // 64 clusters of 60 KB in 4 waves beat the streaming variant 2.7x, 16 clusters of
+    // 94 KB in 2 waves 3.4x, 256 clusters in 19 waves 1.45x); with fewer CTAs per SM
+    // the streaming variant, whose CTAs need no co-scheduling, keeps the GPU fuller
+    auto accept = [&](const Pick &r) {
+        return r.best > 0 && (variant == 1 || r.shape.resident_waves == 1 || r.ctas >= int64_t(sms));
+    };
+    out.split = 0;
+    out.wide = {};
+    if (variant != 2 && g.Cmax <= 4) {
+        const Pick both = search(0);
+        // rows of 32-bit words take about half the shared memory: when a launch sized
+        // for them alone needs fewer waves, it takes those instances and a second launch
+        // (resident if its shape fits, else streaming) takes the instances on 64-bit words
+        if (!(accept(both) && both.shape.resident_waves == 1)) {
+            const Pick narrow = search(1);
+            if (accept(narrow) && (!accept(both) || narrow.shape.resident_waves < both.shape.resident_waves)) {
+                const Pick wide = search(2);
+                SweepShape ws = {};
+                bool ok = wide.best > 0;
+                if (ok) {
+                    ws = wide.shape;
+                } else if (variant != 1) {
+                    ok = stream_shape(g, n, cluster_opt, jsplit_opt, sms, budget, ws) == NEST_OK;
+                }
+                if (ok) {
+                    const SweepShape &ns = narrow.shape;
+                    out = {ns.cluster, ns.jsplit, ns.jc, ns.threads, ns.resident, ns.resident_waves, 1, ws};
+                    if (std::getenv("NEST_DEBUG"))
+                        std::fprintf(stderr,
+                                     "nest: sweep split: resident 32-bit cluster %d jsplit %d threads %d; 64-bit %s "
+                                     "cluster %d jsplit %d threads %d\n",
+                                     ns.cluster, ns.jsplit, ns.threads, ws.resident ? "resident" : "streaming",
+                                     ws.cluster, ws.jsplit, ws.threads);
+                    return NEST_OK;
+                }
+            }
+        }
+        if (accept(both)) {
+            const SweepShape &p = both.shape;
+            out = {p.cluster, p.jsplit, p.jc, p.threads, p.resident, p.resident_waves, 0, {}};
             if (std::getenv("NEST_DEBUG"))
-                std::fprintf(stderr, "nest: sweep resident, cluster %d jsplit %d threads %d\n", pick.cluster,
-                             pick.jsplit, pick.threads);
+                std::fprintf(stderr, "nest: sweep resident, cluster %d jsplit %d threads %d\n", p.cluster, p.jsplit,
+                             p.threads);
             return NEST_OK;
         }
         if (variant == 1) return NEST_E_LIMITS;
     }
-    // streaming: one thread per (slice, device count) holding every candidate
-    int jsplit = jsplit_opt;
-    if (jsplit == 0) {
-        jsplit = 1;
-        while (jsplit < 8 && NTd * jsplit * 2 <= kMaxThreads) jsplit *= 2;
-    }
-    if (NTd * jsplit > kMaxThreads) return NEST_E_INVALID;
-    int cluster = cluster_opt;
-    if (cluster == 0) {
-        cluster = 1;
-        while (cluster < 8 && cluster * 2 <= g.Pcap && int64_t(n) * cluster * 2 <= sms) cluster *= 2;
-    }
-    const int threads = NTd * jsplit;
-    int jc = g.Nmax > 1 ? g.Nmax - 1 : 1;
-    while (jc > 1 && sweep_smem_bytes(g, jc, jsplit, threads) > budget) jc--;
-    if (sweep_smem_bytes(g, jc, jsplit, threads) > budget) return NEST_E_LIMITS;
-    out = {cluster, jsplit, jc, threads, 0, 1};
+    SweepShape sh;
+    if (int rc = stream_shape(g, n, cluster_opt, jsplit_opt, sms, budget, sh)) return rc;
+    out = {sh.cluster, sh.jsplit, sh.jc, sh.threads, 0, 1, 0, {}};
     return NEST_OK;
 }
 

@@ -26,7 +26,7 @@ ERRORS = {NEST_E_INVALID: "invalid argument", NEST_E_LIMITS: "batch dimensions b
 # Every function declared in include/nest.h.
 EXPORTS = ("nest_record_layout", "nest_plan_bytes", "nest_workspace_size", "nest_workspace_size_costs",
            "nest_workspace_layout", "nest_solve", "nest_workspace_size_host", "nest_solve_host",
-           "nest_select_best", "nest_solve_static")
+           "nest_select_best", "nest_solve_static", "nest_describe_launch")
 KEEP_COSTS = 1   # NEST_KEEP_COSTS
 STATIC_SCRATCH_BYTES = 64 << 20   # NEST_STATIC_SCRATCH_BYTES
 
@@ -55,6 +55,12 @@ class Options(C.Structure):
     _fields_ = [("chunk", C.c_int32), ("sweep_cluster", C.c_int32), ("sweep_jsplit", C.c_int32),
                 ("sweep_variant", C.c_int32), ("spin_limit", C.c_int64), ("events", C.c_void_p),
                 ("flags", C.c_uint32), ("reserved", C.c_int32)]
+
+
+class LaunchDesc(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("chunks", "kernels_per_chunk", "sweep_variant", "sweep_cluster",
+                                         "sweep_jsplit", "sweep_threads", "sweep_split", "wide_variant",
+                                         "wide_cluster", "wide_jsplit", "wide_threads", "reserved")]
 
 
 HEADER_DT = np.dtype([("L", "<i4"), ("D", "<i4"), ("unit", "<i4"), ("T", "<i4"), ("C", "<i4"),
@@ -92,6 +98,7 @@ def lib():
                                       C.c_void_p, P(Options)]
         L.nest_solve_static.argtypes = [P(Dims), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, P(Options)]
         L.nest_select_best.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+        L.nest_describe_launch.argtypes = [P(Dims), P(Options), P(LaunchDesc)]
         _lib = L
     return _lib
 
@@ -157,6 +164,15 @@ def workspace_layout(dims: Dims, chunk: int = 0) -> WsLayout:
     if rc:
         raise NestError(rc, "nest_workspace_layout")
     return out
+
+
+def describe_launch(dims: Dims, opt: Options | None = None) -> dict:
+    """nest_describe_launch: the passes, kernels per pass and DP-sweep shape of a solve."""
+    out = LaunchDesc()
+    rc = lib().nest_describe_launch(C.byref(dims), C.byref(opt) if opt is not None else None, C.byref(out))
+    if rc:
+        raise NestError(rc, "nest_describe_launch")
+    return {n: int(getattr(out, n)) for n, _ in LaunchDesc._fields_ if n != "reserved"}
 
 
 def pack_records(instances: Sequence, dims: Dims, out: np.ndarray | None = None) -> np.ndarray:

@@ -62,13 +62,24 @@ def test_random_dags_match_the_oracle(part):
 @pytest.mark.parametrize("cluster,jsplit,variant", [(0, 0, 1), (0, 0, 2), (2, 2, 1), (4, 1, 2)])
 def test_random_dags_every_table(cluster, jsplit, variant):
     insts = tiny_graphs(21000, 24, Lmax=6, Dmax=8)
+    for x in insts:
+        x.Pmax = min(x.Pmax, 4)
+        x.M = max(x.M, x.Pmax)
     s, res = G.run(insts, cluster=cluster, jsplit=jsplit, variant=variant, Pcap=4)
     for b in range(len(insts)):
         o = G.check_graph_tables(s, b, insts[b])
         assert G.same_graph_result(res[b], o), b
 
 
-TWO_TOWER_CONFIGS = [(0, 0, 0), (16, 8, 1), (16, 4, 1), (8, 4, 1), (16, 1, 1), (8, 2, 2), (4, 4, 2), (0, 0, 2)]
+TWO_TOWER_CONFIGS = [(0, 0, 0), (16, 8, 1), (16, 4, 1), (16, 2, 1), (16, 1, 1), (8, 2, 2), (4, 4, 2), (0, 0, 2)]
+
+
+def test_two_tower_resident_needs_one_position_per_cta():
+    # 97 states: the rows of two positions per CTA do not fit in shared memory
+    insts = [synth.two_tower_instance(b) for b in range(2)]
+    with pytest.raises(nest.NestError) as e:
+        G.run(insts, cluster=8, jsplit=4, variant=1)
+    assert e.value.rc == nest.NEST_E_LIMITS
 
 
 @pytest.mark.parametrize("cluster,jsplit,variant", TWO_TOWER_CONFIGS)
@@ -132,3 +143,20 @@ def test_bad_graphs_are_flagged_per_instance():
     # with room for its 255 non-empty up-sets the independent-layer graph solves
     s, res = G.run([wide], Vmax=255, keep_costs=False)
     assert G.same_graph_result(res[0], G.solve_graph(wide))
+
+
+def test_split_sweep_with_both_word_widths():
+    # 16 two-tower instances need two waves when shared memory is sized for 64-bit
+    # rows; the sweep then runs as a 32-bit launch and a 64-bit launch, each taking
+    # its own instances
+    insts = [synth.two_tower_instance(b) for b in range(16)]
+    for b in (2, 5, 11):
+        insts[b] = G.scaled(insts[b], 64)
+    plan = nest.describe_launch(nest.make_dims(insts))
+    assert plan["sweep_split"] == 1 and plan["kernels_per_chunk"] == 5, plan
+    s, res = G.run(insts)
+    oracle = G.oracle_many(insts, fn=G.solve_graph)
+    for b in range(len(insts)):
+        assert G.same_graph_result(res[b], oracle[b]), b
+    for b in (2, 3):
+        G.check_graph_tables(s, b, insts[b])

@@ -300,3 +300,18 @@ def test_bounded_wait_gives_up_and_context_survives(variant):
     _, res2 = G.run(insts)
     oracle = G.oracle_many(insts)
     assert all(G.same_result(a, b) for a, b in zip(res2, oracle))
+
+
+def test_torus_split_sweep_mixed_widths():
+    # three candidate tiers: the resident rows of both widths need two waves for 16
+    # instances, so the sweep is split by word width
+    insts = [synth.torus_instance(b) for b in range(16)]
+    for b in (0, 9):
+        insts[b] = G.scaled(insts[b], 64)
+    plan = nest.describe_launch(nest.make_dims(insts))
+    s, res = G.run(insts)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), (b, plan)
+    for b in (0, 1):
+        check_tables(s, b, insts[b])
