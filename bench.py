@@ -59,29 +59,72 @@ def states(x) -> list:
     return sorted(out, key=lambda D: (-bin(D).count("1"), D))
 
 
+def _pairs(x):
+    """(E, per-state layer counts, nested[i] = bool array over states j, moe_in[i] =
+    bool array: the stage from state i to state j holds a MoE layer)."""
+    if getattr(x, "succ", None) is None:
+        L = x.L
+        pm = np.concatenate([[0], np.cumsum(np.asarray(x.moe, dtype=np.int64))])
+        sizes = [L - i for i in range(L + 1)]
+        nested = [np.arange(L + 1) > i for i in range(L + 1)]
+        moe_in = [(pm - pm[i]) > 0 for i in range(L + 1)]
+        return L, sizes, nested, moe_in
+    st = np.asarray(states(x), dtype=np.uint64)
+    mm = np.uint64(sum(1 << l for l in range(x.L) if int(x.moe[l])))
+    sizes = [bin(int(v)).count("1") for v in st]
+    idx = np.arange(len(st))
+    nested = [(idx > i) & ((st & ~st[i]) == 0) for i in range(len(st))]
+    moe_in = [((st[i] & ~st) & mm) != 0 for i in range(len(st))]
+    return len(st) - 1, sizes, nested, moe_in
+
+
+def _count(x, with_strategies: bool) -> int:
+    Du, P, C, u = x.D // x.unit, x.Pmax, len(x.cand), x.unit
+    G = [int(x.tierG[c]) for c in x.cand]
+    K = Du.bit_length()
+    E, sizes, nested, moe_in = _pairs(x)
+    # strategies valid for a stage of width unit * 2^m, without / with a MoE layer
+    nvalid = np.ones((K, 2), dtype=np.int64)
+    if with_strategies:
+        for m in range(K):
+            k = u << m
+            for hm in (0, 1):
+                nvalid[m, hm] = sum(1 for t, cp, e, _, _ in x.strat
+                                    if not (k % (int(t) * int(cp)) or (k // (int(t) * int(cp))) % int(e)
+                                            or (int(e) > 1 and not hm)))
+    tot = 0
+    for i in range(E):
+        Pi = min(P, sizes[i])
+        inner_j = nested[i].copy()
+        inner_j[E] = False
+        for m in range(K):
+            k = u << m
+            w = nvalid[m][moe_in[i].astype(np.int64)]
+            last = int(w[E])
+            inner = int(w[inner_j].sum())
+            nd = Du - (1 << m) + 1
+            ncp = sum(1 for g in G if 2 * k <= g)
+            for c in range(1 if i == 0 else C):
+                if i > 0 and 2 * k > G[c]:
+                    continue
+                tot += nd * (last + (Pi - 1) * inner * ncp)
+    return tot
+
+
 def relaxations(x) -> int:
     """Min-max transitions (j, m, c') the recurrence evaluates for one instance:
     every cell (i, d, p, c) times its cut points j (states inside state i), widths
     m <= log2 d allowed by the link tier, and next-link candidates c' allowed for
     that width."""
-    Du, P, C, u = x.D // x.unit, x.Pmax, len(x.cand), x.unit
-    G = [int(x.tierG[c]) for c in x.cand]
-    K = Du.bit_length()
-    st = states(x)
-    E = len(st) - 1
-    tot = 0
-    for i in range(E):
-        Pi = min(P, bin(st[i]).count("1"))
-        inner = sum(1 for j in range(i + 1, E) if st[j] & ~st[i] == 0)   # cut points before the end
-        for c in range(1 if i == 0 else C):
-            for m in range(K):
-                k = u << m
-                if i > 0 and 2 * k > G[c]:
-                    continue
-                nd = Du - (1 << m) + 1
-                ncp = sum(1 for g in G if 2 * k <= g)
-                tot += nd * (1 + (Pi - 1) * inner * ncp)
-    return tot
+    return _count(x, False)
+
+
+def relaxations_with_strategies(x) -> int:
+    """The same transitions counted with the strategy axis, (j, m, s, c'): every
+    relaxation times the strategies valid for its stage and width (t cp divides the
+    width, e divides the data-parallel degree, e > 1 only over a MoE layer) - the
+    work of the recurrence before the strategy minimum is hoisted out of it."""
+    return _count(x, True)
 
 
 def state_pairs(x) -> int:
@@ -331,6 +374,7 @@ def main():
         B = len(instances)
         workload += "-joint-mbs" + "-".join(str(b) for b in synth.MICROBATCH_SIZES)
     relax_total = sum(relaxations(x) for x in instances)
+    relax_s_total = sum(relaxations_with_strategies(x) for x in instances)
 
     if args.impl == "reference":
         run_reference(args, workload, instances, relax_total)
@@ -495,6 +539,14 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": stored_traffic(dom, workload),
                 "kernel": dom, "peak_source": f"{peaks['source']} hbm_gbs"}
+    # the stage-loads kernel (cost build + strategy reduction) against HBM: the bytes of
+    # the per-position loads table it must write, over its time in the breakdown pass
+    loads_bytes_all = sum(8 * x.Pmax * state_pairs(x) * (x.D // x.unit).bit_length() for x in instances)
+    roof_loads = {"bound": "hbm", "kernel": "stage_loads", "achieved": loads_bytes_all / (kms["stage_loads"] * 1e-3) / 1e9,
+                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                  "frac": loads_bytes_all / (kms["stage_loads"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "traffic": stored_traffic("stage_loads", workload),
+                  "note": "integer-ALU bound: about 60 exact integer operations per (stage, width, strategy) word"}
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(instances, relax_total, args.cpu_seconds)
@@ -507,10 +559,13 @@ def main():
                            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
                            "parallelism": f"replicas{ws}", "launch": plan},
                 "solves_per_s": solves,
+                "relaxations_jmsc_per_s": job_relax / relax_total * relax_s_total / (ms_per_step * 1e-3),
+                "relaxations_jmsc_note": "the (j, m, s, c') count of the recurrence with the strategy axis, "
+                                         "per second of the whole step",
                 **({"problems_per_s": solves / group, "variants_per_problem": group} if group > 1 else {}),
                 "kernel_ms_per_step": kms,
                 "kernel_ms_note": "separate pass, events at every kernel boundary (no launch overlap)",
-                "roofline": roof, "cpu_baseline": cpu,
+                "roofline": roof, "roofline_stage_loads": roof_loads, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(records.nbytes),
                         "d2h_bytes_per_step": int(8 * B + B * nest.plan_bytes(dims) + (4 * (B // group) if group > 1 else 0)),
                         "ms_per_step": e2e_total / e2e_steps},

@@ -1,0 +1,60 @@
+"""The benchmark's work counts against a direct loop over the recurrence's transitions.
+
+A relaxation is one (j, m, c') min-max transition of Eq. 3 (Nest §4) for one DP cell
+(i, d, p, c); with the strategy axis it is one (j, m, s, c') transition.  The bench
+counts them with vectorised sums; here every cell and transition is enumerated.
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+from memory_aware_device_gb300 import synth  # noqa: E402
+
+
+def direct(x, with_strategies):
+    Du, P, C, u = x.D // x.unit, x.Pmax, len(x.cand), x.unit
+    G = [int(x.tierG[c]) for c in x.cand]
+    st = bench.states(x)
+    E = len(st) - 1
+    moe = sum(1 << l for l in range(x.L) if int(x.moe[l]))
+    n = 0
+    for i in range(E):
+        for d in range(1, Du + 1):
+            for p in range(1, min(P, bin(st[i]).count("1")) + 1):
+                for c in range(1 if i == 0 else C):
+                    for j in range(i + 1, E + 1):
+                        if st[j] & ~st[i] or (j == E) != (p == 1):
+                            continue
+                        for m in range(Du.bit_length()):
+                            k = u << m
+                            if (1 << m) > d or (i > 0 and 2 * k > G[c]):
+                                continue
+                            ns = 1
+                            if with_strategies:
+                                hm = bool((st[i] & ~st[j]) & moe)
+                                ns = sum(1 for t, cp, e, _, _ in x.strat
+                                         if not (k % (int(t) * int(cp)) or (k // (int(t) * int(cp))) % int(e)
+                                                 or (int(e) > 1 and not hm)))
+                            ncp = 1 if j == E else sum(1 for g in G if 2 * k <= g)
+                            n += ns * ncp
+    return n
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_counts_match_a_direct_loop(seed):
+    x = synth.random_tiny(seed + 500, Lmax=6, Dmax=8)
+    if seed % 2:
+        x.succ = synth.random_dag(seed, x.L, (0.2, 0.5)[seed % 4 // 2])
+    assert bench.relaxations(x) == direct(x, False)
+    assert bench.relaxations_with_strategies(x) == direct(x, True)
+
+
+def test_workload_counts():
+    assert sum(bench.relaxations(x) for x in synth.config_batch(2)) == 95544528
+    x = synth.two_tower_instance(0)
+    assert bench.relaxations(x) == 682205648 // 16
+    assert bench.state_pairs(x) == 96 * 97 // 2
