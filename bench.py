@@ -142,9 +142,12 @@ def oracle_solve(x):
 
 
 def src_hash(kernel: str) -> str:
-    p = os.path.join(ROOT, "memory_aware_device_gb300", "csrc", KERNEL_SRC[kernel])
-    h = hashlib.sha256(open(p, "rb").read())
-    h.update(open(os.path.join(ROOT, "memory_aware_device_gb300", "csrc", "nest_internal.cuh"), "rb").read())
+    """Hash of a kernel's source file and every header the kernels share."""
+    d = os.path.join(ROOT, "memory_aware_device_gb300", "csrc")
+    h = hashlib.sha256(open(os.path.join(d, KERNEL_SRC[kernel]), "rb").read())
+    for f in sorted(os.listdir(d)):
+        if f.endswith(".cuh"):
+            h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
