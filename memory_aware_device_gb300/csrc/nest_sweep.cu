@@ -320,11 +320,14 @@ __device__ __forceinline__ bool narrow_words(const PrepHdr *ph) {
 //  - A[buf][slot][j][c][c'][m] = load*(i, j, m, p) + X[i][c] + X[j][c'] when both
 //    links admit the width, else `far`; A[j] holds an odd number of values (banks).
 //  - staged dp rows [2][slot][Cmax][Dpad] (int64 values, uint32 arguments).
+//  - graph instances: the layer mask of every state, and per step parity the list of
+//    cut points j >= i + 2 whose state lies inside state i (8-bit state indices), its
+//    length and whether state i + 1 lies inside state i.
 // The H and A regions are sized for whichever word width needs more, or, for a launch
 // that takes only the instances of one word width (`mode` 1: 32-bit, 2: 64-bit), for
 // that width alone.
 struct ResPlan {
-    int rowbar, X, H, A, sdv, sda, total;  // word offsets; total = words
+    int rowbar, X, H, A, sdv, sda, um, jl, total;  // word offsets; total = words
     int Hpad, Hcol, Hrow, Hslot;           // H strides in values of the chosen width
     int Aj, Aslot, Abuf;                   // A strides in values
     int Srow;                              // values per staged dp row: Cmax * Dpad
@@ -371,6 +374,10 @@ __host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, 
     off = up(off + 2 * nown * s.Srow);
     s.sda = off;
     off = up(off + nown * s.Srow);
+    s.um = off;
+    off = up(off + g.Nmax + 1);
+    s.jl = off;   // [2] x (count, i + 1 inside i, pad, pad) as int32, then [2][Nmax] bytes
+    off = up(off + 2 + (2 * g.Nmax + 7) / 8);
     s.total = off;
     return s;
 }
@@ -502,7 +509,7 @@ __device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, in
 //    (for the backtrack) by bulk copies.
 // The footprint is kept small so that the clusters of a whole batch are resident at
 // once.
-template <int CT, int KT, typename V>
+template <int CT, int KT, typename V, bool kGraph>
 __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
                                               volatile int &abort_flag) {
     constexpr int NA = CT <= 2 ? CT : 1;   // running bests per cell
@@ -516,6 +523,10 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     V *A = reinterpret_cast<V *>(sm + sp.A);
     int64_t *sdv = sm + sp.sdv;
     uint32_t *sda = reinterpret_cast<uint32_t *>(sm + sp.sda);
+    uint64_t *um_s = reinterpret_cast<uint64_t *>(sm + sp.um);               // [Nmax + 1]
+    int *jl_hdr = reinterpret_cast<int *>(sm + sp.jl);                       // [2][2]
+    uint8_t *jl_list = reinterpret_cast<uint8_t *>(sm + sp.jl + 2);          // [2][Nmax]
+    constexpr bool graph = kGraph;   // states are the up-sets of a layer DAG
     constexpr V cap = Word<V>::cap, far = Word<V>::far;
 
     // thread = (slot group, device count d, slice js), slices in adjacent lanes; the
@@ -556,6 +567,11 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
 
     const int64_t *Xg = reinterpret_cast<const int64_t *>(reinterpret_cast<const unsigned char *>(ph) + a.pl.X);
     for (int e = tid; e < (L + 1) * g.Cmax; e += blockDim.x) sm[sp.X + e] = Xg[e];
+    if (graph) {
+        const uint64_t *umg =
+            reinterpret_cast<const uint64_t *>(reinterpret_cast<const unsigned char *>(ph) + a.pl.umask);
+        for (int q = tid; q <= L; q += blockDim.x) um_s[q] = umg[q];
+    }
     for (int q = tid; q < nown * g.Nmax; q += blockDim.x) mbar_init(&rowbar[q], 1);
     // the padding in front of every row: cap (never written again)
     for (int e = tid; e < nown * g.Nmax * g.Cmax * sp.Hpad; e += blockDim.x) {
@@ -571,6 +587,26 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         const int p = rank + 1 + k * cs;
         if (p >= 2 && p <= s.P && j >= 1 && j < L) mbar_expect_tx(&rowbar[q], row_bytes);
     }
+
+    // graph instances: the cut points j >= i + 2 of step i whose state lies inside state
+    // i, compacted by one warp (ballots), and whether state i + 1 lies inside it; the
+    // other pairs of states are no transition (their A entries are far)
+    auto build_list = [&](int ii) {
+        const uint64_t Di = um_s[ii];
+        uint8_t *lst = jl_list + (ii & 1) * g.Nmax;
+        int cnt = 0;
+        for (int base = ii + 2; base < L; base += 32) {
+            const int j = base + lane;
+            const bool ok = j < L && (um_s[j] & ~Di) == 0;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+            if (ok) lst[cnt + __popc(bal & ((1u << lane) - 1u))] = uint8_t(j);
+            cnt += __popc(bal);
+        }
+        if (lane == 0) {
+            jl_hdr[(ii & 1) * 2] = cnt;
+            jl_hdr[(ii & 1) * 2 + 1] = ii + 1 < L && (um_s[ii + 1] & ~Di) == 0;
+        }
+    };
 
     // A[j][c][c'][m] for a stage starting at layer i (the rows of step i): the load
     // plus both link costs when the incoming link of cell c (none for the first stage,
@@ -598,6 +634,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         }
     };
     a_rows(L - 1, tid);
+    if (graph && tid < 32) build_list(L - 1);
     // the next position's row and barrier base in its owner's shared memory, for this
     // thread's first slot (the common case has one slot per CTA); rows of step i sit
     // i * Hrow values and i barriers further on
@@ -616,8 +653,11 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         const bool a_mine = a_have && i > 0 && a_r <= L - i;
         const uint64_t pre = a_mine ? a_src[ro * g.Kpad] : kInf;
         // cut points j >= i + 2 dealt round-robin over the slices; j = i + 1 (whose row
-        // arrives last) is the final item of the last slice
-        const int n = L - i - 2 > 0 ? L - i - 2 : 0;
+        // arrives last) is the final item of the last slice.  A graph instance takes only
+        // the states inside state i (its list for this step)
+        const int n = graph ? jl_hdr[(i & 1) * 2] : (L - i - 2 > 0 ? L - i - 2 : 0);
+        const bool take1 = !graph || jl_hdr[(i & 1) * 2 + 1] != 0;
+        const uint8_t *jlst = jl_list + (i & 1) * g.Nmax;
         const int cnt = n > js ? (n - js + jsplit - 1) >> lgs : 0;
         const int items = cnt + (js == jlast ? 1 : 0);
 
@@ -657,12 +697,15 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
                         if (!abort_flag && !mbar_wait(&rowbar[k * g.Nmax + j], 0, spin)) abort_flag = 1;
                 for (int t = 0; t < items; t++) {
                     const bool last = t == cnt;
-                    const int j = last ? i + 1 : i + 2 + js + (t << lgs);
+                    const int q = js + (t << lgs);
+                    const int j = last ? i + 1 : graph ? int(jlst[q]) : i + 2 + q;
                     if (last) {
-                        // row i + 1 is the one the neighbour pushed last (bounded wait); it
+                        // row i + 1 is the one the neighbour pushed last (bounded wait; later
+                        // steps read it too, so the wait is kept when it is no cut point); it
                         // is the smallest cut point and wins ties, so compare against bv + 1
                         // until it has improved a running best
                         if (!abort_flag && !mbar_wait(&rowbar[k * g.Nmax + i + 1], 0, spin)) abort_flag = 1;
+                        if (!take1) break;
 #pragma unroll
                         for (int c = 0; c < CT; c++)
 #pragma unroll
@@ -733,6 +776,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
         // this step's pushes (which the neighbour is waiting for)
         if (a_mine) a_entry(a_dst + ((i - 1) & 1) * sp.Abuf + i * sp.Aj, i - 1, i + a_r, a_m, pre);
         if (i > 0 && a_total > int(blockDim.x)) a_rows(i - 1, tid + blockDim.x);
+        if (graph && i > 0 && tid < 32) build_list(i - 1);
         // the staged rows of step i go to global memory by bulk copies; those of step
         // i + 1 have been read by now (their buffer is written again at step i - 1)
         fence_proxy_async();
@@ -762,6 +806,25 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     if (tid == 0 && abort_flag) ph->status = NEST_TIMED_OUT;
 }
 
+// Each (word width, graph) variant of the body: a called function for up to two
+// candidates, so that every variant gets its own register allocation (measured: 4 %
+// faster on the dense workload than all four inlined into the kernel), inlined for four
+// (called, those spill).
+template <int CT, int KT, typename V, bool kGraph>
+__device__ __noinline__ void resident_body_call(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
+                                                volatile int &abort_flag) {
+    resident_body<CT, KT, V, kGraph>(a, ph, b, rank, sm, abort_flag);
+}
+
+template <int CT, int KT, typename V, bool kGraph>
+__device__ __forceinline__ void run_body(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
+                                         volatile int &abort_flag) {
+    if constexpr (CT <= 2)
+        resident_body_call<CT, KT, V, kGraph>(a, ph, b, rank, sm, abort_flag);
+    else
+        resident_body<CT, KT, V, kGraph>(a, ph, b, rank, sm, abort_flag);
+}
+
 template <int CT, int KT>
 __global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs a) {
     extern __shared__ __align__(128) int64_t sm[];
@@ -776,10 +839,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs
     // a launch for one width leaves the other width's instances to its companion launch
     const bool narrow = narrow_words(ph);
     if ((a.word_mode == 1 && !narrow) || (a.word_mode == 2 && narrow)) return;
-    if (narrow)
-        resident_body<CT, KT, uint32_t>(a, ph, b, rank, sm, abort_flag);
-    else
-        resident_body<CT, KT, int64_t>(a, ph, b, rank, sm, abort_flag);
+    if (narrow) {
+        if (ph->graph)
+            run_body<CT, KT, uint32_t, true>(a, ph, b, rank, sm, abort_flag);
+        else
+            run_body<CT, KT, uint32_t, false>(a, ph, b, rank, sm, abort_flag);
+    } else {
+        if (ph->graph)
+            run_body<CT, KT, int64_t, true>(a, ph, b, rank, sm, abort_flag);
+        else
+            run_body<CT, KT, int64_t, false>(a, ph, b, rank, sm, abort_flag);
+    }
 }
 
 // ---------------------------------------------------------------------------------
