@@ -160,3 +160,19 @@ def test_split_sweep_with_both_word_widths():
         assert G.same_graph_result(res[b], oracle[b]), b
     for b in (2, 3):
         G.check_graph_tables(s, b, insts[b])
+
+
+def test_widest_graph_matches_chain_mode():
+    # 63 layers as a graph (bit 62 of the masks in use) against the same chain
+    base = synth.config_instance(2, 5)
+    base.L, base.Pmax = 63, 8
+    for f in ("fl", "pd", "pe", "ao", "aw", "a2a", "moe"):
+        setattr(base, f, np.resize(getattr(base, f), 63))
+    import copy
+    g = copy.deepcopy(base)
+    g.succ = synth.chain_succ(63)
+    s, res = G.run([base, g])
+    o = O.solve(base, want_dp=True)
+    assert G.same_result(res[0], o) and G.same_result(res[1], o)
+    assert res[1]["layers"][0] & (1 << 62) or res[1]["layers"][-1] & (1 << 62)
+    np.testing.assert_array_equal(G.dp_keys(s, 1, g), G.oracle_dp_keys(base, o["dp"]))

@@ -452,3 +452,20 @@ def test_pair_tables_cover_every_pair_of_states(seed):
     c2, l2 = O.lattice_pair_tables(y, synth.chain_succ(y.L))
     np.testing.assert_array_equal(c2, O.cost_tensor(y))
     np.testing.assert_array_equal(l2, O.loads(y))
+
+
+def test_widest_graph_chain_of_63_layers():
+    # 63 layers is the widest graph (64-bit masks, the top bit stays clear)
+    x = synth.config_instance(2, 5)
+    x.L = 63
+    for f in ("fl", "pd", "pe", "ao", "aw", "a2a", "moe"):
+        setattr(x, f, np.resize(getattr(x, f), 63))
+    x.Pmax = 8
+    st = O.lattice_states(x, synth.chain_succ(63))
+    assert len(st) == 64 and int(st[0]) == (1 << 63) - 1
+    a, b = O.solve(x, want_dp=True), O.solve_lattice(x, synth.chain_succ(63), want_dp=True)
+    assert a["status"] == 0 and a["plan"] == b["plan"] and np.array_equal(a["dp"], b["dp"])
+    x.L = 64
+    for f in ("fl", "pd", "pe", "ao", "aw", "a2a", "moe"):
+        setattr(x, f, np.resize(getattr(x, f), 64))
+    assert O.solve_lattice(x, synth.chain_succ(64))["status"] == 2
