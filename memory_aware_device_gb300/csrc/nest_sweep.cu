@@ -407,83 +407,79 @@ __device__ __forceinline__ void relax_one(const V *Aj, const V *Hj, int Hcol, in
     }
 }
 
-// The same for exactly MT widths m < MT (every lane's excluded widths read far or
-// cap): all dp values of a c' are loaded first, then each cell takes the minimum
-// over its MT candidates with a tree that keeps the smaller m on ties, and merges it
-// into its running best.  Loads overlap and the serial depth is log2(MT).
+// The same for one next-link candidate c2 and exactly MT widths m < MT (every lane's
+// excluded widths read far or cap): the dp values of c2 are loaded first, then each
+// cell takes the minimum over its MT candidates with a tree that keeps the smaller m
+// on ties, and merges it into its running best for c2.  Loads overlap and the serial
+// depth is log2(MT).
 template <int CT, int KT, int NA, int MT, typename V>
-__device__ __forceinline__ void relax_cut_t(const V *Aj, const V *Hj, int Hcol, int d, int C, uint32_t jarg,
-                                            V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+__device__ __forceinline__ void relax_c2_t(const V *Aj, const V *Hj, int Hcol, int d, int c2, uint32_t jarg,
+                                           V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
     constexpr bool kPad = sizeof(V) == 4;   // rows padded with cap below x = 0
+    V nv[MT];
 #pragma unroll
-    for (int c2 = 0; c2 < CT; c2++) {
-        if (c2 >= C) break;
-        V nv[MT];
+    for (int m = 0; m < MT; m++) {
+        const int x = kPad ? d - (1 << m) : (d - (1 << m) > 0 ? d - (1 << m) : 0);
+        nv[m] = Hj[c2 * Hcol + x];
+    }
+#pragma unroll
+    for (int c = 0; c < CT; c++) {
+        V v[MT];
+        int id[MT];
 #pragma unroll
         for (int m = 0; m < MT; m++) {
-            const int x = kPad ? d - (1 << m) : (d - (1 << m) > 0 ? d - (1 << m) : 0);
-            nv[m] = Hj[c2 * Hcol + x];
+            const V av = Aj[(c * CT + c2) * KT + m];
+            v[m] = av > nv[m] ? av : nv[m];
+            id[m] = m;
         }
 #pragma unroll
-        for (int c = 0; c < CT; c++) {
-            V v[MT];
-            int id[MT];
+        for (int w = 1; w < MT; w <<= 1)
 #pragma unroll
-            for (int m = 0; m < MT; m++) {
-                const V av = Aj[(c * CT + c2) * KT + m];
-                v[m] = av > nv[m] ? av : nv[m];
-                id[m] = m;
+            for (int q = 0; q + w < MT; q += 2 * w) {
+                const bool r = v[q + w] < v[q];   // the left holds the smaller widths
+                v[q] = r ? v[q + w] : v[q];
+                id[q] = r ? id[q + w] : id[q];
             }
-#pragma unroll
-            for (int w = 1; w < MT; w <<= 1)
-#pragma unroll
-                for (int q = 0; q + w < MT; q += 2 * w) {
-                    const bool r = v[q + w] < v[q];   // the left holds the smaller widths
-                    v[q] = r ? v[q + w] : v[q];
-                    id[q] = r ? id[q + w] : id[q];
-                }
-            const bool take = v[0] < bv[c][c2];
-            bv[c][c2] = take ? v[0] : bv[c][c2];
-            bi[c][c2] = take ? jarg | (uint32_t(id[0]) << 4) | uint32_t(c2) : bi[c][c2];
-        }
+        const bool take = v[0] < bv[c][c2];
+        bv[c][c2] = take ? v[0] : bv[c][c2];
+        bi[c][c2] = take ? jarg | (uint32_t(id[0]) << 4) | uint32_t(c2) : bi[c][c2];
     }
 }
 
+// Relaxation of one cut point: for every next-link candidate c2 < C, the widths up to
+// mwc[c2], the warp's widest width within c2's link tier (wider ones would read far
+// in every A entry of c2, which never improves a running best).  With NA = CT each c2
+// dispatches once on its (warp-uniform) width count to a fully unrolled body; with
+// NA = 1 one running best per cell is visited in the canonical (m, c') order.
 template <int CT, int KT, int NA, typename V>
-__device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, int d, int C, uint32_t jarg, int mw,
-                                          V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
-    if constexpr (NA > 1) {
-        // exactly mw + 1 widths, unrolled (the warp-uniform mw selects the copy)
-        switch (mw) {
-        case -1: return;
-        case 0: relax_cut_t<CT, KT, NA, 1, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return;
-        case 1: if constexpr (KT >= 2) { relax_cut_t<CT, KT, NA, 2, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
-        case 2: if constexpr (KT >= 3) { relax_cut_t<CT, KT, NA, 3, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
-        case 3: if constexpr (KT >= 4) { relax_cut_t<CT, KT, NA, 4, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
-        case 4: if constexpr (KT >= 5) { relax_cut_t<CT, KT, NA, 5, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
-        case 5: if constexpr (KT >= 6) { relax_cut_t<CT, KT, NA, 6, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
-        case 6: if constexpr (KT >= 7) { relax_cut_t<CT, KT, NA, 7, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
-        case 7: if constexpr (KT >= 8) { relax_cut_t<CT, KT, NA, 8, V>(Aj, Hj, Hcol, d, C, jarg, bv, bi); return; } break;
-        default: break;
-        }
-    }
+__device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, int d, int C, uint32_t jarg,
+                                          const int (&mwc)[CT], V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
     if constexpr (NA > 1) {
 #pragma unroll
         for (int c2 = 0; c2 < CT; c2++) {
             if (c2 >= C) break;
-#pragma unroll
-            for (int m = 0; m < KT; m++) {
-                if (m > mw) break;
-                relax_one<CT, KT, NA, V>(Aj, Hj, Hcol, d, jarg, m, c2, c2, bv, bi);
+            switch (mwc[c2]) {
+            case 0: relax_c2_t<CT, KT, NA, 1, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 1: if constexpr (KT >= 2) relax_c2_t<CT, KT, NA, 2, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 2: if constexpr (KT >= 3) relax_c2_t<CT, KT, NA, 3, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 3: if constexpr (KT >= 4) relax_c2_t<CT, KT, NA, 4, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 4: if constexpr (KT >= 5) relax_c2_t<CT, KT, NA, 5, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 5: if constexpr (KT >= 6) relax_c2_t<CT, KT, NA, 6, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 6: if constexpr (KT >= 7) relax_c2_t<CT, KT, NA, 7, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 7: if constexpr (KT >= 8) relax_c2_t<CT, KT, NA, 8, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            default:
+                // more than 8 widths: one at a time
+                for (int m = 0; m <= mwc[c2] && m < KT; m++) relax_one<CT, KT, NA, V>(Aj, Hj, Hcol, d, jarg, m, c2, c2, bv, bi);
+                break;
             }
         }
     } else {
 #pragma unroll
         for (int m = 0; m < KT; m++) {
-            if (m > mw) break;
 #pragma unroll
             for (int c2 = 0; c2 < CT; c2++) {
                 if (c2 >= C) break;
+                if (m > mwc[c2]) continue;
                 relax_one<CT, KT, NA, V>(Aj, Hj, Hcol, d, jarg, m, c2, 0, bv, bi);
             }
         }
@@ -648,6 +644,9 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     for (int i = L - 1; i >= 0; i--) {
         const int Pi = s.P < L - i ? s.P : L - i;
         const int mw = i > 0 ? mw_n : mw_0;
+        int mwc[CT];   // widest width per next-link candidate (its tier's limit)
+#pragma unroll
+        for (int c2 = 0; c2 < CT; c2++) mwc[c2] = c2 < C ? (mlink[c2] < mw ? mlink[c2] : mw) : -1;
         // the loads of step i - 1, fetched now and stored after the relaxation
         ro -= L - i + 1;   // row_offset(i - 1, L)
         const bool a_mine = a_have && i > 0 && a_r <= L - i;
@@ -711,7 +710,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
 #pragma unroll
                             for (int q = 0; q < NA; q++) bv[c][q] += bv[c][q] < cap ? 1 : 0;
                     }
-                    relax_cut<CT, KT, NA, V>(Ak + j * sp.Aj, Hk + j * sp.Hrow, sp.Hcol, d, C, uint32_t(j) << 8, mw,
+                    relax_cut<CT, KT, NA, V>(Ak + j * sp.Aj, Hk + j * sp.Hrow, sp.Hcol, d, C, uint32_t(j) << 8, mwc,
                                              bv, bi);
                     if (last) {
 #pragma unroll
