@@ -101,7 +101,10 @@ int nest_describe_launch(const nest_dims *dims, const nest_options *opt, nest_la
     if (rc != NEST_OK) return rc;
     std::memset(out, 0, sizeof *out);
     out->chunks = dims->B == 0 ? 0 : (dims->B + chunk - 1) / chunk;
-    out->kernels_per_chunk = cfg.split ? 5 : 4;
+    // prep, stage loads, the sweep (two launches when split), and the backtrack unless
+    // every sweep launch is resident (their clusters write the plans)
+    const bool fuse = cfg.resident && (!cfg.split || cfg.wide.resident);
+    out->kernels_per_chunk = 3 + (cfg.split ? 1 : 0) + (fuse ? 0 : 1);
     out->sweep_variant = cfg.resident ? 1 : 2;
     out->sweep_cluster = cfg.cluster;
     out->sweep_jsplit = cfg.jsplit;
@@ -170,6 +173,7 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
     a.resident = cfg.resident;
     a.spin_limit = opt ? opt->spin_limit : 0;
     a.keep_costs = keep ? 1 : 0;
+    a.fuse_walk = cfg.resident && (!cfg.split || cfg.wide.resident) ? 1 : 0;
     cudaEvent_t *ev = opt ? reinterpret_cast<cudaEvent_t *>(opt->events) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto mark = [&](int chunk_idx, int k) {
@@ -184,7 +188,7 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
         a.plans_out = static_cast<unsigned char *>(plans_out) + int64_t(first) * a.plan_stride;
         if ((rc = mark(ci, 0)) || (rc = launch_prep(a, st)) || (rc = mark(ci, 1)) || (rc = launch_loads(a, st)) ||
             (rc = mark(ci, 2)) || (rc = sweep_pass(a, cfg, st)) || (rc = mark(ci, 3)) ||
-            (rc = launch_backtrack(a, st)) || (rc = mark(ci, 4)))
+            (!a.fuse_walk && (rc = launch_backtrack(a, st))) || (rc = mark(ci, 4)))
             return rc;
     }
     return NEST_OK;

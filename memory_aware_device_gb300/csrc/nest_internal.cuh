@@ -192,6 +192,9 @@ struct PassArgs {
     int32_t keep_costs;            // also write the stage-cost tensor
     int32_t word_mode;             // sweep launch takes: 0 every instance, 1 those on 32-bit
                                    // words only, 2 those on 64-bit words only
+    int32_t fuse_walk;             // resident sweep: rank 0 of each cluster also writes the plan
+                                   // (the final reduction and backtrack), no backtrack launch
+    int32_t pad;
 };
 
 __host__ __device__ inline PrepHdr *prep_hdr(const PassArgs &a, int b) {

@@ -544,7 +544,7 @@ static __device__ __noinline__ void loads_slice(const PassArgs &a, int b, const 
 // The final batch-time loop and the plan of instance b, by one whole warp; `walk`
 // is 64 ints of shared scratch for the warp (stage q -> (i | j << 8 | m << 16 |
 // c' << 20, p)).
-static __device__ __noinline__ void backtrack_warp(const PassArgs &a, int b, int *walk) {
+__device__ __forceinline__ void backtrack_warp_body(const PassArgs &a, int b, int *walk) {
     const int lane = threadIdx.x & 31;
     const PrepHdr *ph = prep_hdr(a, b);
     nest_plan_header *hdr = reinterpret_cast<nest_plan_header *>(a.plans_out + int64_t(b) * a.plan_stride);
@@ -636,5 +636,8 @@ static __device__ __noinline__ void backtrack_warp(const PassArgs &a, int b, int
     }
 }
 
+
+// The same as a called function (the backtrack kernel); the fused sweep inlines the body.
+static __device__ __noinline__ void backtrack_warp(const PassArgs &a, int b, int *walk) { backtrack_warp_body(a, b, walk); }
 
 }  // namespace nest

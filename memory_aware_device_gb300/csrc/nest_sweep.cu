@@ -36,7 +36,7 @@
 #include <cstdio>
 #include <cstdlib>
 
-#include "nest_internal.cuh"
+#include "nest_stages.cuh"
 
 namespace nest {
 
@@ -93,6 +93,9 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Orders this thread's completed async-proxy global writes (bulk copies) before its later
+// generic-proxy operations (a release that other CTAs acquire).
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Bounded wait for the given phase of an mbarrier.  Each poll is a try_wait that
 // suspends the warp in hardware for up to kSuspendNs while the phase is incomplete,
@@ -792,7 +795,10 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
             bulk_commit();
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) {
+        bulk_wait_all();
+        fence_proxy_async_global();   // the dp rows are read by rank 0's plan walk
+    }
     // every row pushed to this CTA has landed before it may exit (bounded waits)
     if (tid == 0) {
         for (int k = 0; k < nown; k++) {
@@ -801,8 +807,8 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
             for (int j = 1; j < L; j++) mbar_wait(&rowbar[k * g.Nmax + j], 0, kDefaultSpin);
         }
     }
+    if (tid == 0 && abort_flag) ph->status = NEST_TIMED_OUT;   // before the barrier: rank 0 reads it
     cluster_sync();
-    if (tid == 0 && abort_flag) ph->status = NEST_TIMED_OUT;
 }
 
 // Each (word width, graph) variant of the body: a called function for up to two
@@ -833,7 +839,13 @@ __global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs
     const int b = blockIdx.x / a.cluster;
     const int rank = int(cluster_rank());
     PrepHdr *ph = prep_hdr(a, b);
-    if (ph->status != NEST_SOLVED) return;  // uniform over the cluster
+    __shared__ int walk[64];   // the plan walk's scratch
+    if (ph->status != NEST_SOLVED) {   // uniform over the cluster
+        // the plan header of an instance that is not solved; the 64-bit launch of a split
+        // sweep leaves it to the first launch
+        if (a.fuse_walk && a.word_mode != 2 && rank == 0 && threadIdx.x < 32) backtrack_warp_body(a, b, walk);
+        return;
+    }
     // the word width is uniform over the cluster too: every CTA reads the same header;
     // a launch for one width leaves the other width's instances to its companion launch
     const bool narrow = narrow_words(ph);
@@ -849,6 +861,11 @@ __global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs
         else
             run_body<CT, KT, int64_t, false>(a, ph, b, rank, sm, abort_flag);
     }
+    // the final reduction and the plan, by one warp of rank 0, once every CTA of the
+    // cluster has written its dp rows (the cluster barrier at the end of the sweep);
+    // other clusters' sweeps hide it.  Its indices are read again here so that nothing
+    // stays live across the body (which would take registers from it).
+    if (a.fuse_walk && cluster_rank() == 0 && threadIdx.x < 32) backtrack_warp_body(a, int(blockIdx.x) / a.cluster, walk);
 }
 
 // ---------------------------------------------------------------------------------

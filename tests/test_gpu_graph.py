@@ -153,7 +153,9 @@ def test_split_sweep_with_both_word_widths():
     for b in (2, 5, 11):
         insts[b] = G.scaled(insts[b], 64)
     plan = nest.describe_launch(nest.make_dims(insts))
-    assert plan["sweep_split"] == 1 and plan["kernels_per_chunk"] == 5, plan
+    # prep, stage loads and the two sweep launches; both are resident, so their clusters
+    # write the plans and no backtrack kernel runs
+    assert plan["sweep_split"] == 1 and plan["kernels_per_chunk"] == 4, plan
     s, res = G.run(insts)
     oracle = G.oracle_many(insts, fn=G.solve_graph)
     for b in range(len(insts)):
