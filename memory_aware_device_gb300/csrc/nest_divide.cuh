@@ -40,8 +40,35 @@ __host__ __device__ inline uint64_t mulhi64(uint64_t a, uint64_t b) {
 #endif
 }
 
-// floor((hi * 2^64 + 0) / d) for hi < d, by restoring long division over 64 bits.
+// floor((hi * 2^64 + 0) / d) for hi < d.  Divisors below 2^41 take three long-division
+// steps of 22, 21 and 21 quotient bits (the remainder stays below d, so the shifted
+// remainder fits 64 bits): each step estimates its quotient digit with a float
+// reciprocal (within a few units of the digit, which is below 2^22) and corrects it
+// exactly with integer arithmetic.  Larger divisors go bit by bit.
 __host__ __device__ inline uint64_t div128_by_64(uint64_t hi, uint64_t d) {
+    if (d < (uint64_t(1) << 41)) {
+        const float rd = 1.0f / float(d);
+        uint64_t q = 0, r = hi;
+        const int step[3] = {22, 21, 21};
+        for (int k = 0; k < 3; k++) {
+            r <<= step[k];                                       // r < 2^63
+            float est = float(r) * rd;
+            est = est < 0.0f ? 0.0f : est;
+            uint64_t qk = uint64_t(est);                         // < 2^22 + a few
+            int64_t rem = int64_t(r - qk * d);   // the true difference is a few d: wraps exactly
+            while (rem < 0) {
+                qk--;
+                rem += int64_t(d);
+            }
+            while (rem >= int64_t(d)) {
+                qk++;
+                rem -= int64_t(d);
+            }
+            r = uint64_t(rem);
+            q = (q << step[k]) | qk;
+        }
+        return q;
+    }
     uint64_t q = 0, r = hi;  // invariant r < d
     for (int bit = 63; bit >= 0; --bit) {
         const bool carry = (r >> 63) != 0;  // r * 2 overflows 64 bits
@@ -56,8 +83,12 @@ __host__ __device__ inline uint64_t div128_by_64(uint64_t hi, uint64_t d) {
 
 __host__ __device__ inline Divisor make_divisor(uint64_t d) {
     Divisor v;
-    uint32_t l = 0;
-    while (l < 64 && (uint64_t(1) << l) < d) l++;  // l = ceil(log2 d)
+    // l = ceil(log2 d)
+#ifdef __CUDA_ARCH__
+    const uint32_t l = d <= 1 ? 0u : uint32_t(64 - __clzll((long long)(d - 1)));
+#else
+    const uint32_t l = d <= 1 ? 0u : uint32_t(64 - __builtin_clzll(d - 1));
+#endif
     // m' = floor(2^64 (2^l - d) / d) + 1; (2^l - d) < d so the quotient fits 64 bits
     const uint64_t top = l == 64 ? uint64_t(0) - d : (uint64_t(1) << l) - d;
     v.mul = div128_by_64(top, d) + 1;

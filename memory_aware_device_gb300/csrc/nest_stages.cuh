@@ -148,10 +148,18 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
         ph->G[t] = t < h.T ? G[t] : 0;
         ph->bw[t] = t < h.T ? bw[t] : 1;
         ph->lat[t] = t < h.T ? lat[t] : 0;
-        ph->bwdiv[t] = make_divisor(uint64_t(t < h.T ? bw[t] : 1));
     }
-    if (threadIdx.x == 8) ph->Mdiv = make_divisor(uint64_t(h.M));
-    if (threadIdx.x == 9) ph->Rdiv = make_divisor(uint64_t(h.R));
+    // the ten invariant divisors (tier bandwidths, M, R), one per warp's lane 0 so that
+    // they are computed side by side rather than serialised within one warp
+    if ((threadIdx.x & 31) == 0)
+        for (int k = int(threadIdx.x >> 5); k < 10; k += int(blockDim.x >> 5)) {
+            if (k < 8)
+                ph->bwdiv[k] = make_divisor(uint64_t(k < h.T ? bw[k] : 1));
+            else if (k == 8)
+                ph->Mdiv = make_divisor(uint64_t(h.M));
+            else
+                ph->Rdiv = make_divisor(uint64_t(h.R));
+        }
     for (int x = threadIdx.x; x < 16; x += blockDim.x) {
         int t = 0;
         while (t < h.T - 1 && G[t] < (int64_t(1) << x)) t++;

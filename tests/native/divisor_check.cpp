@@ -1,6 +1,8 @@
 // Host-side check of the invariant-divisor division used by the cost builder:
 // compares nest::divide / nest::divide_up with the C++ operators on edge values
-// and on random values across the ranges the solver uses.
+// (including both sides of 2^41, where the multiplier's long division changes from
+// three 64-bit steps to bit by bit) and on random values across the ranges the
+// solver uses.
 #include <cstdint>
 #include <cstdio>
 #include <random>
@@ -11,7 +13,8 @@ int main() {
     std::mt19937_64 rng(12345);
     const uint64_t edge_d[] = {1, 2, 3, 5, 7, 10, 999, 1000, 1001, 1024, 4095, 4096, 4097, 6250, 12500, 25000,
                                50000, 900000, (1ull << 20) - 1, 1ull << 20, (1ull << 40) - 1, 1ull << 40,
-                               (1ull << 40) + 1, (1ull << 63) - 1, 1ull << 63, ~0ull};
+                               (1ull << 40) + 1, (1ull << 41) - 1, 1ull << 41, (1ull << 41) + 1,
+                               (1ull << 63) - 1, 1ull << 63, ~0ull};
     const uint64_t edge_n[] = {0, 1, 2, 999, 1000, 1001, (1ull << 32) - 1, 1ull << 32, (1ull << 59) + 12345,
                                (1ull << 62) - 1, (1ull << 63) - 1, 1ull << 63, ~0ull - 1, ~0ull};
     long bad = 0, count = 0;
