@@ -549,7 +549,8 @@ def main():
                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                   "frac": loads_bytes_all / (kms["stage_loads"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
                   "traffic": stored_traffic("stage_loads", workload),
-                  "note": "integer-ALU bound: about 60 exact integer operations per (stage, width, strategy) word"}
+                  "note": "integer-ALU bound: exact 64-bit collective prices, about 430 integer instructions "
+                          "per (stage, width, strategy) word (ncu: 9.5 M warp instructions for 709 K words)"}
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(instances, relax_total, args.cpu_seconds)
