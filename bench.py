@@ -571,7 +571,7 @@ def main():
                 "kernel_ms_note": "separate pass, events at every kernel boundary (no launch overlap)",
                 "roofline": roof, "roofline_stage_loads": roof_loads, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(records.nbytes),
-                        "d2h_bytes_per_step": int(8 * B + B * nest.plan_bytes(dims) + (4 * (B // group) if group > 1 else 0)),
+                        "d2h_bytes_per_step": int(B * nest.plan_bytes(dims) + (8 * B + 4 * (B // group) if group > 1 else 0)),
                         "ms_per_step": e2e_total / e2e_steps},
                 "gpu_launches": launches, "clocks": clk}
         print(json.dumps(line), flush=True)

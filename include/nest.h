@@ -218,7 +218,8 @@ int nest_solve(const nest_dims *dims, const void *records, int64_t *costs_out, v
 size_t nest_workspace_size_host(const nest_dims *dims, int32_t chunk);
 
 /* Solve a batch held in HOST memory: copies the records to the device workspace,
- * solves, copies costs and plans back and synchronises the stream.
+ * solves, copies the plans back (costs_host is filled from their headers' t_batch)
+ * and synchronises the stream.
  *   records_host, costs_host, plans_host   HOST buffers (pinned memory is faster)
  *   workspace    DEVICE, >= nest_workspace_size_host(dims, opt->chunk) bytes
  * Returns NEST_OK, NEST_E_TIMEOUT if some instance timed out, or NEST_E_*. */

@@ -231,17 +231,20 @@ int nest_solve_host(const nest_dims *dims, const void *records_host, int64_t *co
     if (rc != NEST_OK) return rc;
     rc = nest_solve(dims, rec_d, costs_d, plans_d, ws, ws_left, stream, opt);
     if (rc != NEST_OK) return rc;
-    if ((rc = cuda_status(cudaMemcpyAsync(costs_host, costs_d, size_t(8 * B), cudaMemcpyDeviceToHost, st),
-                          "cudaMemcpyAsync (costs)")) ||
-        (rc = cuda_status(cudaMemcpyAsync(plans_host, plans_d, size_t(B * plan_bytes(g)), cudaMemcpyDeviceToHost, st),
+    // one copy back: every plan header carries its instance's t_batch (-1 unless solved),
+    // which is what costs_out holds
+    if ((rc = cuda_status(cudaMemcpyAsync(plans_host, plans_d, size_t(B * plan_bytes(g)), cudaMemcpyDeviceToHost, st),
                           "cudaMemcpyAsync (plans)")) ||
         (rc = cuda_status(cudaStreamSynchronize(st), "cudaStreamSynchronize")))
         return rc;
     const unsigned char *ph = static_cast<const unsigned char *>(plans_host);
-    for (int64_t b = 0; b < B; b++)
-        if (reinterpret_cast<const nest_plan_header *>(ph + b * plan_bytes(g))->status == NEST_TIMED_OUT)
-            return NEST_E_TIMEOUT;
-    return NEST_OK;
+    bool timed_out = false;
+    for (int64_t b = 0; b < B; b++) {
+        const nest_plan_header *h = reinterpret_cast<const nest_plan_header *>(ph + b * plan_bytes(g));
+        costs_host[b] = h->t_batch;
+        timed_out = timed_out || h->status == NEST_TIMED_OUT;
+    }
+    return timed_out ? NEST_E_TIMEOUT : NEST_OK;
 }
 
 }  // extern "C"

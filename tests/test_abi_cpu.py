@@ -143,3 +143,16 @@ def test_cost_tensor_sizes_match_workload_table():
         x = synth.config_instance(cfg, 0)
         K = (x.D // x.unit).bit_length()
         assert x.L * (x.L + 1) // 2 * K * len(x.strat) == words
+
+
+def test_describe_launch_without_a_device():
+    # no GPU here: the shape falls back to the streaming sweep, followed by the backtrack
+    dims = nest.make_dims(synth.config_batch(2, B=4))
+    d = nest.describe_launch(dims)
+    assert d["chunks"] == 1 and d["sweep_variant"] in (1, 2)
+    assert d["kernels_per_chunk"] == (3 if d["sweep_variant"] == 1 else 4) + d["sweep_split"]
+    assert nest.describe_launch(dims, nest.options(chunk=3))["chunks"] == 2
+    bad = nest.Dims(B=1, Lmax=256, Tmax=1, Cmax=1, Smax=1, Pcap=1, Dumax=1)
+    with pytest.raises(nest.NestError):
+        nest.describe_launch(bad)
+    assert nest.lib().nest_describe_launch(C.byref(dims), None, None) == nest.NEST_E_INVALID
