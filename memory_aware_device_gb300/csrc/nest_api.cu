@@ -1,9 +1,11 @@
 // C ABI of the placement-DP solver (declared in include/nest.h).
 //
 // A call validates the batch dimensions on the host, then, for each chunk of
-// instances, enqueues four kernels on the caller's stream: prep (validation,
-// prefix sums, link costs), stage loads (cost build and strategy reduction), DP
-// sweep and backtrack.  Nothing is allocated and no state survives the call.
+// instances, enqueues on the caller's stream: prep (validation, prefix sums, DP
+// states, link costs), stage loads (cost build and strategy reduction), the DP sweep
+// (two launches when split by word width) and, after a streaming sweep only, the
+// backtrack (a resident sweep's clusters write their plans).  Nothing is allocated
+// and no state survives the call.
 #include <cuda_runtime.h>
 
 #include <cstdio>

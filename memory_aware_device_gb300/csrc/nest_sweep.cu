@@ -1,32 +1,37 @@
 // DP sweep: the backward min-max recurrence of Nest (Network- and Memory-Aware
-// Device Placement) §4 Eq. 3, one step per start layer i = L-1 .. 0.
+// Device Placement) §4 Eq. 3, one step per DP state i = L-1 .. 0 (the suffixes of a
+// chain, or the up-sets of a layer DAG; L is the last state, the empty set).
 //
 //   dp[i][d][p][c] = min over j in (i, L], width unit * 2^m <= d units, next-link
 //                    candidate c' of  max(load*(i, j, m, p) + X[i][c] + X[j][c'],
 //                                         dp[j][d - 2^m][p - 1][c'])
 //
-// c is the candidate tier of the link into the stage starting at i (the "delayed
-// forward cost" of the not yet placed producer), c' the tier of the link to the
-// next stage; a stage of width k next to a link over candidate c needs
-// 2k <= G[cand c].  p counts stages of the suffix (the stage's 1F1B position,
-// §3.3), so load* is the per-position strategy minimum from the reduction pass.
+// c is the candidate tier of the link into the stage starting at state i (the
+// "delayed forward cost" of the not yet placed producer), c' the tier of the link to
+// the next stage; a stage of width k next to a link over candidate c needs
+// 2k <= G[cand c].  p counts the stages still to place (the stage's 1F1B position,
+// §3.3), so load* is the per-position strategy minimum from the stage-loads pass; for
+// a graph, a pair of states that is not nested has no load and is no transition.
 // Cells keep the smallest packed key (v << 24) | (j << 8) | (m << 4) | c', which
 // makes the argmin unique and deterministic.
 //
-// GB300 mapping.  One cluster of `cluster` CTAs per instance; positions p are
-// dealt round-robin over the cluster (CTA r owns p = r + 1 + k * cluster).  A
-// thread owns one device count d and all candidates c of that d; `jsplit` threads
-// share a cell by splitting the cut points j and combine by a min over packed keys.
-// Steps are separated by a cluster barrier (release / acquire).
+// GB300 mapping.  One cluster of `cluster` CTAs per instance; positions p are dealt
+// round-robin over the cluster (CTA r owns p = r + 1 + k * cluster).  A thread owns
+// one device count d and all candidates c of that d; `jsplit` threads (adjacent
+// lanes) share a cell by splitting the cut points j and combine by shuffles.
 //
 // Two variants:
 //  - resident: every CTA keeps, in shared memory, all rows dp[j][*][p-1][*] it will
 //    read for its positions p.  The owner of position p pushes each new row into the
-//    shared memory of the owner of p + 1 with distributed-shared-memory stores, so a
-//    step reads no dp data from global memory at all; the loads of the next step are
-//    prefetched by a TMA bulk copy one step ahead.  Used when the rows fit.
+//    shared memory of the owner of p + 1 with st.async stores that complete on a
+//    per-row mbarrier, so the CTAs form a pipeline over positions and a step reads no
+//    dp data from global memory.  Value words are 32-bit when exact for the instance,
+//    else 64-bit; when shared memory sized for both widths would leave the batch in
+//    more waves, the sweep is two launches, one per width.  At the end each cluster's
+//    rank 0 picks t_batch and walks the plan (the backtrack kernel is not needed).
 //  - streaming: rows dp[j > i][p-1] and the loads are staged from global memory by
-//    TMA bulk copies into double-buffered shared memory, tiles of `jc` cut points.
+//    TMA bulk copies into double-buffered shared memory, tiles of `jc` cut points,
+//    with the cluster in lockstep; 64-bit words.
 // Every mbarrier wait is bounded; a wait that gives up marks the instance
 // NEST_TIMED_OUT, drains the copies in flight and keeps taking part in every
 // cluster barrier.
