@@ -345,6 +345,9 @@ def main():
     ap.add_argument("--graph", default="chain", choices=["chain", "two-tower"],
                     help="two-tower: the dense workload's blocks as two 8-block encoder branches feeding a "
                          "16-block trunk, solved over the up-sets of that layer DAG")
+    ap.add_argument("--cuda-graph", action=argparse.BooleanOptionalAction, default=True,
+                    help="capture one solve (all its kernels) in a CUDA graph and time its replays; "
+                         "--no-cuda-graph times direct launches")
     ap.add_argument("--joint", action="store_true",
                     help="joint microbatch-size search: every problem solved with 1, 2, 4 and 8 samples "
                          "per microbatch, the best variant selected on the GPU")
@@ -418,13 +421,14 @@ def main():
 
     best = torch.empty(B // group, dtype=torch.int32, device=dev)
 
-    def step(opt):
-        rc = nest.solve_raw(dims, solver.records, solver.costs, solver.plans, solver.workspace, stream, opt)
+    def step(opt, st=None):
+        st = stream if st is None else st
+        rc = nest.solve_raw(dims, solver.records, solver.costs, solver.plans, solver.workspace, st, opt)
         if rc:
             raise nest.NestError(rc)
         if group > 1:   # the joint search: best variant of every problem
             rc = nest.lib().nest_select_best(solver.costs.data_ptr(), B, group, best.data_ptr(),
-                                             ctypes.c_void_p(stream.cuda_stream))
+                                             ctypes.c_void_p(st.cuda_stream))
             if rc:
                 raise nest.NestError(rc, "nest_select_best")
 
@@ -442,6 +446,20 @@ def main():
     dom = max(wk, key=wk.get)
     qdom = KERNELS.index(dom)
 
+    graph = None
+    if args.cuda_graph:
+        # one solve captured once; each timed step replays it (the per-kernel events
+        # cannot be recorded inside the graph, so the roofline uses the warm-up figures)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(nest.options(chunk=args.chunk), side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                step(nest.options(chunk=args.chunk), side)
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+
     # one set of events per step, so nothing syncs inside the timed region
     opts = [make_opt(qdom) for _ in range(args.steps)]
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -454,10 +472,13 @@ def main():
     for s in range(args.steps):
         flush.zero_()                      # L2 flush outside the timed events
         starts[s].record(stream)
-        step(opts[s][0])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(opts[s][0])
         ends[s].record(stream)
     torch.cuda.synchronize(dev)
-    dom_ms = kernel_ms(opts)[dom]
+    dom_ms = kernel_ms(opts)[dom] if graph is None else wk[dom]
     clk = clocks.stop()
     # per-kernel breakdown from a separate pass with events at every kernel boundary
     bd = [make_opt() for _ in range(min(args.steps, 100))]
@@ -568,6 +589,7 @@ def main():
                                          "per second of the whole step",
                 **({"problems_per_s": solves / group, "variants_per_problem": group} if group > 1 else {}),
                 "kernel_ms_per_step": kms,
+                **({"cuda_graph": "each timed step replays one captured solve"} if graph is not None else {}),
                 "kernel_ms_note": "separate pass, events at every kernel boundary (no launch overlap)",
                 "roofline": roof, "roofline_stage_loads": roof_loads, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(records.nbytes),

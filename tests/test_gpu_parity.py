@@ -315,3 +315,31 @@ def test_torus_split_sweep_mixed_widths():
         assert G.same_result(res[b], oracle[b]), (b, plan)
     for b in (0, 1):
         check_tables(s, b, insts[b])
+
+
+@pytest.mark.parametrize("workload", [1, 2])
+def test_solve_replays_from_a_cuda_graph(workload):
+    # nest_solve only enqueues kernels (no allocation, no synchronisation), so a caller
+    # can capture it once and replay it; the replays give the direct results
+    import torch
+    insts = synth.config_batch(workload)
+    dims = nest.make_dims(insts)
+    s = nest.Solver(dims)
+    s.load(nest.pack_records(insts, dims))
+    s.run()
+    torch.cuda.synchronize()
+    want = s.results()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        s.run(stream=side)   # warm the launch attributes on the capturing stream
+        side.synchronize()
+        s.plans.zero_()
+        s.costs.fill_(-7)
+        with torch.cuda.graph(graph, stream=side):
+            s.run(stream=side)
+    for _ in range(2):
+        s.plans.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert s.results() == want
