@@ -345,9 +345,10 @@ def main():
     ap.add_argument("--graph", default="chain", choices=["chain", "two-tower"],
                     help="two-tower: the dense workload's blocks as two 8-block encoder branches feeding a "
                          "16-block trunk, solved over the up-sets of that layer DAG")
-    ap.add_argument("--cuda-graph", action=argparse.BooleanOptionalAction, default=True,
-                    help="also capture one solve (all its kernels) in a CUDA graph and time the faster of "
-                         "its replays and direct launches; --no-cuda-graph times direct launches only")
+    ap.add_argument("--cuda-graph", action="store_true",
+                    help="capture one solve (all its kernels) in a CUDA graph and time its replays; the "
+                         "dominant kernel's duration for the roofline then comes from the warm-up steps "
+                         "(events cannot be read per replay)")
     ap.add_argument("--joint", action="store_true",
                     help="joint microbatch-size search: every problem solved with 1, 2, 4 and 8 samples "
                          "per microbatch, the best variant selected on the GPU")
@@ -459,21 +460,6 @@ def main():
                 step(nest.options(chunk=args.chunk), side)
         stream.wait_stream(side)
         torch.cuda.synchronize(dev)
-
-        # the faster launch mode for this batch: replays or direct launches (the same work)
-        def trial(replay, n=20):
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
-            o = nest.options(chunk=args.chunk)
-            for q in range(n):
-                flush.zero_()
-                ev[2 * q].record(stream)
-                graph.replay() if replay else step(o)
-                ev[2 * q + 1].record(stream)
-            torch.cuda.synchronize(dev)
-            return sum(ev[2 * q].elapsed_time(ev[2 * q + 1]) for q in range(n)) / n
-        t_direct, t_graph = trial(False), trial(True)
-        if t_graph >= t_direct:
-            graph = None
 
     # one set of events per step, so nothing syncs inside the timed region
     opts = [make_opt(qdom) for _ in range(args.steps)]
@@ -605,8 +591,7 @@ def main():
                 **({"problems_per_s": solves / group, "variants_per_problem": group} if group > 1 else {}),
                 "kernel_ms_per_step": kms,
                 "launch_mode": ("CUDA graph: each timed step replays one captured solve" if graph is not None
-                                else "direct launches" + (" (faster than graph replays for this batch)"
-                                                          if args.cuda_graph else "")),
+                                else "direct launches, events around the dominant kernel"),
                 "kernel_ms_note": "separate pass, events at every kernel boundary (no launch overlap)",
                 "roofline": roof, "roofline_stage_loads": roof_loads, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(records.nbytes),
