@@ -178,3 +178,21 @@ def test_widest_graph_matches_chain_mode():
     assert G.same_result(res[0], o) and G.same_result(res[1], o)
     assert res[1]["layers"][0] & (1 << 62) or res[1]["layers"][-1] & (1 << 62)
     np.testing.assert_array_equal(G.dp_keys(s, 1, g), G.oracle_dp_keys(base, o["dp"]))
+
+
+def test_largest_state_count_on_the_dense_tiers():
+    # 8 independent layers (every subset is an up-set: 256 states, the most the 8-bit
+    # state index allows) with the dense workload's tiers, widths and strategies, next
+    # to a chain instance in the same batch
+    g = synth.config_instance(2, 2)
+    g.L, g.Pmax, g.M = 8, 8, 64
+    for f in ("fl", "pd", "pe", "ao", "aw", "a2a", "moe"):
+        setattr(g, f, np.resize(getattr(g, f), 8))
+    g.succ = np.zeros(8, np.uint64)
+    chain = synth.config_instance(2, 3)
+    chain.Pmax = 8
+    s, res = G.run([g, chain], Vmax=255)
+    og = G.check_graph_tables(s, 0, g)
+    assert og["status"] == 0 and len(og["states"]) == 256
+    assert G.same_graph_result(res[0], og)
+    assert G.same_result(res[1], O.solve(chain))
