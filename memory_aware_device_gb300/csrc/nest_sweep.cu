@@ -1073,9 +1073,9 @@ int launch_cluster(Kern fn, const PassArgs &a, void *stream, size_t smem, const 
                          a);
 }
 
-// The resident variant is instantiated for up to 4 candidates and KT = 4, 8 or 16 widths.
+// The resident variant is instantiated for 1, 2, 3 or 4 candidates and KT = 4, 8 or 16 widths.
 inline int kt_of(int Kmax) { return Kmax <= 4 ? 4 : Kmax <= 8 ? 8 : 16; }
-inline int ct_of(int Cmax) { return Cmax <= 1 ? 1 : Cmax <= 2 ? 2 : 4; }
+inline int ct_of(int Cmax) { return Cmax <= 3 ? Cmax : 4; }
 
 template <int CT, int KT>
 int resident_capacity(int cluster, int threads, size_t smem) {
@@ -1102,6 +1102,7 @@ int resident_capacity_ct(const Geo &g, int cluster, int threads, size_t smem) {
     if (g.Cmax > 4) return 0;
     if (CT == 1) return resident_capacity_kt<1>(KT, cluster, threads, smem);
     if (CT == 2) return resident_capacity_kt<2>(KT, cluster, threads, smem);
+    if (CT == 3) return resident_capacity_kt<3>(KT, cluster, threads, smem);
     return resident_capacity_kt<4>(KT, cluster, threads, smem);
 }
 
@@ -1289,6 +1290,7 @@ int launch_sweep(const PassArgs &a, void *stream) {
     if (a.resident) {
         if (a.g.Cmax <= 1) return launch_resident_kt<1>(a, stream);
         if (a.g.Cmax <= 2) return launch_resident_kt<2>(a, stream);
+        if (a.g.Cmax <= 3) return launch_resident_kt<3>(a, stream);
         return launch_resident_kt<4>(a, stream);
     }
     if (a.g.Cmax <= 1) return launch_ct<1>(a, stream);
