@@ -1217,7 +1217,11 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
                 if (cap <= 0) continue;
                 const int waves = (n + cap - 1) / cap;
                 const int serial = (nown_c + ngrp - 1) / ngrp;
-                const double ideal = g.Nmax >= 64 ? 512.0 : g.Nmax > 32 ? 8.0 * g.Nmax : 256.0;
+                // a pass whose CTAs fill at most half the SMs is latency-bound: the most
+                // threads per instance then (measured: 16 x 32-state instances at B <= 4
+                // 8 % faster with jsplit 8, at B = 8 slower)
+                const bool sparse = int64_t(n) * cs * 2 <= int64_t(sms);
+                const double ideal = sparse || g.Nmax >= 64 ? 512.0 : g.Nmax > 32 ? 8.0 * g.Nmax : 256.0;
                 const double score = 1.0 / (double(waves) * serial * ngrp * (1.0 + (16 - cs) / 64.0) *
                                             (1.0 + std::fabs(std::log2(gsize / ideal)) / 8));
                 if (score > r.best) {
