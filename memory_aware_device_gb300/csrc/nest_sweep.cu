@@ -835,8 +835,12 @@ __device__ __forceinline__ void run_body(const PassArgs &a, PrepHdr *ph, int b, 
         resident_body<CT, KT, V, kGraph>(a, ph, b, rank, sm, abort_flag);
 }
 
-template <int CT, int KT>
-__global__ void __launch_bounds__(kMaxThreads, 2) sweep_resident_kernel(PassArgs a) {
+// MAXT: the largest CTA the instantiation serves.  512 threads at 2 CTAs per SM leave
+// 64 registers per thread; CTAs of up to 256 threads with one or two candidates get an
+// instantiation for 3 CTAs per SM, which leaves 85 (measured: 3 % faster on the dense
+// workload, whose 256-thread CTAs no longer spill).
+template <int CT, int KT, int MAXT>
+__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 3 : 2) sweep_resident_kernel(PassArgs a) {
     extern __shared__ __align__(128) int64_t sm[];
     __shared__ volatile int abort_flag;
     pdl_wait();
@@ -1077,17 +1081,28 @@ int launch_cluster(Kern fn, const PassArgs &a, void *stream, size_t smem, const 
 inline int kt_of(int Kmax) { return Kmax <= 4 ? 4 : Kmax <= 8 ? 8 : 16; }
 inline int ct_of(int Cmax) { return Cmax <= 3 ? Cmax : 4; }
 
-template <int CT, int KT>
-int resident_capacity(int cluster, int threads, size_t smem) {
-    if (set_attributes(sweep_resident_kernel<CT, KT>, smem, cluster, "resident occupancy") != NEST_OK) return 0;
+template <int CT, int KT, int MAXT>
+int resident_capacity_b(int cluster, int threads, size_t smem) {
+    if (set_attributes(sweep_resident_kernel<CT, KT, MAXT>, smem, cluster, "resident occupancy") != NEST_OK) return 0;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = cluster_config(1, cluster, threads, smem, nullptr, attr);
     int num = 0;
-    if (cudaOccupancyMaxActiveClusters(&num, sweep_resident_kernel<CT, KT>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&num, sweep_resident_kernel<CT, KT, MAXT>, &cfg) != cudaSuccess) {
         cudaGetLastError();   // clear the error of an unsupported shape
         return 0;
     }
     return num;
+}
+
+// The instantiation a CTA of `threads` threads runs (see sweep_resident_kernel).
+template <int CT>
+constexpr bool small_bounds_ok() { return CT <= 2; }
+
+template <int CT, int KT>
+int resident_capacity(int cluster, int threads, size_t smem) {
+    if constexpr (small_bounds_ok<CT>())
+        if (threads <= 256) return resident_capacity_b<CT, KT, 256>(cluster, threads, smem);
+    return resident_capacity_b<CT, KT, kMaxThreads>(cluster, threads, smem);
 }
 
 template <int CT>
@@ -1110,7 +1125,10 @@ template <int CT, int KT>
 int launch_resident(const PassArgs &a, void *stream) {
     if (a.cluster < 2 && a.g.Pcap > 1) return NEST_E_LIMITS;   // pushes need a peer CTA
     const size_t smem = size_t(sweep_resident_smem_bytes(a.g, a.cluster, a.jsplit, a.threads, a.word_mode));
-    return launch_cluster(sweep_resident_kernel<CT, KT>, a, stream, smem, "sweep (resident) launch");
+    if constexpr (small_bounds_ok<CT>())
+        if (a.threads <= 256)
+            return launch_cluster(sweep_resident_kernel<CT, KT, 256>, a, stream, smem, "sweep (resident) launch");
+    return launch_cluster(sweep_resident_kernel<CT, KT, kMaxThreads>, a, stream, smem, "sweep (resident) launch");
 }
 
 template <int CT>
