@@ -18,7 +18,7 @@ namespace nest {
 // Shared scratch of prep_instance: flags and counters, the record, the layer values,
 // the sparse table and the up-set lists of a graph instance (byte offsets).
 struct PrepScratch {
-    int64_t flags, rec, sv, sst, gen, lev, bytes;
+    int64_t flags, rec, sv, sst, gen, lev, sain, sdiv, bytes;
 };
 
 __host__ __device__ inline PrepScratch prep_scratch(const Geo &g, const nest_layout &rl) {
@@ -29,7 +29,9 @@ __host__ __device__ inline PrepScratch prep_scratch(const Geo &g, const nest_lay
     s.sst = s.sv + align_up(8 * int64_t(kNumPfx) * g.Lmax, 128);
     s.gen = s.sst + align_up(8 * int64_t(kLogL) * g.Lmax, 128);
     s.lev = s.gen + 8 * kMaxStates;
-    s.bytes = s.lev + 4 * 72;
+    s.sain = s.lev + 4 * 72;                          // bytes entering each state
+    s.sdiv = s.sain + 8 * kMaxStates;                 // the tier divisors
+    s.bytes = s.sdiv + int64_t(sizeof(Divisor)) * 8;
     return s;
 }
 
@@ -149,16 +151,24 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
         ph->bw[t] = t < h.T ? bw[t] : 1;
         ph->lat[t] = t < h.T ? lat[t] : 0;
     }
-    // the ten invariant divisors (tier bandwidths, M, R), one per warp's lane 0 so that
-    // they are computed side by side rather than serialised within one warp
+    // the invariant divisors (the tiers' bandwidths, M and R), one per warp's lane 0 so
+    // that they are computed side by side; the tier divisors are kept in shared memory
+    // for the link table too
+    Divisor *sdiv = reinterpret_cast<Divisor *>(scr + ps.sdiv);
     if ((threadIdx.x & 31) == 0)
         for (int k = int(threadIdx.x >> 5); k < 10; k += int(blockDim.x >> 5)) {
-            if (k < 8)
-                ph->bwdiv[k] = make_divisor(uint64_t(k < h.T ? bw[k] : 1));
-            else if (k == 8)
+            // k < T: tier k; T: M; T + 1: R; beyond: the unused tiers (divisor 1)
+            if (k < h.T) {
+                sdiv[k] = make_divisor(uint64_t(bw[k]));
+                ph->bwdiv[k] = sdiv[k];
+            } else if (k == h.T) {
                 ph->Mdiv = make_divisor(uint64_t(h.M));
-            else
+            } else if (k == h.T + 1) {
                 ph->Rdiv = make_divisor(uint64_t(h.R));
+            } else {
+                const int t = k - 2;   // h.T <= t < 8
+                ph->bwdiv[t] = make_divisor(1);
+            }
         }
     for (int x = threadIdx.x; x < 16; x += blockDim.x) {
         int t = 0;
@@ -227,11 +237,12 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
     // layer mask, the bytes entering it and the link cost into it per candidate
     const int64_t *ao_in = reinterpret_cast<const int64_t *>(rec + a.rl.ao);
     int64_t *ain = reinterpret_cast<int64_t *>(pb + a.pl.ain);
+    int64_t *sain = reinterpret_cast<int64_t *>(scr + ps.sain);   // the same, in shared memory
     uint64_t *um = reinterpret_cast<uint64_t *>(pb + a.pl.umask);
     int E = L;   // the last state, the empty set
     if (!h.graph) {
         for (int q = threadIdx.x; q <= L; q += blockDim.x) {
-            ain[q] = q > 0 ? ao_in[q - 1] : ao_in[0];
+            sain[q] = ain[q] = q > 0 ? ao_in[q - 1] : ao_in[0];
             um[q] = L <= 64 ? low_bits(L) & ~low_bits(q) : 0;
         }
     } else {
@@ -292,7 +303,7 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
                 const uint64_t bit = uint64_t(1) << l;
                 if (D == full ? !(fed & bit) : (!(D & bit) && (succ[l] & D))) v += ao_in[l];
             }
-            ain[q] = v;
+            sain[q] = ain[q] = v;
         }
         E = n - 1;
     }
@@ -304,7 +315,7 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
         int64_t v = 0;
         if (q > 0 && q < E) {
             const int tr = cand[c];
-            v = lat[tr] + cdiv(ain[q] * 1000, bw[tr]);
+            v = lat[tr] + int64_t(divide_up(uint64_t(sain[q]) * 1000, uint64_t(bw[tr]), sdiv[tr]));
         }
         X[int64_t(q) * g.Cmax + c] = v;
         atomicMax(&xmax, v < 0x7FFFFFFF ? uint32_t(v) : 0x7FFFFFFFu);
