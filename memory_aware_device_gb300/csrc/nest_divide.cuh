@@ -46,6 +46,7 @@ __host__ __device__ inline uint64_t mulhi64(uint64_t a, uint64_t b) {
 // reciprocal (within a few units of the digit, which is below 2^22) and corrects it
 // exactly with integer arithmetic.  Larger divisors go bit by bit.
 __host__ __device__ inline uint64_t div128_by_64(uint64_t hi, uint64_t d) {
+    if (d == 0) return 0;   // no divisor: never used (callers validate d >= 1 first)
     if (d < (uint64_t(1) << 41)) {
         const float rd = 1.0f / float(d);
         uint64_t q = 0, r = hi;
