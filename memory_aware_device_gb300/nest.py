@@ -295,6 +295,20 @@ class Solver:
     def results(self) -> List[dict]:
         return decode_plans(self.plans.cpu().numpy(), self.dims)
 
+    def capture(self, opt: Options | None = None):
+        """One solve of the loaded records captured in a CUDA graph (nest_solve only enqueues
+        kernels, so it captures as is); graph.replay() re-runs it on the current stream."""
+        import torch
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            self.run(stream=side, opt=opt)   # launch attributes set outside the capture
+            with torch.cuda.graph(graph, stream=side):
+                self.run(stream=side, opt=opt)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        return graph
+
 
 def select_best(costs, group: int, stream=None):
     """nest_select_best on a torch int64 CUDA tensor of t_batch values: the best index

@@ -329,15 +329,8 @@ def test_solve_replays_from_a_cuda_graph(workload):
     s.run()
     torch.cuda.synchronize()
     want = s.results()
-    side = torch.cuda.Stream()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        s.run(stream=side)   # warm the launch attributes on the capturing stream
-        side.synchronize()
-        s.plans.zero_()
-        s.costs.fill_(-7)
-        with torch.cuda.graph(graph, stream=side):
-            s.run(stream=side)
+    graph = s.capture()
+    torch.cuda.synchronize()
     for _ in range(2):
         s.plans.zero_()
         graph.replay()
