@@ -196,3 +196,16 @@ def test_largest_state_count_on_the_dense_tiers():
     assert og["status"] == 0 and len(og["states"]) == 256
     assert G.same_graph_result(res[0], og)
     assert G.same_result(res[1], O.solve(chain))
+
+
+def test_graph_batches_in_ragged_chunks():
+    # passes of 7 instances over a mix of DAGs and chains give the oracle's results
+    insts = tiny_graphs(23000, 40, Lmax=7, Dmax=16)
+    for x in insts[::3]:
+        x.succ = None
+    s, res = G.run(insts, chunk=7, keep_costs=False)
+    for b, x in enumerate(insts):
+        o = O.solve(x) if x.succ is None else G.solve_graph(x)
+        assert G.same_result(res[b], o), b
+        if x.succ is not None:
+            assert G.same_graph_result(res[b], o), b
