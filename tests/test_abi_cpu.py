@@ -156,3 +156,13 @@ def test_describe_launch_without_a_device():
     with pytest.raises(nest.NestError):
         nest.describe_launch(bad)
     assert nest.lib().nest_describe_launch(C.byref(dims), None, None) == nest.NEST_E_INVALID
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    # there is no CPU fallback: with libnest.so absent, loading raises instead of solving
+    monkeypatch.setattr(nest, "_lib", None)
+    monkeypatch.setattr(nest, "LIB_PATH", str(tmp_path / "libnest.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        nest.lib()
+    with pytest.raises(RuntimeError):
+        nest.make_dims(synth.config_batch(1)) and nest.record_layout(nest.make_dims(synth.config_batch(1)))
