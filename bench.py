@@ -36,8 +36,9 @@ METRIC = "DP relaxations/sec and placement solves/sec on 1 GB300; % of HBM roofl
 UNIT = "relaxations/s"
 KERNELS = ("prep", "stage_loads", "dp_sweep", "backtrack")
 NEV = len(KERNELS) + 1   # events per chunk
-KERNEL_SRC = {"prep": "nest_prep.cu", "stage_loads": "nest_loads.cu", "dp_sweep": "nest_sweep.cu",
-              "backtrack": "nest_backtrack.cu"}
+KERNEL_SRC = {"prep": ("nest_prep.cu",), "stage_loads": ("nest_loads.cu",),
+              "dp_sweep": ("nest_sweep.cu", "nest_sweep_res_a.cu", "nest_sweep_res_b.cu"),
+              "backtrack": ("nest_backtrack.cu",)}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -142,9 +143,11 @@ def oracle_solve(x):
 
 
 def src_hash(kernel: str) -> str:
-    """Hash of a kernel's source file and every header the kernels share."""
+    """Hash of a kernel's source files and every header the kernels share."""
     d = os.path.join(ROOT, "memory_aware_device_gb300", "csrc")
-    h = hashlib.sha256(open(os.path.join(d, KERNEL_SRC[kernel]), "rb").read())
+    h = hashlib.sha256()
+    for f in KERNEL_SRC[kernel]:
+        h.update(open(os.path.join(d, f), "rb").read())
     for f in sorted(os.listdir(d)):
         if f.endswith(".cuh"):
             h.update(open(os.path.join(d, f), "rb").read())
