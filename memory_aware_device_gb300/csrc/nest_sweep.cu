@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) sweep_stream_kernel(PassArgs a
     const int rank = int(cluster_rank());
     PrepHdr *ph = prep_hdr(a, b);
     if (ph->status != NEST_SOLVED) return;  // uniform over the cluster
-    if (a.word_mode == 2 && narrow_words(ph)) return;   // taken by the resident launch
+    if (a.word_mode == 2 && narrow_words(ph, word_tag_bits(g.Kmax, g.Cmax))) return;   // taken by the resident launch
     const Inst s = load_inst(a, ph, b);
     const StreamPlan sp = stream_plan(g, a.jc, a.jsplit, a.threads);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + sp.mbar);

@@ -302,8 +302,9 @@ __device__ __forceinline__ void st_async_remote(uint32_t addr, uint32_t v, uint3
 // Value words of the resident variant.  `cap` marks a cell without a value, `far` an
 // A entry no cell can take; every finite value stays below `cap`, and far plus any
 // link cost neither overflows nor drops below cap.  32-bit words are exact when the
-// largest load plus two link costs is below 2^30, which the strategy reduction and
-// the prep pass record per instance; otherwise the instance uses 64-bit words.
+// largest load plus two link costs is below 2^30, which the strategy reduction and the
+// prep pass record per instance; otherwise the instance uses 64-bit words.  With one or
+// two candidates the 32-bit words are packed (below) when a few bits more are free.
 template <typename V>
 struct Word;
 template <>
@@ -317,8 +318,41 @@ struct Word<int64_t> {
     static constexpr int64_t far = int64_t(1) << 46;
 };
 
-__device__ __forceinline__ bool narrow_words(const PrepHdr *ph) {
-    return uint64_t(ph->maxload32) + 2 * uint64_t(ph->maxX32) < (uint64_t(1) << 30);
+// Tagged 32-bit words, taken by the instantiations for one or two candidates (KT
+// widths): a value v is held as (v << tb) | m, its width index m in the tb = log2(KT)
+// low bits; `cap` has every value bit set and a clear tag, `far` every bit set.  The
+// maximum of two words with equal tags keeps the tag, so one unsigned minimum over the
+// widths of a cut point orders its candidates by value and then by width, the order
+// of the key fields, with no argument to carry alongside.  Exact while every finite
+// value is at most 2^(32 - tb) - 2; an instance whose values need those bits runs with
+// tb = 0 (plain values, cap = far = all ones) and finds each best's width again.
+template <int KT>
+struct Packed {
+    static constexpr int TB = KT == 4 ? 2 : KT == 8 ? 3 : 4;
+};
+
+// The template widths and candidates a batch's geometry is instantiated for.
+__host__ __device__ constexpr int kt_of(int Kmax) { return Kmax <= 4 ? 4 : Kmax <= 8 ? 8 : 16; }
+__host__ __device__ constexpr int ct_of(int Cmax) { return Cmax <= 3 ? Cmax : 4; }
+
+// Tag bits of the batch's 32-bit words: log2(KT) for one or two candidates, else 0.
+__host__ __device__ constexpr int word_tag_bits(int Kmax, int Cmax) {
+    return ct_of(Cmax) <= 2 ? (kt_of(Kmax) == 4 ? 2 : kt_of(Kmax) == 8 ? 3 : 4) : 0;
+}
+
+// Whether 32-bit words packed with tb tag bits hold an instance: its largest load plus
+// two link costs (an upper bound of every finite value of its DP) is at most
+// 2^(32 - tb) - 2 (below 2^30 with no tag).
+__device__ __forceinline__ bool packed_words(const PrepHdr *ph, int tb) {
+    const uint64_t lim = tb ? (uint64_t(1) << (32 - tb)) - 1 : uint64_t(1) << 30;
+    return uint64_t(ph->maxload32) + 2 * uint64_t(ph->maxX32) < lim;
+}
+
+// Whether an instance takes the resident sweep's 32-bit words (tb: the batch's tag
+// bits).  A chain takes them below 2^30, packed when it can and plain otherwise; a
+// graph only packed (its sweep is instantiated for packed words alone).
+__device__ __forceinline__ bool narrow_words(const PrepHdr *ph, int tb) {
+    return packed_words(ph, ph->graph ? tb : 0);
 }
 
 // Shared-memory plan of the resident variant, in 8-byte words.
@@ -329,7 +363,10 @@ __device__ __forceinline__ bool narrow_words(const PrepHdr *ph) {
 //    with Hrow = dpw / s (mod 32 / s) for values of s 4-byte words and dpw device
 //    counts per warp: those reads land in different banks.
 //  - A[buf][slot][j][c][c'][m] = load*(i, j, m, p) + X[i][c] + X[j][c'] when both
-//    links admit the width, else `far`; A[j] holds an odd number of values (banks).
+//    links admit the width, else `far`.  With 32-bit values A[j] spans CT*CT*KT + 4
+//    values, so every (c, c') run of KT widths starts on 16 bytes (vector loads) and
+//    the lanes reading adjacent j start in different banks; with 64-bit values an odd
+//    number of values does the same for scalar loads.
 //  - staged dp rows [2][slot][Cmax][Dpad] (int64 values, uint32 arguments).
 //  - graph instances: the layer mask of every state, and per step parity the list of
 //    cut points j >= i + 2 whose state lies inside state i (8-bit state indices), its
@@ -375,11 +412,14 @@ __host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, 
     const int h4 = (nown * g.Nmax * res_hrow(g, jsplit, 4) + 1) / 2, h8 = nown * g.Nmax * res_hrow(g, jsplit, 8);
     s.H = off;
     off = up(off + (mode == 1 ? h4 : mode == 2 ? h8 : h4 > h8 ? h4 : h8));
-    s.Aj = CT * CT * KT + 1;
+    const int aj4 = CT * CT * KT + 4, aj8 = CT * CT * KT + 1;
+    s.Aj = vbytes == 4 ? aj4 : aj8;
     s.Aslot = (g.Nmax + 1) * s.Aj;
     s.Abuf = nown * s.Aslot;
+    // two buffers of 4- or 8-byte values (in 8-byte words), sized like H
+    const int a4 = nown * (g.Nmax + 1) * aj4, a8 = 2 * nown * (g.Nmax + 1) * aj8;
     s.A = off;
-    off = up(off + (mode == 1 ? s.Abuf : 2 * s.Abuf));   // two buffers of 4- or 8-byte values
+    off = up(off + (mode == 1 ? a4 : mode == 2 ? a8 : a4 > a8 ? a4 : a8));
     s.Srow = g.Cmax * g.Dpad;
     s.sdv = off;
     off = up(off + 2 * nown * s.Srow);
@@ -401,18 +441,20 @@ __host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, 
 // chains); with NA = 1 one running best per cell is visited in the canonical (m, c')
 // order.  Either way the first strict improvement within a running best is its
 // smallest key.  `mw` is the widest width any lane of the warp admits (uniform).
-template <int CT, int KT, int NA, typename V>
+template <int CT, int KT, int NA, typename V, bool PK>
 __device__ __forceinline__ void relax_one(const V *Aj, const V *Hj, int Hcol, int d, uint32_t jarg, int m, int c2,
-                                          int a_, V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+                                          int a_, V tmask, V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
     constexpr bool kPad = sizeof(V) == 4;   // rows padded with cap below x = 0
+    constexpr bool kPk = PK;   // tagged words: the tag is the width (tmask its bits)
     const int x = kPad ? d - (1 << m) : (d - (1 << m) > 0 ? d - (1 << m) : 0);
-    const V nv = Hj[c2 * Hcol + x];
-    const uint32_t idx = jarg | (uint32_t(m) << 4) | uint32_t(c2);
+    const V nv = kPk ? V(Hj[c2 * Hcol + x] | (V(m) & tmask)) : Hj[c2 * Hcol + x];
+    const uint32_t idx = kPk ? jarg : jarg | (uint32_t(m) << 4) | uint32_t(c2);
 #pragma unroll
     for (int c = 0; c < CT; c++) {
         const V av = Aj[(c * CT + c2) * KT + m];
         const V v = av > nv ? av : nv;
-        const bool take = v < bv[c][a_];
+        // tagged words: a strictly smaller value only (tag bits set for the test)
+        const bool take = (kPk ? V(v | tmask) : v) < bv[c][a_];
         bv[c][a_] = take ? v : bv[c][a_];
         bi[c][a_] = take ? idx : bi[c][a_];
     }
@@ -422,38 +464,72 @@ __device__ __forceinline__ void relax_one(const V *Aj, const V *Hj, int Hcol, in
 // excluded widths read far or cap): the dp values of c2 are loaded first, then each
 // cell takes the minimum over its MT candidates with a tree that keeps the smaller m
 // on ties, and merges it into its running best for c2.  Loads overlap and the serial
-// depth is log2(MT).
-template <int CT, int KT, int NA, int MT, typename V>
+// depth is log2(MT).  On packed 32-bit words the width is the tag, so the tree is a
+// plain minimum and the A words come in 16-byte loads.
+template <int CT, int KT, int NA, int MT, typename V, bool PK>
 __device__ __forceinline__ void relax_c2_t(const V *Aj, const V *Hj, int Hcol, int d, int c2, uint32_t jarg,
-                                           V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+                                           V tmask, V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
     constexpr bool kPad = sizeof(V) == 4;   // rows padded with cap below x = 0
-    V nv[MT];
+    if constexpr (PK) {
+        // tagged words: the dp values of c2 tagged with their width, then per cell the
+        // MT A words by 16-byte loads, one max per width and a tree of minima
+        V nv[MT];
 #pragma unroll
-    for (int m = 0; m < MT; m++) {
-        const int x = kPad ? d - (1 << m) : (d - (1 << m) > 0 ? d - (1 << m) : 0);
-        nv[m] = Hj[c2 * Hcol + x];
-    }
+        for (int m = 0; m < MT; m++) nv[m] = Hj[c2 * Hcol + d - (1 << m)] | (V(m) & tmask);
+        constexpr int NV = (MT + 3) / 4;
 #pragma unroll
-    for (int c = 0; c < CT; c++) {
-        V v[MT];
-        int id[MT];
+        for (int c = 0; c < CT; c++) {
+            const uint4 *a4 = reinterpret_cast<const uint4 *>(Aj + (c * CT + c2) * KT);
+            V v[4 * NV];
+#pragma unroll
+            for (int w = 0; w < NV; w++) {
+                const uint4 t = a4[w];
+                v[4 * w] = t.x;
+                v[4 * w + 1] = t.y;
+                v[4 * w + 2] = t.z;
+                v[4 * w + 3] = t.w;
+            }
+#pragma unroll
+            for (int m = 0; m < MT; m++) v[m] = v[m] > nv[m] ? v[m] : nv[m];
+#pragma unroll
+            for (int w = 1; w < MT; w <<= 1)
+#pragma unroll
+                for (int q = 0; q + w < MT; q += 2 * w) v[q] = v[q + w] < v[q] ? v[q + w] : v[q];
+            // a strictly smaller value only (a later cut point never wins a tie, whatever
+            // its width): compare with the tag bits set
+            const bool take = (v[0] | tmask) < bv[c][c2];
+            bv[c][c2] = take ? v[0] : bv[c][c2];
+            bi[c][c2] = take ? jarg : bi[c][c2];
+        }
+    } else {
+        V nv[MT];
 #pragma unroll
         for (int m = 0; m < MT; m++) {
-            const V av = Aj[(c * CT + c2) * KT + m];
-            v[m] = av > nv[m] ? av : nv[m];
-            id[m] = m;
+            const int x = kPad ? d - (1 << m) : (d - (1 << m) > 0 ? d - (1 << m) : 0);
+            nv[m] = Hj[c2 * Hcol + x];
         }
 #pragma unroll
-        for (int w = 1; w < MT; w <<= 1)
+        for (int c = 0; c < CT; c++) {
+            V v[MT];
+            int id[MT];
 #pragma unroll
-            for (int q = 0; q + w < MT; q += 2 * w) {
-                const bool r = v[q + w] < v[q];   // the left holds the smaller widths
-                v[q] = r ? v[q + w] : v[q];
-                id[q] = r ? id[q + w] : id[q];
+            for (int m = 0; m < MT; m++) {
+                const V av = Aj[(c * CT + c2) * KT + m];
+                v[m] = av > nv[m] ? av : nv[m];
+                id[m] = m;
             }
-        const bool take = v[0] < bv[c][c2];
-        bv[c][c2] = take ? v[0] : bv[c][c2];
-        bi[c][c2] = take ? jarg | (uint32_t(id[0]) << 4) | uint32_t(c2) : bi[c][c2];
+#pragma unroll
+            for (int w = 1; w < MT; w <<= 1)
+#pragma unroll
+                for (int q = 0; q + w < MT; q += 2 * w) {
+                    const bool r = v[q + w] < v[q];   // the left holds the smaller widths
+                    v[q] = r ? v[q + w] : v[q];
+                    id[q] = r ? id[q + w] : id[q];
+                }
+            const bool take = v[0] < bv[c][c2];
+            bv[c][c2] = take ? v[0] : bv[c][c2];
+            bi[c][c2] = take ? jarg | (uint32_t(id[0]) << 4) | uint32_t(c2) : bi[c][c2];
+        }
     }
 }
 
@@ -462,25 +538,25 @@ __device__ __forceinline__ void relax_c2_t(const V *Aj, const V *Hj, int Hcol, i
 // in every A entry of c2, which never improves a running best).  With NA = CT each c2
 // dispatches once on its (warp-uniform) width count to a fully unrolled body; with
 // NA = 1 one running best per cell is visited in the canonical (m, c') order.
-template <int CT, int KT, int NA, typename V>
+template <int CT, int KT, int NA, typename V, bool PK>
 __device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, int d, int C, uint32_t jarg,
-                                          const int (&mwc)[CT], V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
+                                          const int (&mwc)[CT], V tmask, V (&bv)[CT][NA], uint32_t (&bi)[CT][NA]) {
     if constexpr (NA > 1) {
 #pragma unroll
         for (int c2 = 0; c2 < CT; c2++) {
             if (c2 >= C) break;
             switch (mwc[c2]) {
-            case 0: relax_c2_t<CT, KT, NA, 1, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
-            case 1: if constexpr (KT >= 2) relax_c2_t<CT, KT, NA, 2, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
-            case 2: if constexpr (KT >= 3) relax_c2_t<CT, KT, NA, 3, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
-            case 3: if constexpr (KT >= 4) relax_c2_t<CT, KT, NA, 4, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
-            case 4: if constexpr (KT >= 5) relax_c2_t<CT, KT, NA, 5, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
-            case 5: if constexpr (KT >= 6) relax_c2_t<CT, KT, NA, 6, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
-            case 6: if constexpr (KT >= 7) relax_c2_t<CT, KT, NA, 7, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
-            case 7: if constexpr (KT >= 8) relax_c2_t<CT, KT, NA, 8, V>(Aj, Hj, Hcol, d, c2, jarg, bv, bi); break;
+            case 0: relax_c2_t<CT, KT, NA, 1, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
+            case 1: if constexpr (KT >= 2) relax_c2_t<CT, KT, NA, 2, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
+            case 2: if constexpr (KT >= 3) relax_c2_t<CT, KT, NA, 3, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
+            case 3: if constexpr (KT >= 4) relax_c2_t<CT, KT, NA, 4, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
+            case 4: if constexpr (KT >= 5) relax_c2_t<CT, KT, NA, 5, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
+            case 5: if constexpr (KT >= 6) relax_c2_t<CT, KT, NA, 6, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
+            case 6: if constexpr (KT >= 7) relax_c2_t<CT, KT, NA, 7, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
+            case 7: if constexpr (KT >= 8) relax_c2_t<CT, KT, NA, 8, V, PK>(Aj, Hj, Hcol, d, c2, jarg, tmask, bv, bi); break;
             default:
                 // more than 8 widths: one at a time
-                for (int m = 0; m <= mwc[c2] && m < KT; m++) relax_one<CT, KT, NA, V>(Aj, Hj, Hcol, d, jarg, m, c2, c2, bv, bi);
+                for (int m = 0; m <= mwc[c2] && m < KT; m++) relax_one<CT, KT, NA, V, PK>(Aj, Hj, Hcol, d, jarg, m, c2, c2, tmask, bv, bi);
                 break;
             }
         }
@@ -491,7 +567,7 @@ __device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, in
             for (int c2 = 0; c2 < CT; c2++) {
                 if (c2 >= C) break;
                 if (m > mwc[c2]) continue;
-                relax_one<CT, KT, NA, V>(Aj, Hj, Hcol, d, jarg, m, c2, 0, bv, bi);
+                relax_one<CT, KT, NA, V, PK>(Aj, Hj, Hcol, d, jarg, m, c2, 0, tmask, bv, bi);
             }
         }
     }
@@ -516,7 +592,7 @@ __device__ __forceinline__ void relax_cut(const V *Aj, const V *Hj, int Hcol, in
 //    (for the backtrack) by bulk copies.
 // The footprint is kept small so that the clusters of a whole batch are resident at
 // once.
-template <int CT, int KT, typename V, bool kGraph>
+template <int CT, int KT, typename V, bool kGraph, int kTag>
 __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
                                               volatile int &abort_flag) {
     constexpr int NA = CT <= 2 ? CT : 1;   // running bests per cell
@@ -534,7 +610,17 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     int *jl_hdr = reinterpret_cast<int *>(sm + sp.jl);                       // [2][2]
     uint8_t *jl_list = reinterpret_cast<uint8_t *>(sm + sp.jl + 2);          // [2][Nmax]
     constexpr bool graph = kGraph;   // states are the up-sets of a layer DAG
-    constexpr V cap = Word<V>::cap, far = Word<V>::far;
+    // tagged 32-bit words (kTag 1 or 2; one or two candidates): the width index rides
+    // in the tb low bits of every value, so the running bests carry only the cut point
+    // in bi.  With kTag 1 an instance whose values leave no room for the tag runs with
+    // tb = 0 (plain values, cap = far = all ones) and finds the width of each cell's
+    // best again at the end of the step; kTag 2 always has room (tb fixed)
+    constexpr bool kPack = kTag != 0;
+    static_assert(!kPack || (sizeof(V) == 4 && CT <= 2), "tagged words are 32-bit, one or two candidates");
+    const int tb = kTag == 2 ? Packed<KT>::TB : kTag == 1 && packed_words(ph, Packed<KT>::TB) ? Packed<KT>::TB : 0;
+    const V tmask = kPack ? V((1u << tb) - 1u) : V(0);
+    const V cap = kPack ? V(~0u << tb) : Word<V>::cap;
+    constexpr V far = kPack ? V(~0u) : Word<V>::far;
 
     // thread = (slot group, device count d, slice js), slices in adjacent lanes; the
     // ngrp groups of gsize threads work on different slots at the same time
@@ -627,7 +713,8 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
             for (int c2 = 0; c2 < CT; c2++) {
                 if (c2 >= C) break;
                 const bool ok = lw != kInf && cin && (j == L || m <= mlink[c2]);
-                at[(c * CT + c2) * KT] = ok ? V(lw >> 16) + xi + V(sm[sp.X + j * g.Cmax + c2]) : far;
+                const V val = V(lw >> 16) + xi + V(sm[sp.X + j * g.Cmax + c2]);
+                at[(c * CT + c2) * KT] = ok ? (kPack ? V((val << tb) | (V(m) & tmask)) : val) : far;
             }
         }
     };
@@ -675,6 +762,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
             const int p = rank + 1 + k * cs;
             V bv[CT][NA];   // running bests
             uint32_t bi[CT][NA];
+            V bv_keep[CT][NA];   // packed words: the bests before the bump of the last item
 #pragma unroll
             for (int c = 0; c < CT; c++)
 #pragma unroll
@@ -695,7 +783,7 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
                             const V v = m <= mlog ? a0[c * CT * KT] : far;
                             const bool take = v < bv[c][0];
                             bv[c][0] = take ? v : bv[c][0];
-                            bi[c][0] = take ? (uint32_t(L) << 8) | (uint32_t(m) << 4) : bi[c][0];
+                            bi[c][0] = take ? (uint32_t(L) << 8) | (kPack && tb ? 0u : uint32_t(m) << 4) : bi[c][0];
                         }
                     }
                 }
@@ -719,16 +807,27 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
 #pragma unroll
                         for (int c = 0; c < CT; c++)
 #pragma unroll
-                            for (int q = 0; q < NA; q++) bv[c][q] += bv[c][q] < cap ? 1 : 0;
+                            for (int q = 0; q < NA; q++) {
+                                if constexpr (kPack) {   // value + 1 with a clear tag: equal values win
+                                    bv_keep[c][q] = bv[c][q];
+                                    bv[c][q] = bv[c][q] < cap ? V((bv[c][q] | tmask) + 1) : bv[c][q];
+                                } else {
+                                    bv[c][q] += bv[c][q] < cap ? 1 : 0;
+                                }
+                            }
                     }
-                    relax_cut<CT, KT, NA, V>(Ak + j * sp.Aj, Hk + j * sp.Hrow, sp.Hcol, d, C, uint32_t(j) << 8, mwc,
-                                             bv, bi);
+                    relax_cut<CT, KT, NA, V, kPack>(Ak + j * sp.Aj, Hk + j * sp.Hrow, sp.Hcol, d, C, uint32_t(j) << 8, mwc,
+                                                    tmask, bv, bi);
                     if (last) {
 #pragma unroll
                         for (int c = 0; c < CT; c++)
 #pragma unroll
-                            for (int q = 0; q < NA; q++)   // bumped and not improved: undo
-                                bv[c][q] -= bi[c][q] != kNoArg && int(bi[c][q] >> 8) != i + 1 ? 1 : 0;
+                            for (int q = 0; q < NA; q++) {   // bumped and not improved: undo
+                                if constexpr (kPack)
+                                    bv[c][q] = int(bi[c][q] >> 8) == i + 1 ? bv[c][q] : bv_keep[c][q];
+                                else
+                                    bv[c][q] -= bi[c][q] != kNoArg && int(bi[c][q] >> 8) != i + 1 ? 1 : 0;
+                            }
                     }
                 }
             }
@@ -739,7 +838,29 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
                 key[c] = kInf;
 #pragma unroll
                 for (int q = 0; q < NA; q++) {
-                    const uint64_t kq = bv[c][q] < cap ? (uint64_t(bv[c][q]) << 24) | bi[c][q] : kInf;
+                    uint64_t kq;
+                    if constexpr (kPack) {
+                        // the width: the tag; with tb = 0 the last stage recorded it and a
+                        // cut point's best finds it again, the smallest width of that cut
+                        // point that reaches the value
+                        uint32_t mm = tb ? uint32_t(bv[c][q] & tmask) : (bi[c][q] >> 4) & 15u;
+                        if (!tb && p > 1 && bv[c][q] < cap) {
+                            const int jw = int(bi[c][q] >> 8);
+                            const V *aw = Ak + jw * sp.Aj + (c * CT + q) * KT;
+                            const V *hw = Hk + jw * sp.Hrow + q * sp.Hcol + d;
+#pragma unroll
+                            for (int m = KT - 1; m >= 0; m--) {
+                                if (m > mwc[q]) continue;
+                                const V hx = hw[-(1 << m)];
+                                mm = (aw[m] > hx ? aw[m] : hx) == bv[c][q] ? uint32_t(m) : mm;
+                            }
+                        }
+                        kq = bv[c][q] < cap ? (uint64_t(bv[c][q] >> tb) << 24) | (bi[c][q] & 0xFFFF00u) | (mm << 4) |
+                                                  uint32_t(q)
+                                            : kInf;
+                    } else {
+                        kq = bv[c][q] < cap ? (uint64_t(bv[c][q]) << 24) | bi[c][q] : kInf;
+                    }
                     key[c] = kq < key[c] ? kq : key[c];
                 }
             }
@@ -773,7 +894,8 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
                 if (dlive) {
                     sdv[so + at] = int64_t(kc >> 24);
                     sda[so + at] = uint32_t(kc & 0xFFFFFF);
-                    if (push) st_async_remote(rrow + uint32_t(ht * sizeof(V)), kc == kInf ? cap : V(kc >> 24), bar);
+                    if (push)
+                        st_async_remote(rrow + uint32_t(ht * sizeof(V)), kc == kInf ? cap : V(V(kc >> 24) << tb), bar);
                 }
                 if (d == 1) {
                     sdv[so + at - 1] = kCap;
@@ -819,23 +941,34 @@ __device__ __forceinline__ void resident_body(const PassArgs &a, PrepHdr *ph, in
     cluster_sync();
 }
 
-// Each (word width, graph) variant of the body: a called function for up to two
+// Each (word kind, graph) variant of the body: a called function for up to two
 // candidates, so that every variant gets its own register allocation (measured: 4 %
-// faster on the dense workload than all four inlined into the kernel), inlined for four
-// (called, those spill).
-template <int CT, int KT, typename V, bool kGraph>
+// faster on the dense workload than all variants inlined into the kernel), inlined for
+// three or four (called, those spill).
+template <int CT, int KT, typename V, bool kGraph, int kTag>
 __device__ __noinline__ void resident_body_call(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
                                                 volatile int &abort_flag) {
-    resident_body<CT, KT, V, kGraph>(a, ph, b, rank, sm, abort_flag);
+    resident_body<CT, KT, V, kGraph, kTag>(a, ph, b, rank, sm, abort_flag);
 }
 
-template <int CT, int KT, typename V, bool kGraph>
+// The body of an instance: 32-bit words are tagged for one or two candidates, with the
+// tag width chosen per instance for chains and fixed for graphs (measured: a third
+// 32-bit body in the kernel, even one never called, slows the others by 4 %).
+template <int CT, int KT, typename V>
 __device__ __forceinline__ void run_body(const PassArgs &a, PrepHdr *ph, int b, int rank, int64_t *sm,
                                          volatile int &abort_flag) {
-    if constexpr (CT <= 2)
-        resident_body_call<CT, KT, V, kGraph>(a, ph, b, rank, sm, abort_flag);
-    else
-        resident_body<CT, KT, V, kGraph>(a, ph, b, rank, sm, abort_flag);
+    constexpr bool tag = sizeof(V) == 4 && CT <= 2;
+    if constexpr (CT <= 2) {
+        if (ph->graph)
+            resident_body_call<CT, KT, V, true, tag ? 2 : 0>(a, ph, b, rank, sm, abort_flag);
+        else
+            resident_body_call<CT, KT, V, false, tag ? 1 : 0>(a, ph, b, rank, sm, abort_flag);
+    } else {
+        if (ph->graph)
+            resident_body<CT, KT, V, true, 0>(a, ph, b, rank, sm, abort_flag);
+        else
+            resident_body<CT, KT, V, false, 0>(a, ph, b, rank, sm, abort_flag);
+    }
 }
 
 // MAXT: the largest CTA the instantiation serves.  512 threads at 2 CTAs per SM leave
@@ -859,20 +992,14 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 3 : 2) sweep_resident_kern
         return;
     }
     // the word width is uniform over the cluster too: every CTA reads the same header;
-    // a launch for one width leaves the other width's instances to its companion launch
-    const bool narrow = narrow_words(ph);
+    // a launch for one width leaves the other width's instances to its companion launch.
+    // With one or two candidates the 32-bit words carry a width tag
+    const bool narrow = narrow_words(ph, CT <= 2 ? Packed<KT>::TB : 0);
     if ((a.word_mode == 1 && !narrow) || (a.word_mode == 2 && narrow)) return;
-    if (narrow) {
-        if (ph->graph)
-            run_body<CT, KT, uint32_t, true>(a, ph, b, rank, sm, abort_flag);
-        else
-            run_body<CT, KT, uint32_t, false>(a, ph, b, rank, sm, abort_flag);
-    } else {
-        if (ph->graph)
-            run_body<CT, KT, int64_t, true>(a, ph, b, rank, sm, abort_flag);
-        else
-            run_body<CT, KT, int64_t, false>(a, ph, b, rank, sm, abort_flag);
-    }
+    if (!narrow)
+        run_body<CT, KT, int64_t>(a, ph, b, rank, sm, abort_flag);
+    else
+        run_body<CT, KT, uint32_t>(a, ph, b, rank, sm, abort_flag);
     // the final reduction and the plan, by one warp of rank 0, once every CTA of the
     // cluster has written its dp rows (the cluster barrier at the end of the sweep);
     // other clusters' sweeps hide it.  Its indices are read again here so that nothing
@@ -913,8 +1040,6 @@ int launch_cluster(Kern fn, const PassArgs &a, void *stream, size_t smem, const 
 }
 
 // The resident variant is instantiated for 1, 2, 3 or 4 candidates and KT = 4, 8 or 16 widths.
-inline int kt_of(int Kmax) { return Kmax <= 4 ? 4 : Kmax <= 8 ? 8 : 16; }
-inline int ct_of(int Cmax) { return Cmax <= 3 ? Cmax : 4; }
 
 template <int CT, int KT, int MAXT>
 int resident_capacity_b(int cluster, int threads, size_t smem) {

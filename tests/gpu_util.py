@@ -84,14 +84,39 @@ def oracle_many(instances, fn=O.solve, threads=None):
         return list(ex.map(fn, instances))
 
 
-def narrow_words(inst):
-    """Whether the resident sweep takes its 32-bit value words for this instance: the
-    largest finite per-position load plus twice the largest link cost is below 2^30."""
+def word_tag_bits(instances):
+    """Tag bits of the resident sweep's 32-bit words for a batch: log2 of the widths its
+    kernels are instantiated for (4, 8 or 16) when the batch has at most two link
+    candidates (packed words), else 0 (plain words)."""
+    dims = nest.make_dims(instances)
+    kmax = int(dims.Dumax).bit_length()
+    kt = 4 if kmax <= 4 else 8 if kmax <= 8 else 16
+    return {4: 2, 8: 3, 16: 4}[kt] if dims.Cmax <= 2 else 0
+
+
+def value_bound(inst):
+    """The largest finite per-position load plus twice the largest link cost (each
+    saturated at 2^31 - 1), a bound of every finite value of the instance's DP."""
     lo = O.loads(inst)
     fin = lo[lo != np.uint64(2**64 - 1)]
     ml = int((fin >> U64(16)).max()) if fin.size else 0
     mx = int(np.max(O.links(inst)))
-    return min(ml, 2**31 - 1) + 2 * min(mx, 2**31 - 1) < 2**30
+    return min(ml, 2**31 - 1) + 2 * min(mx, 2**31 - 1)
+
+
+def packed_words(inst, tb):
+    """Whether the 32-bit words are packed with tb tag bits (tb > 0): the value bound
+    is below 2^(32 - tb) - 1."""
+    return tb > 0 and value_bound(inst) < 2**(32 - tb) - 1
+
+
+def narrow_words(inst, tb=0):
+    """Whether the resident sweep takes its 32-bit value words for this instance (tb:
+    the batch's tag bits): a chain below 2^30 (packed or plain), a graph only when its
+    words can be packed (or, with no tag bits, below 2^30)."""
+    if getattr(inst, "succ", None) is not None and tb:
+        return packed_words(inst, tb)
+    return value_bound(inst) < 2**30
 
 
 def scaled(inst, factor):

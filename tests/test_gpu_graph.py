@@ -103,6 +103,28 @@ def test_two_tower_wide_words(variant):
         assert G.same_graph_result(res[b], o), b
 
 
+def test_two_tower_word_kinds():
+    # graphs take packed 32-bit words or 64-bit words: values past 2^29 leave no room
+    # for the width tag, and plain 32-bit words are not instantiated for graphs.  The
+    # chain next to them takes plain 32-bit words at the same values (the width of each
+    # best found again at the end of a step)
+    chain = G.scaled(synth.config_instance(2, 1), 8)
+    insts = [synth.two_tower_instance(0), G.scaled(synth.two_tower_instance(1), 10),
+             G.scaled(synth.two_tower_instance(2), 64), chain]
+    tb = G.word_tag_bits(insts)
+    assert tb == 3
+    assert [G.packed_words(x, tb) for x in insts] == [True, False, False, False]
+    assert [G.narrow_words(x, tb) for x in insts] == [True, False, False, True]
+    for variant in (0, 1):
+        s, res = G.run(insts, variant=variant)
+        for b in range(3):
+            o = G.check_graph_tables(s, b, insts[b])
+            assert G.same_graph_result(res[b], o), (variant, b)
+        o = O.solve(chain, want_dp=True)
+        assert G.same_result(res[3], o), variant
+        np.testing.assert_array_equal(G.dp_keys(s, 3, chain), G.oracle_dp_keys(chain, o["dp"]))
+
+
 def test_chains_and_graphs_in_one_launch():
     insts = synth.config_batch(2, B=3) + [synth.two_tower_instance(b) for b in range(3)]
     insts[1].succ = synth.chain_succ(insts[1].L)

@@ -88,6 +88,56 @@ def test_workload2_wide_words(cluster, jsplit, variant):
         check_tables(s, b, insts[b])
 
 
+def test_packed_words_near_their_limit():
+    # two candidates and 64 device counts: 32-bit words packed with 3 tag bits, exact for
+    # values up to 2^29 - 2.  Flops scaled so that the value bounds lie at 0.71 and 0.91 x
+    # 2^29 (packed words, their top value bits in use), at 1.04 and 1.27 x 2^29 (plain
+    # 32-bit words: no room for the tag) and beyond 2^30 (64-bit words), all in one launch
+    base = synth.config_batch(2, B=5)
+    insts = [G.scaled(base[0], 7), G.scaled(base[1], 7), G.scaled(base[2], 7), G.scaled(base[3], 12),
+             G.scaled(base[4], 64)]
+    tb = G.word_tag_bits(insts)
+    assert tb == 3
+    assert [G.packed_words(x, tb) for x in insts] == [True, True, False, False, False]
+    assert [G.narrow_words(x) for x in insts] == [True, True, True, True, False]
+    assert G.value_bound(insts[1]) > 2**28 + 2**27
+    for variant in (0, 1):
+        s, res = G.run(insts, variant=variant)
+        oracle = G.oracle_many(insts)
+        for b in range(len(insts)):
+            assert G.same_result(res[b], oracle[b]), (variant, b)
+            check_tables(s, b, insts[b])
+
+
+def tagged_batch(n=90):
+    """Random instances with one or two link candidates (tagged 32-bit words), flops
+    scaled so that the value bounds spread over packed words, plain 32-bit words and
+    64-bit words."""
+    xs, k = [], 0
+    while len(xs) < n:
+        x = synth.random_tiny(31000 + k, Lmax=7, Dmax=16)
+        k += 1
+        if len(x.cand) <= 2 and G.value_bound(x) > 0:
+            xs.append(x)
+    targets = (0.3, 0.9, 1.3, 1.8, 2.5)   # x 2^29
+    return [G.scaled(x, max(1, round(targets[b % 5] * 2**29 / G.value_bound(x)))) for b, x in enumerate(xs)]
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_tagged_words_on_random_instances(variant):
+    insts = tagged_batch()
+    tb = G.word_tag_bits(insts)
+    kind = ["packed" if G.packed_words(x, tb) else "plain" if G.narrow_words(x) else "wide" for x in insts]
+    assert tb == 3 and min(kind.count(k) for k in ("packed", "plain", "wide")) >= 5
+    s, res = G.run(insts, Pcap=6, variant=variant)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), (b, kind[b])
+    for k in ("packed", "plain", "wide"):
+        for b in [b for b in range(len(insts)) if kind[b] == k][:4]:
+            check_tables(s, b, insts[b])
+
+
 def test_mixed_word_widths_in_one_launch():
     insts = synth.config_batch(2, B=6)
     for b in (1, 3, 4):
