@@ -548,16 +548,28 @@ def main():
         mhz = (clk or {}).get("sm_mhz") or peaks["sm_max_mhz"]
         derived = alu_peak_relax_per_s(peaks["sm_max_mhz"]) / 1e9
         achieved = relax_total / (dom_ms * 1e-3) / 1e9
-        meas = measured_relax_peak(0)
+        # batches with at most two link candidates run on tagged 32-bit words (one max and
+        # one min per candidate and cell), the others on plain ones (max, compare, two
+        # selects): the peak is measured on the op mix the sweep issues
+        # (a streaming sweep runs on 64-bit words)
+        streaming = plan.get("sweep_variant") == 2
+        tagged = max(len(x.cand) for x in instances) <= 2 and not streaming
+        mode = 1 if streaming else 2 if tagged else 0
+        meas = measured_relax_peak(mode)
+        meas_plain = measured_relax_peak(0) if mode else meas
         peak = meas / 1e9 if meas else derived
+        mix = ("tagged 32-bit words (one max and one min per candidate and cell)" if mode == 2 else
+               "64-bit words (max, compare, two selects per candidate and cell)" if mode == 1 else
+               "32-bit words (max, compare, two selects per candidate and cell)")
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Grelax/s",
                 "frac": achieved / peak, "traffic": stored_traffic(dom, workload), "kernel": dom,
-                "peak_source": ("measured: register-only microbenchmark of the relaxation arithmetic on 32-bit "
-                                "words (max, compare, two selects per candidate and cell; 4 independent chains "
-                                "per thread, every SM full) - the words this batch's sweep runs on"
+                "peak_source": (f"measured: register-only microbenchmark of the relaxation arithmetic on {mix}; "
+                                "4 independent chains per thread, every SM full - the words this batch's sweep "
+                                "runs on"
                                 if meas else
                                 f"derived: {SMS} SMs x {INT32_LANES} INT32 lanes x {peaks['sm_max_mhz']:.0f} MHz"
                                 f" / {OPS_PER_RELAX} ops per relaxation"),
+                "peak_plain_32bit": meas_plain / 1e9 if meas_plain else None,
                 "derived_64bit_peak": derived, "sm_mhz_seen": mhz}
     else:
         # the per-position loads table is what the stage-loads kernel must write

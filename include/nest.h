@@ -252,8 +252,10 @@ int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *
  * sweep shape follows the device's shared memory and occupancy, so call it with the
  * device current that will run the solve.  When the resident sweep sized for 32-bit
  * value words alone (instances whose largest load plus two link costs stays below
- * 2^30 ns) needs fewer waves than one sized for both widths, the sweep is split:
- * that launch takes the 32-bit instances and a second launch the others.
+ * 2^30 ns; for a graph instance in a batch of at most two link candidates, at most
+ * 2^(32 - b) - 2 ns, b = 2, 3 or 4 for up to 4, 8 or 16 widths) needs fewer waves than
+ * one sized for both widths, the sweep is split: that launch takes the 32-bit instances
+ * and a second launch the others.
  * Returns NEST_OK, NEST_E_INVALID (null pointer, bad option) or NEST_E_LIMITS. */
 typedef struct {
     int32_t chunks;             /* passes through the kernels */

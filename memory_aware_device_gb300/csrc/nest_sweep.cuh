@@ -363,10 +363,10 @@ __device__ __forceinline__ bool narrow_words(const PrepHdr *ph, int tb) {
 //    with Hrow = dpw / s (mod 32 / s) for values of s 4-byte words and dpw device
 //    counts per warp: those reads land in different banks.
 //  - A[buf][slot][j][c][c'][m] = load*(i, j, m, p) + X[i][c] + X[j][c'] when both
-//    links admit the width, else `far`.  With 32-bit values A[j] spans CT*CT*KT + 4
-//    values, so every (c, c') run of KT widths starts on 16 bytes (vector loads) and
-//    the lanes reading adjacent j start in different banks; with 64-bit values an odd
-//    number of values does the same for scalar loads.
+//    links admit the width, else `far`.  With tagged 32-bit values (one or two
+//    candidates) A[j] spans CT*CT*KT + 4 values, so every (c, c') run of KT widths
+//    starts on 16 bytes (vector loads) and the lanes reading adjacent j start in
+//    different banks; otherwise an odd number of values does the same for scalar loads.
 //  - staged dp rows [2][slot][Cmax][Dpad] (int64 values, uint32 arguments).
 //  - graph instances: the layer mask of every state, and per step parity the list of
 //    cut points j >= i + 2 whose state lies inside state i (8-bit state indices), its
@@ -412,7 +412,7 @@ __host__ __device__ inline ResPlan res_plan(const Geo &g, int nown, int jsplit, 
     const int h4 = (nown * g.Nmax * res_hrow(g, jsplit, 4) + 1) / 2, h8 = nown * g.Nmax * res_hrow(g, jsplit, 8);
     s.H = off;
     off = up(off + (mode == 1 ? h4 : mode == 2 ? h8 : h4 > h8 ? h4 : h8));
-    const int aj4 = CT * CT * KT + 4, aj8 = CT * CT * KT + 1;
+    const int aj4 = CT * CT * KT + (CT <= 2 ? 4 : 1), aj8 = CT * CT * KT + 1;
     s.Aj = vbytes == 4 ? aj4 : aj8;
     s.Aslot = (g.Nmax + 1) * s.Aj;
     s.Abuf = nown * s.Aslot;
