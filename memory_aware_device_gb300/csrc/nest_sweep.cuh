@@ -1,7 +1,8 @@
 // DP sweep (shared by nest_sweep.cu and the resident instantiations in
-// nest_sweep_res_a.cu and nest_sweep_res_b.cu): the backward min-max recurrence of Nest (Network- and Memory-Aware
-// Device Placement) §4 Eq. 3, one step per DP state i = L-1 .. 0 (the suffixes of a
-// chain, or the up-sets of a layer DAG; L is the last state, the empty set).
+// nest_sweep_res_a.cu and nest_sweep_res_b.cu): the backward min-max recurrence of
+// Nest (Network- and Memory-Aware Device Placement) §4 Eq. 3, one step per DP state
+// i = L-1 .. 0 (the suffixes of a chain, or the up-sets of a layer DAG; L is the last
+// state, the empty set).
 //
 //   dp[i][d][p][c] = min over j in (i, L], width unit * 2^m <= d units, next-link
 //                    candidate c' of  max(load*(i, j, m, p) + X[i][c] + X[j][c'],
@@ -27,8 +28,10 @@
 //    shared memory of the owner of p + 1 with st.async stores that complete on a
 //    per-row mbarrier, so the CTAs form a pipeline over positions and a step reads no
 //    dp data from global memory.  Value words are 32-bit when exact for the instance,
-//    else 64-bit; when shared memory sized for both widths would leave the batch in
-//    more waves, the sweep is two launches, one per width.  At the end each cluster's
+//    else 64-bit; with one or two candidates the 32-bit words carry the width index
+//    in their low bits (tagged: one max and one min per width).  When shared memory
+//    sized for both widths would leave the batch in more waves, the sweep is two
+//    launches, one per width.  At the end each cluster's
 //    rank 0 picks t_batch and walks the plan (the backtrack kernel is not needed).
 //  - streaming: rows dp[j > i][p-1] and the loads are staged from global memory by
 //    TMA bulk copies into double-buffered shared memory, tiles of `jc` cut points,
