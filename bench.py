@@ -187,6 +187,16 @@ def measured_relax_peak(wide: int = 0):
         return None
 
 
+def relax_peak_mode(instances, plan) -> int:
+    """Which relaxation peak the sweep's roofline divides by, as the microbenchmark's mode:
+    2 = tagged 32-bit words (batches of at most two link candidates: one max and one min
+    per candidate and cell), 0 = plain 32-bit words (max, compare, two selects), 1 = 64-bit
+    words (a streaming sweep runs on those)."""
+    if plan.get("sweep_variant") == 2:
+        return 1
+    return 2 if max(len(x.cand) for x in instances) <= 2 else 0
+
+
 def stored_traffic(kernel, workload):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -548,13 +558,8 @@ def main():
         mhz = (clk or {}).get("sm_mhz") or peaks["sm_max_mhz"]
         derived = alu_peak_relax_per_s(peaks["sm_max_mhz"]) / 1e9
         achieved = relax_total / (dom_ms * 1e-3) / 1e9
-        # batches with at most two link candidates run on tagged 32-bit words (one max and
-        # one min per candidate and cell), the others on plain ones (max, compare, two
-        # selects): the peak is measured on the op mix the sweep issues
-        # (a streaming sweep runs on 64-bit words)
-        streaming = plan.get("sweep_variant") == 2
-        tagged = max(len(x.cand) for x in instances) <= 2 and not streaming
-        mode = 1 if streaming else 2 if tagged else 0
+        # the peak is measured on the op mix the sweep issues
+        mode = relax_peak_mode(instances, plan)
         meas = measured_relax_peak(mode)
         meas_plain = measured_relax_peak(0) if mode else meas
         peak = meas / 1e9 if meas else derived

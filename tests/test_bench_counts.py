@@ -58,3 +58,15 @@ def test_workload_counts():
     x = synth.two_tower_instance(0)
     assert bench.relaxations(x) == 682205648 // 16
     assert bench.state_pairs(x) == 96 * 97 // 2
+
+
+def test_relax_peak_mode():
+    # the roofline divides by the peak of the words the sweep runs on
+    resident, streaming = {"sweep_variant": 1}, {"sweep_variant": 2}
+    dense = synth.config_batch(2, B=2)                       # two candidates: tagged words
+    torus = [synth.torus_instance(b) for b in range(2)]      # three candidates: plain words
+    assert len(dense[0].cand) == 2 and len(torus[0].cand) == 3
+    assert bench.relax_peak_mode(dense, resident) == 2
+    assert bench.relax_peak_mode(torus, resident) == 0
+    assert bench.relax_peak_mode(dense, streaming) == 1
+    assert bench.relax_peak_mode(dense + torus, resident) == 0
