@@ -562,7 +562,9 @@ def main():
         mode = relax_peak_mode(instances, plan)
         meas = measured_relax_peak(mode)
         meas_plain = measured_relax_peak(0) if mode else meas
-        peak = meas / 1e9 if meas else derived
+        # without the microbenchmark: INT32 lanes x clock / the mix's operations per relaxation
+        ops = {2: 2, 0: 4, 1: OPS_PER_RELAX}[mode]
+        peak = meas / 1e9 if meas else SMS * INT32_LANES * peaks["sm_max_mhz"] * 1e6 / ops / 1e9
         mix = ("tagged 32-bit words (one max and one min per candidate and cell)" if mode == 2 else
                "64-bit words (max, compare, two selects per candidate and cell)" if mode == 1 else
                "32-bit words (max, compare, two selects per candidate and cell)")
@@ -573,7 +575,7 @@ def main():
                                 "runs on"
                                 if meas else
                                 f"derived: {SMS} SMs x {INT32_LANES} INT32 lanes x {peaks['sm_max_mhz']:.0f} MHz"
-                                f" / {OPS_PER_RELAX} ops per relaxation"),
+                                f" / {ops} ops per relaxation ({mix})"),
                 "peak_plain_32bit": meas_plain / 1e9 if meas_plain else None,
                 "derived_64bit_peak": derived, "sm_mhz_seen": mhz}
     else:
