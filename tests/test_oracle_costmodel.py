@@ -261,3 +261,80 @@ def test_standard_workloads_are_valid():
         for b in (0, 1):
             if b < synth.CONFIG_BATCH[cfg]:
                 assert O.validate(synth.config_instance(cfg, b)) == 0
+
+
+# ---- expert-parallel gradient sync and ZeRO-3 gathers, and the tiers of groups that
+# ---- sit inside a tensor-parallel group.  Two or three tiers with different links make
+# ---- the tier choice visible; a wrong group size (q instead of q / e) or tier changes
+# ---- every value below.
+
+EXP_TIERS = dict(G=(4, 8), bw=(10**7, 2 * 10**6), lat=(10, 700))   # tier(8) = 1: alpha 700, beta 2e6
+
+
+def test_expert_gradient_sync_over_the_expert_data_parallel_group():
+    # 8 devices, EP 2: the expert weights are data parallel over q / e = 4 replicas, and
+    # their gradients are synchronised within that group, on the tier of the whole stage
+    Pe = 16 * 10**6
+    strat = tuple((1, 1, 2, z, 0) for z in range(4))
+    inst = make(pe=Pe, moe=1, M=1, strat=strat, **EXP_TIERS)
+    n, We, alpha, beta = 4, Pe // 2, 700, 2 * 10**6
+    se = [O.terms(inst, 0, 1, 3, z)["se"] for z in range(4)]
+    assert se[0] == ring_allreduce(n, We, alpha, beta)        # no ZeRO: AllReduce
+    assert se[1] == se[2] == 2 * ring_gather(n, We, alpha, beta)   # ZeRO-1/2: ReduceScatter + AllGather
+    assert se[3] == ring_gather(n, We, alpha, beta)            # ZeRO-3: ReduceScatter only
+    # nothing dense to synchronise, and the sync is amortised over the M microbatches
+    t0 = O.terms(inst, 0, 1, 3, 0)
+    assert t0["sd"] == 0 and t0["tau"] == se[0]
+
+
+def test_expert_zero3_gathers_over_the_expert_data_parallel_group():
+    # ZeRO-3 gathers the expert shards (We / (q / e) each) before the forward and the
+    # backward pass of every MoE layer; the dense weights are gathered over all q replicas
+    Pd, Pe = 8 * 10**6, 16 * 10**6
+    inst = make(pd=Pd, pe=Pe, moe=1, M=1, strat=((1, 1, 2, 3, 0),), **EXP_TIERS)
+    q, qe, alpha, beta = 8, 4, 700, 2 * 10**6
+    Wd, We = Pd, Pe // 2
+    t = O.terms(inst, 0, 1, 3, 0)
+    dense = 2 * (q - 1) * alpha + F(q - 1, q) * 2 * Wd * 1000 / beta
+    expert = 2 * (qe - 1) * alpha + F(qe - 1, qe) * 2 * We * 1000 / beta
+    assert t["z3"] == dense + expert
+    assert t["sd"] == ring_gather(q, Wd, alpha, beta) and t["se"] == ring_gather(qe, We, alpha, beta)
+    assert t["tau"] == -(-t["z3"] // q) + t["sd"] + t["se"]
+    # ZeRO-3 memory: every shard over its own group
+    assert t["w"] == Wd // q + We // qe
+
+
+def test_context_parallel_priced_on_the_tier_of_tp_times_cp():
+    # TP 2 x CP 2: the CP pairs are inside a 4-device TP x CP group, so their gathers use
+    # the tier that holds 4 devices (tier 1), not the 2-device tier (tier 0) that TP uses
+    A = 8 * 10**6
+    tiers = dict(G=(2, 4, 8), bw=(8 * 10**6, 2 * 10**6, 10**6), lat=(10, 300, 5000))
+    inst = make(ao=A, strat=((2, 2, 1, 0, 0),), **tiers)
+    t = O.terms(inst, 0, 1, 2, 0)   # k = 4 = t cp, q = 1
+    assert t["cpc"] == 4 * ring_gather(2, A // 2, 300, 2 * 10**6)      # volume Ao / t per collective
+    assert t["tp"] == 4 * ring_allreduce(2, A // 2, 10, 8 * 10**6)     # volume Ao / cp per collective
+    assert t["tau"] == t["cpc"] + t["tp"]
+
+
+def test_expert_parallel_priced_on_the_tier_of_tp_times_cp_times_ep():
+    # TP 2 x EP 2 on 8 devices: each AllToAll group of 2 lies inside a 4-device TP x EP
+    # block, priced on the tier that holds 4 devices; the volume is split over t cp
+    V = 16 * 10**6
+    tiers = dict(G=(2, 4, 8), bw=(8 * 10**6, 2 * 10**6, 10**6), lat=(10, 300, 5000))
+    inst = make(a2a=V, moe=1, strat=((2, 1, 2, 0, 0),), **tiers)
+    t = O.terms(inst, 0, 1, 3, 0)   # k = 8, q = 4, q / e = 2
+    assert t["ep"] == 4 * ring_gather(2, V // 2, 300, 2 * 10**6)
+    assert t["tau"] == t["ep"] / 4
+
+
+def test_context_and_expert_groups_together():
+    # TP 1 x CP 2 x EP 2: CP on tier(2) = 0, EP on tier(4) = 1; with TP 2 both move up
+    A, V = 8 * 10**6, 16 * 10**6
+    tiers = dict(G=(2, 4, 8), bw=(8 * 10**6, 2 * 10**6, 10**6), lat=(10, 300, 5000))
+    inst = make(ao=A, a2a=V, moe=1, strat=((1, 2, 2, 0, 0), (2, 2, 2, 0, 0)), **tiers)
+    a = O.terms(inst, 0, 1, 3, 0)   # k = 8: q = 4
+    assert a["cpc"] == 4 * ring_gather(2, A, 10, 8 * 10**6)
+    assert a["ep"] == 4 * ring_gather(2, V // 2, 300, 2 * 10**6)
+    b = O.terms(inst, 0, 1, 3, 1)   # k = 8: t cp = 4, q = 2, e = 2
+    assert b["cpc"] == 4 * ring_gather(2, A // 2, 300, 2 * 10**6)
+    assert b["ep"] == 4 * ring_gather(2, V // 4, 5000, 10**6)
