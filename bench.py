@@ -84,6 +84,7 @@ def _count(x, with_strategies: bool) -> int:
     G = [int(x.tierG[c]) for c in x.cand]
     K = Du.bit_length()
     E, sizes, nested, moe_in = _pairs(x)
+    sizes = np.asarray(sizes)
     # strategies valid for a stage of width unit * 2^m, without / with a MoE layer
     nvalid = np.ones((K, 2), dtype=np.int64)
     if with_strategies:
@@ -102,21 +103,30 @@ def _count(x, with_strategies: bool) -> int:
             k = u << m
             w = nvalid[m][moe_in[i].astype(np.int64)]
             last = int(w[E])
-            inner = int(w[inner_j].sum())
-            nd = Du - (1 << m) + 1
             ncp = sum(1 for g in G if 2 * k <= g)
+            # position p >= 2 relaxes cut point j only when state j can still hold the
+            # p - 1 stages after it, and width 2^m only when d - 2^m >= p - 1 units remain
+            # for them: otherwise the successor cell dp[j][d - 2^m][p - 1] has no value
+            n_after = 0
+            for p in range(2, Pi + 1):
+                nd = Du - (1 << m) - (p - 1) + 1
+                if nd <= 0:
+                    break
+                n_after += nd * int(w[inner_j & (sizes >= p - 1)].sum())
             for c in range(1 if i == 0 else C):
                 if i > 0 and 2 * k > G[c]:
                     continue
-                tot += nd * (last + (Pi - 1) * inner * ncp)
+                tot += (Du - (1 << m) + 1) * last + n_after * ncp
     return tot
 
 
 def relaxations(x) -> int:
-    """Min-max transitions (j, m, c') the recurrence evaluates for one instance:
-    every cell (i, d, p, c) times its cut points j (states inside state i), widths
-    m <= log2 d allowed by the link tier, and next-link candidates c' allowed for
-    that width."""
+    """Min-max transitions (j, m, c') of the recurrence for one instance whose
+    successor cell can hold a value: every cell (i, d, p, c) times its cut points j
+    (states inside state i with at least p - 1 layers), widths 2^m <= d - (p - 1)
+    allowed by the link tier, and next-link candidates c' allowed for that width.
+    Transitions into successor cells that are empty by construction (too few layers
+    or device units left for the remaining p - 1 stages) are not counted."""
     return _count(x, False)
 
 

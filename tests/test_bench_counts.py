@@ -1,8 +1,11 @@
 """The benchmark's work counts against a direct loop over the recurrence's transitions.
 
 A relaxation is one (j, m, c') min-max transition of Eq. 3 (Nest §4) for one DP cell
-(i, d, p, c); with the strategy axis it is one (j, m, s, c') transition.  The bench
-counts them with vectorised sums; here every cell and transition is enumerated.
+(i, d, p, c) whose successor cell dp[j][d - 2^m][p - 1][c'] can hold a value (state j
+keeps at least p - 1 layers and d - 2^m >= p - 1 device units remain for the p - 1
+stages after the new one); with the strategy axis it is one (j, m, s, c') transition.
+The bench counts them with vectorised sums; here every cell and transition is
+enumerated.
 """
 import os
 import sys
@@ -29,9 +32,11 @@ def direct(x, with_strategies):
                     for j in range(i + 1, E + 1):
                         if st[j] & ~st[i] or (j == E) != (p == 1):
                             continue
+                        if bin(st[j]).count("1") < p - 1:   # too few layers left for p - 1 stages
+                            continue
                         for m in range(Du.bit_length()):
                             k = u << m
-                            if (1 << m) > d or (i > 0 and 2 * k > G[c]):
+                            if (1 << m) > d - (p - 1) or (i > 0 and 2 * k > G[c]):
                                 continue
                             ns = 1
                             if with_strategies:
@@ -54,9 +59,15 @@ def test_counts_match_a_direct_loop(seed):
 
 
 def test_workload_counts():
-    assert sum(bench.relaxations(x) for x in synth.config_batch(2)) == 95544528
+    # the (j, k, c') and (j, k, s, c') counts of the dense 32-layer workload (16 instances)
+    # and of the tiny 8-layer one, as the work-per-batch sizing gives them
+    batch = synth.config_batch(2)
+    assert sum(bench.relaxations(x) for x in batch) == 57229968
+    assert sum(bench.relaxations_with_strategies(x) for x in batch) == 394430160
+    tiny = synth.config_instance(1, 0)
+    assert (bench.relaxations(tiny), bench.relaxations_with_strategies(tiny)) == (1216, 4326)
     x = synth.two_tower_instance(0)
-    assert bench.relaxations(x) == 682205648 // 16
+    assert bench.relaxations(x) == direct(x, False)
     assert bench.state_pairs(x) == 96 * 97 // 2
 
 
