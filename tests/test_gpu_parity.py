@@ -5,8 +5,8 @@ exact equality: the stage-cost words (cost builder), the per-position strategy
 loads (reduction), every DP cell key (sweep), and the batch time, bottleneck and
 plan (backtrack).  Workloads 1, 2 and 4 are compared in full; workload 3 on its
 full batch with every result checked and two instances' tables checked cell by
-cell; workload 5 at its full size (1024 instances, chunked as the benchmark runs
-it) on sampled instances.
+cell; workload 5 at its full size (1024 instances, chunked) on every result, against
+the oracle's stored results, and two instances' tables.
 """
 import numpy as np
 import pytest
@@ -235,18 +235,52 @@ def test_workload4_full_batch():
         check_tables(s, b, insts[b])
 
 
-def test_workload5_full_size_sampled():
-    """All 1024 instances solved in chunks of 152; sampled instances against the oracle."""
+def _golden5():
+    import importlib.util
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "make_workload5_results.py")
+    spec = importlib.util.spec_from_file_location("make_workload5_results", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.fixture(scope="module")
+def workload5():
+    """The 1024 instances of the mixed-128L workload, the oracle's stored results for
+    them (tests/golden/workload5_results.txt, written by the oracle alone), and the
+    oracle's tables of two instances of the last chunk of 152."""
+    mod = _golden5()
     insts = synth.config_batch(5)
-    s, res = G.run(insts, chunk=152)
-    assert all(r["status"] in (nest.SOLVED, nest.INFEASIBLE) for r in res)
-    sample = [0, 511, 1023]
-    oracle = G.oracle_many([insts[b] for b in sample])
-    for b, o in zip(sample, oracle):
-        assert G.same_result(res[b], o), b
-    # the last chunk's tables are still in the workspace: check one of its instances
+    gold = mod.parse()
+    assert sorted(gold) == list(range(1024))
+    for b, x in enumerate(insts):   # the generator still draws the inputs the file was written for
+        assert gold[b][0] == mod.fingerprint(x), b
     last0 = (1024 // 152) * 152
-    np.testing.assert_array_equal(G.cost_table(s, 1023 - last0, insts[1023]), O.cost_tensor(insts[1023]))
+    tables = {}
+    for b in (last0, 1023):
+        o = O.solve(insts[b], want_dp=True)
+        tables[b] = (O.cost_tensor(insts[b]), O.loads(insts[b]), G.oracle_dp_keys(insts[b], o["dp"]))
+    return insts, gold, tables, last0
+
+
+@pytest.mark.parametrize("variant", [0, 2])
+def test_workload5_full_size_all_instances(workload5, variant):
+    """All 1024 instances solved in chunks of 152 (the library's sweep choice, and the
+    streaming variant): every status, t_batch, bottleneck and plan against the oracle's
+    stored results, and every table (stage-cost words, per-position loads, DP keys) of
+    two instances against the oracle."""
+    insts, gold, tables, last0 = workload5
+    s, res = G.run(insts, chunk=152, variant=variant)
+    for b in range(1024):
+        _, st, t, v, plan = gold[b]
+        assert (res[b]["status"], res[b]["t_batch"]) == (st, t), (b, res[b])
+        if st == 0:
+            assert res[b]["bottleneck"] == v and res[b]["plan"] == plan, (b, res[b])
+    for b, (cost, loads, keys) in tables.items():
+        np.testing.assert_array_equal(G.cost_table(s, b - last0, insts[b]), cost)
+        np.testing.assert_array_equal(G.loads_table(s, b - last0, insts[b]), loads)
+        np.testing.assert_array_equal(G.dp_keys(s, b - last0, insts[b]), keys)
 
 
 @pytest.mark.parametrize("part,variant,factor", [(0, 0, 1), (1, 1, 1), (2, 2, 1), (3, 1, 1), (4, 1, 1 << 20)])
