@@ -202,6 +202,8 @@ def relax_peak_mode(instances, plan) -> int:
     2 = tagged 32-bit words (batches of at most two link candidates: one max and one min
     per candidate and cell), 0 = plain 32-bit words (max, compare, two selects), 1 = 64-bit
     words (a streaming sweep runs on those)."""
+    if plan.get("sweep_variant") == 3:
+        return 2   # layered: tagged 32-bit words, one max and one min per pair and cell
     if plan.get("sweep_variant") == 2:
         return 1
     return 2 if max(len(x.cand) for x in instances) <= 2 else 0
@@ -355,6 +357,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--sweep-variant", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="DP sweep variant: 0 = the library's choice, 1 = resident, 2 = streaming, "
+                         "3 = layered (one launch per pipeline position)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -432,7 +437,7 @@ def main():
         # their programmatic dependent launches)
         ev = [torch.cuda.Event(enable_timing=True) if only is None or q % NEV in (only, only + 1) else None
               for q in range(NEV * nchunks)]
-        return nest.options(chunk=args.chunk, events=ev), ev
+        return nest.options(chunk=args.chunk, events=ev, variant=args.sweep_variant), ev
 
     def kernel_ms(opts):   # average ms per step of each kernel, over all chunks
         out = {k: 0.0 for k in KERNELS}
@@ -477,10 +482,10 @@ def main():
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            step(nest.options(chunk=args.chunk), side)
+            step(nest.options(chunk=args.chunk, variant=args.sweep_variant), side)
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=side):
-                step(nest.options(chunk=args.chunk), side)
+                step(nest.options(chunk=args.chunk, variant=args.sweep_variant), side)
         stream.wait_stream(side)
         torch.cuda.synchronize(dev)
 
@@ -516,7 +521,7 @@ def main():
     ms_per_step = total_ms / args.steps
     value = job_relax / (ms_per_step * 1e-3)
     solves = B * ws / (ms_per_step * 1e-3)
-    plan = nest.describe_launch(dims, nest.options(chunk=args.chunk))
+    plan = nest.describe_launch(dims, nest.options(chunk=args.chunk, variant=args.sweep_variant))
     launches = (plan["kernels_per_chunk"] * plan["chunks"] + (1 if group > 1 else 0)) * args.steps
 
     # end to end through the host-buffer entry point: H2D records, solve, D2H results
@@ -525,7 +530,7 @@ def main():
     rec_pin = torch.from_numpy(records.ravel().copy()).pin_memory()
     costs_pin = torch.empty(B, dtype=torch.int64).pin_memory()
     plans_pin = torch.empty(B * nest.plan_bytes(dims), dtype=torch.uint8).pin_memory()
-    hopt = nest.options(chunk=args.chunk)
+    hopt = nest.options(chunk=args.chunk, variant=args.sweep_variant)
 
     best_pin = torch.empty(max(B // group, 1), dtype=torch.int32).pin_memory()
 

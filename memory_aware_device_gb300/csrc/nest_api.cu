@@ -106,8 +106,11 @@ int nest_describe_launch(const nest_dims *dims, const nest_options *opt, nest_la
     // prep, stage loads, the sweep (two launches when split), and the backtrack unless
     // every sweep launch is resident (their clusters write the plans)
     const bool fuse = cfg.resident && (!cfg.split || cfg.wide.resident);
-    out->kernels_per_chunk = 3 + (cfg.split ? 1 : 0) + (fuse ? 0 : 1);
-    out->sweep_variant = cfg.resident ? 1 : 2;
+    // the layered sweep: position 1, one launch per later position, the streaming launch
+    // for the instances beyond its words
+    const int sweep_launches = cfg.layered ? g.Pcap + 1 : 1 + (cfg.split ? 1 : 0);
+    out->kernels_per_chunk = 2 + sweep_launches + (fuse ? 0 : 1);
+    out->sweep_variant = cfg.layered ? 3 : cfg.resident ? 1 : 2;
     out->sweep_cluster = cfg.cluster;
     out->sweep_jsplit = cfg.jsplit;
     out->sweep_threads = cfg.threads;
@@ -124,6 +127,13 @@ int nest_describe_launch(const nest_dims *dims, const nest_options *opt, nest_la
 // The DP sweep of one pass: one launch, or the 32-bit-word launch followed by the
 // 64-bit-word one (each leaves the other's instances alone).
 static int sweep_pass(PassArgs a, const SweepConfig &cfg, void *stream) {
+    if (cfg.layered) {
+        // the layered launches, then the streaming variant for the instances whose values
+        // do not fit their words (its CTAs for the others exit at once)
+        if (int rc = launch_layered(a, stream)) return rc;
+        a.word_mode = 3;
+        return launch_sweep(a, stream);
+    }
     if (!cfg.split) {
         a.word_mode = 0;
         return launch_sweep(a, stream);

@@ -29,6 +29,8 @@ struct Geo {
     int32_t Kpad;  // Kmax rounded up to even (16-byte rows)
     int32_t Spad;  // Smax rounded up to even
     int32_t Dpad;  // Dumax + 1 rounded up to a multiple of 4 (rows of 16-byte multiples)
+    int32_t Dx;    // Dumax rounded up to a multiple of 4 (32-bit rows of device counts 1 .. Dx)
+    int32_t pad_;
 };
 
 inline bool make_geo(const nest_dims &d, Geo &g) {
@@ -52,6 +54,8 @@ inline bool make_geo(const nest_dims &d, Geo &g) {
     g.Kpad = (K + 1) & ~1;
     g.Spad = (d.Smax + 1) & ~1;
     g.Dpad = (d.Dumax + 4) & ~3;
+    g.Dx = (d.Dumax + 3) & ~3;
+    g.pad_ = 0;
     return true;
 }
 
@@ -90,6 +94,9 @@ struct PrepHdr {
     int32_t schedule;    // 0 = 1F1B, 1 = GPipe
     int32_t graph;       // 0 = chain, 1 = states are the up-sets of a layer DAG
     int32_t layers;      // layers of the instance
+    int32_t lay_sat;     // the layered sweep met a value beyond its 32-bit words (the
+                         // streaming sweep then solves the instance again)
+    int32_t lay_pad[3];
     int64_t R, M, budget, opt;
     int64_t G[8], bw[8], lat[8];
     int32_t cand[16];
@@ -133,8 +140,8 @@ __host__ __device__ inline PrepLayout prep_layout(const Geo &g) {
 
 // Workspace regions for passes of `ch` instances.
 struct WsLayout {
-    int64_t prep, loads, dpv, dpa, total, cost, total_costs;
-    int64_t prep_stride, cost_stride, loads_stride, dp_stride;  // per instance (elements for tables)
+    int64_t prep, loads, dpv, dpa, dp32, total, cost, total_costs;
+    int64_t prep_stride, cost_stride, loads_stride, dp_stride, dp32_stride;  // per instance (elements for tables)
 };
 
 __host__ __device__ inline WsLayout ws_layout(const Geo &g, int64_t ch) {
@@ -144,6 +151,7 @@ __host__ __device__ inline WsLayout ws_layout(const Geo &g, int64_t ch) {
     w.cost_stride = int64_t(g.NP) * g.Kmax * g.Spad;            // uint64 words
     w.loads_stride = int64_t(g.Pcap) * g.NP * g.Kpad;           // uint64 words
     w.dp_stride = int64_t(g.Pcap) * g.Nmax * g.Cmax * g.Dpad;   // cells
+    w.dp32_stride = int64_t(g.Pcap) * g.Nmax * g.Cmax * g.Dx;   // 32-bit words (layered sweep)
     int64_t off = 0;
     w.prep = off;
     off = align_up(off + ch * w.prep_stride, 256);
@@ -153,6 +161,8 @@ __host__ __device__ inline WsLayout ws_layout(const Geo &g, int64_t ch) {
     off = align_up(off + ch * w.dp_stride * 8, 256);
     w.dpa = off;
     off = align_up(off + ch * w.dp_stride * 4, 256);
+    w.dp32 = off;
+    off = align_up(off + ch * w.dp32_stride * 4, 256);
     w.total = off;
     w.cost = off;   // only with NEST_KEEP_COSTS
     off = align_up(off + ch * w.cost_stride * 8, 256);
@@ -191,7 +201,8 @@ struct PassArgs {
     int64_t spin_limit;            // polls per bounded wait (negative: give up at once)
     int32_t keep_costs;            // also write the stage-cost tensor
     int32_t word_mode;             // sweep launch takes: 0 every instance, 1 those on 32-bit
-                                   // words only, 2 those on 64-bit words only
+                                   // words only, 2 those on 64-bit words only, 3 (streaming)
+                                   // those the layered sweep leaves (values beyond its words)
     int32_t fuse_walk;             // resident sweep: rank 0 of each cluster also writes the plan
                                    // (the final reduction and backtrack), no backtrack launch
     int32_t pad;
@@ -245,12 +256,15 @@ int launch_prep(const PassArgs &a, void *stream);
 int launch_loads(const PassArgs &a, void *stream);
 int launch_sweep(const PassArgs &a, void *stream);
 int launch_backtrack(const PassArgs &a, void *stream);
+// The layered sweep (nest_layered.cu): position 1, then one launch per position 2 .. Pcap.
+int launch_layered(const PassArgs &a, void *stream);
+int64_t layered_smem_bytes(const Geo &g);
 // Dynamic shared memory of the streaming and resident sweep variants.
 int64_t sweep_smem_bytes(const Geo &g, int jc, int jsplit, int threads);
 int64_t sweep_resident_smem_bytes(const Geo &g, int cluster, int jsplit, int threads, int mode);
 
 // Launch shape of the DP sweep for passes of n instances.  cluster_opt / jsplit_opt
-// (0 = choose) and variant (0 = choose, 1 = resident, 2 = streaming) come from
+// (0 = choose) and variant (0 = choose, 1 = resident, 2 = streaming, 3 = layered) come from
 // nest_options.  With split set, the sweep is two launches: the resident shape above
 // sized for the instances on 32-bit words alone (word_mode 1), then `wide` for those
 // on 64-bit words (word_mode 2).  Returns NEST_OK, NEST_E_INVALID or NEST_E_LIMITS.
@@ -261,6 +275,7 @@ struct SweepConfig {
     int cluster, jsplit, jc, threads, resident, resident_waves;
     int split;
     SweepShape wide;
+    int layered;   // 1: the layered sweep, then the streaming shape above for the instances it leaves
 };
 int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int variant, SweepConfig &out);
 

@@ -332,6 +332,7 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
         ph->L = E;
         ph->maxX32 = xmax;
         ph->maxload32 = 0;   // raised by the strategy reduction
+        ph->lay_sat = 0;
         ph->status = NEST_SOLVED;
     }
 }

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) sweep_stream_kernel(PassArgs a
     PrepHdr *ph = prep_hdr(a, b);
     if (ph->status != NEST_SOLVED) return;  // uniform over the cluster
     if (a.word_mode == 2 && narrow_words(ph, word_tag_bits(g.Kmax, g.Cmax))) return;   // taken by the resident launch
+    if (a.word_mode == 3 && !lay_leaves(ph)) return;   // solved by the layered sweep
     const Inst s = load_inst(a, ph, b);
     const StreamPlan sp = stream_plan(g, a.jc, a.jsplit, a.threads);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + sp.mbar);
@@ -234,6 +235,18 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
     auto ok_cluster = [](int c) { return c == 1 || c == 2 || c == 4 || c == 8 || c == 16; };
     auto ok_jsplit = [](int j) { return j == 1 || j == 2 || j == 4 || j == 8; };
     if ((cluster_opt && !ok_cluster(cluster_opt)) || (jsplit_opt && !ok_jsplit(jsplit_opt))) return NEST_E_INVALID;
+    if (variant < 0 || variant > 3) return NEST_E_INVALID;
+    // layered: one launch per position over every instance's cells (up to four link
+    // candidates, 32-bit tagged words); the streaming shape takes the instances whose
+    // values do not fit those words
+    auto layered = [&]() {
+        if (g.Cmax > 4 || layered_smem_bytes(g) > budget) return int(NEST_E_LIMITS);
+        SweepShape sh;
+        if (int rc = stream_shape(g, n, cluster_opt, jsplit_opt, sms, budget, sh)) return rc;
+        out = {sh.cluster, sh.jsplit, sh.jc, sh.threads, 0, 1, 0, {}, 1};
+        return int(NEST_OK);
+    };
+    if (variant == 3) return layered();
 
     // resident: one thread per (device count, slice) holding every candidate, the
     // slices of a device count in adjacent lanes, and up to ngrp such groups per CTA
@@ -347,9 +360,10 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
         }
         if (variant == 1) return NEST_E_LIMITS;
     }
+    if (variant == 0 && layered() == NEST_OK) return NEST_OK;
     SweepShape sh;
     if (int rc = stream_shape(g, n, cluster_opt, jsplit_opt, sms, budget, sh)) return rc;
-    out = {sh.cluster, sh.jsplit, sh.jc, sh.threads, 0, 1, 0, {}};
+    out = {sh.cluster, sh.jsplit, sh.jc, sh.threads, 0, 1, 0, {}, 0};
     return NEST_OK;
 }
 

@@ -136,6 +136,39 @@ __device__ __forceinline__ uint32_t cluster_map(const void *local, uint32_t rank
     return r;
 }
 
+// The 32-bit words of an instance on the layered sweep (nest_layered.cu): a value v is
+// held as (v << tb) | tag; values 0 .. vmax are exact, vmax + 1 ("sat") stands for any
+// larger finite value, and all value bits set for no value.
+struct LayWords {
+    bool ok;         // the instance takes the layered sweep
+    bool fits;       // its value bound (largest load plus two link costs) is at most vmax,
+                     // so no word saturates
+    int tb;          // tag bits
+    uint32_t nmask;  // value bits of a word
+    uint32_t vmax;   // largest exact value
+};
+
+// tb = log2 of the number of (m, c') pairs a row block can admit (at most those of the
+// first stage, which has no input link: every width up to the next link's tier).
+__device__ __forceinline__ LayWords lay_words(const PrepHdr *ph) {
+    int E = 0;
+    for (int c = 0; c < ph->C && c < 16; c++)
+        if (ph->mlim[c] >= 0) E += (ph->mlim[c] < ph->K - 1 ? ph->mlim[c] : ph->K - 1) + 1;
+    int tb = 1;
+    while ((1 << tb) < E) tb++;
+    LayWords w;
+    w.tb = tb;
+    w.nmask = ~((1u << tb) - 1u);
+    w.vmax = (1u << (32 - tb)) - 3u;
+    w.ok = ph->C <= 4;
+    w.fits = uint64_t(ph->maxload32) + 2 * uint64_t(ph->maxX32) <= uint64_t(w.vmax);
+    return w;
+}
+
+// Whether the layered sweep leaves the instance to the 64-bit streaming sweep: more
+// than four candidates, or a value beyond its words met in some cell.
+__device__ __forceinline__ bool lay_leaves(const PrepHdr *ph) { return !lay_words(ph).ok || ph->lay_sat != 0; }
+
 // ---------------------------------------------------------------------------------
 // The relaxation of one cut point j for the cells (c, d) of one thread
 // ---------------------------------------------------------------------------------

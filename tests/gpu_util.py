@@ -153,3 +153,27 @@ def same_graph_result(g, o):
         return False
     st = o["states"]
     return g["status"] != 0 or g["layers"] == [int(st[i]) & ~int(st[j]) for i, j, *_ in o["plan"]]
+
+
+def layered_tag_bits(inst):
+    """Tag bits of the layered sweep's 32-bit words for an instance: log2 of the (m, c')
+    pairs its first stage admits (every width up to each next-link candidate's tier)."""
+    Du = inst.D // inst.unit
+    K = Du.bit_length()
+    E = 0
+    for c in inst.cand:
+        G = int(inst.tierG[int(c)])
+        ml = max((m for m in range(16) if 2 * (int(inst.unit) << m) <= G), default=-1)
+        if ml >= 0:
+            E += min(ml, K - 1) + 1
+    tb = 1
+    while (1 << tb) < E:
+        tb += 1
+    return tb
+
+
+def layered_words(inst):
+    """Whether the layered sweep holds the instance on its 32-bit words: at most four
+    candidates and a value bound of at most 2^(32 - tb) - 2."""
+    tb = layered_tag_bits(inst)
+    return len(inst.cand) <= 4 and value_bound(inst) <= 2**(32 - tb) - 2

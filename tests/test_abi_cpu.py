@@ -146,11 +146,18 @@ def test_cost_tensor_sizes_match_workload_table():
 
 
 def test_describe_launch_without_a_device():
-    # no GPU here: the shape falls back to the streaming sweep, followed by the backtrack
+    # no GPU here: no resident shape can be sized, so the shape falls back to the layered
+    # sweep (position 1, one launch per later position, the streaming launch for the
+    # instances beyond its words), followed by the backtrack
     dims = nest.make_dims(synth.config_batch(2, B=4))
     d = nest.describe_launch(dims)
-    assert d["chunks"] == 1 and d["sweep_variant"] in (1, 2)
-    assert d["kernels_per_chunk"] == (3 if d["sweep_variant"] == 1 else 4) + d["sweep_split"]
+    assert d["chunks"] == 1 and d["sweep_variant"] in (1, 2, 3)
+    per = {1: 3 + d["sweep_split"], 2: 4 + d["sweep_split"], 3: 2 + dims.Pcap + 1 + 1}
+    assert d["kernels_per_chunk"] == per[d["sweep_variant"]]
+    for v in (2, 3):
+        assert nest.describe_launch(dims, nest.options(variant=v))["sweep_variant"] == v
+    with pytest.raises(nest.NestError):
+        nest.describe_launch(dims, nest.options(variant=4))
     assert nest.describe_launch(dims, nest.options(chunk=3))["chunks"] == 2
     bad = nest.Dims(B=1, Lmax=256, Tmax=1, Cmax=1, Smax=1, Pcap=1, Dumax=1)
     with pytest.raises(nest.NestError):
