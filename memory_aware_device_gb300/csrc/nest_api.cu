@@ -106,9 +106,9 @@ int nest_describe_launch(const nest_dims *dims, const nest_options *opt, nest_la
     // prep, stage loads, the sweep (two launches when split), and the backtrack unless
     // every sweep launch is resident (their clusters write the plans)
     const bool fuse = cfg.resident && (!cfg.split || cfg.wide.resident);
-    // the layered sweep: position 1, one launch per later position, the streaming launch
-    // for the instances beyond its words
-    const int sweep_launches = cfg.layered ? g.Pcap + 1 : 1 + (cfg.split ? 1 : 0);
+    // the layered sweep: position 1, two launches (rank and width tags) per later
+    // position, the streaming launch for the instances beyond its words
+    const int sweep_launches = cfg.layered ? 1 + 2 * (g.Pcap - 1) + 1 : 1 + (cfg.split ? 1 : 0);
     out->kernels_per_chunk = 2 + sweep_launches + (fuse ? 0 : 1);
     out->sweep_variant = cfg.layered ? 3 : cfg.resident ? 1 : 2;
     out->sweep_cluster = cfg.cluster;

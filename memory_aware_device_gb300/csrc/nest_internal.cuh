@@ -96,7 +96,9 @@ struct PrepHdr {
     int32_t layers;      // layers of the instance
     int32_t lay_sat;     // the layered sweep met a value beyond its 32-bit words (the
                          // streaming sweep then solves the instance again)
-    int32_t lay_pad[3];
+    int32_t ngrp;        // strategy groups: runs of equal (t, cp, e) in the sorted strategy list
+    int32_t ngd;         // dense groups: runs of equal (t, cp), each a run of strategy groups
+    int32_t lay_pad;
     int64_t R, M, budget, opt;
     int64_t G[8], bw[8], lat[8];
     int32_t cand[16];
@@ -116,6 +118,9 @@ struct PrepLayout {
     int64_t awst;   // int64 [kLogL][Lmax] sparse table of max(aw)
     int64_t X;      // int64 [Nmax + 1][Cmax] link cost into each state per candidate
     int64_t strat;  // uint32 [Smax] packed log2 t | log2 cp << 4 | log2 e << 8 | z << 12 | r << 14
+    int64_t ssort;  // uint32 [Smax] the codes sorted by (t, cp, e, z, r, s), each | s << 16
+    int64_t sgrp;   // uint32 [Smax + 1] start of each strategy group in ssort (ngrp + 1 entries)
+    int64_t sgd;    // uint32 [Smax + 1] first strategy group of each dense group (ngd + 1 entries)
     int64_t bytes;
 };
 
@@ -134,6 +139,12 @@ __host__ __device__ inline PrepLayout prep_layout(const Geo &g) {
     off += 8 * int64_t(g.Nmax + 1) * g.Cmax;
     p.strat = off;
     off += 4 * int64_t(g.Smax);
+    p.ssort = off;
+    off += 4 * int64_t(g.Smax);
+    p.sgrp = off;
+    off += 4 * int64_t(g.Smax + 1);
+    p.sgd = off;
+    off += 4 * int64_t(g.Smax + 1);
     p.bytes = align_up(off, 256);
     return p;
 }

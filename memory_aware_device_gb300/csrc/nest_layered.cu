@@ -12,20 +12,23 @@
 // index (j, m, c'), where the A operand load*(i, j, m, p) + X[i][c] + X[j][c'] does
 // not depend on d and the B operand dp[j][d - 2^m][p-1][c'] is row (j, c') of the
 // previous position shifted by 2^m.  It is tiled like a matrix product:
-//  - a CTA owns eight consecutive states i and one input candidate c (a "row block"),
-//    and every device count d of them; a thread owns the 8 x 4 cells (i0..i0+7,
-//    4t+1..4t+4), so each A word is shared by 4 cells and each B word by 8;
+//  - a CTA owns RT consecutive states i and one input candidate c (a "row block"),
+//    and every device count d of them; a thread owns the RT x 4 cells (i0..i0+RT-1,
+//    4t+1..4t+4), so each A word is shared by 4 cells and each B word by RT;
 //  - the cut points j are streamed through double-buffered shared memory: the B rows
 //    (j, c') of the previous position by bulk copies (cp.async.bulk, completing on an
-//    mbarrier), the A words of (i0..i0+7, j) built by the CTA's threads from the
+//    mbarrier), the A words of (i0..i0+RT-1, j) built by the CTA's threads from the
 //    per-position loads table, whose global loads are issued one cut point ahead;
-//  - all words are 32-bit and tagged: a finite value v is held as (v << tb) | e, where
-//    e is the rank of (m, c') among the row block's admissible pairs in (m, c') order.
-//    The maximum of two words with the same tag keeps the tag, so the minimum over
-//    (m, c') of max(A, B) is one unsigned max and one unsigned min per cell and pair,
-//    and orders equal values by (m, c') as the packed key (v, j, m, c') does.  Across
-//    cut points (visited in increasing j) a later one wins only with a strictly smaller
-//    value, so each cell keeps its best word and its cut point.
+//  - all words are 32-bit and tagged: a finite value v is held as (v << tb) | tag, and
+//    the maximum of two words with the same tag keeps the tag.  With rank tags (RT = 8)
+//    the tag is the rank of (m, c') among the row block's admissible pairs in (m, c')
+//    order, so the minimum over (m, c') of max(A, B) is one unsigned max and one min
+//    per cell and pair and orders equal values as the packed key (v, j, m, c') does.
+//    With width tags (RT = 4, for instances whose values need more bits) the tag is m:
+//    the minimum over m orders (v, m), the next-link candidates c' are visited in
+//    increasing order and one replaces the cut point's best only when strictly smaller.
+//    Across cut points (visited in increasing j) a later one wins only with a strictly
+//    smaller value, so each cell keeps its best word and its cut point (and c').
 // Values up to vmax = 2^(32 - tb) - 3 are exact.  A larger finite value saturates to
 // vmax + 1: it can neither win nor tie against an exact value, so every cell whose
 // optimum is at most vmax still gets its exact key, and a cell whose optimum is
@@ -41,7 +44,6 @@ namespace nest {
 
 namespace {
 
-constexpr int kLRows = 8;      // states i per thread (a row block)
 constexpr int kLCols = 4;      // device counts per thread
 constexpr int kLMaxThreads = 128;
 
@@ -56,14 +58,14 @@ struct LayPlan {
     int64_t mbar, X, rk, dec, A, B, total;
 };
 
-__host__ __device__ inline LayPlan lay_plan(const Geo &g, int CT) {
+__host__ __device__ inline LayPlan lay_plan(const Geo &g, int CT, int RT) {
     LayPlan s;
     s.NT = ((g.Dumax + kLCols - 1) / kLCols + 31) / 32 * 32;
     s.Dx = g.Dx;
     s.XOFF = (((1 << (g.Kmax - 1)) + 3) & ~3) + 3;
     s.ROWW = (s.XOFF + kLCols * s.NT + 1 + 3) & ~3;
     s.Emax = CT * g.Kmax;
-    s.NIB = (g.Nmax - 1 + kLRows - 1) / kLRows;
+    s.NIB = (g.Nmax - 1 + RT - 1) / RT;
     int64_t off = 0;
     s.mbar = off;
     off += 16;
@@ -73,18 +75,18 @@ __host__ __device__ inline LayPlan lay_plan(const Geo &g, int CT) {
     off += 4 * 16 * CT;
     s.dec = off;                         // int32 [Emax]: (m << 4) | c'
     off = align_up(off + 4 * int64_t(s.Emax), 16);
-    s.A = off;                           // uint32 [2][Emax][8]
-    off += 2 * 4 * int64_t(s.Emax) * kLRows;
+    s.A = off;                           // uint32 [2][Emax][RT]
+    off += 2 * 4 * int64_t(s.Emax) * RT;
     s.B = off;                           // uint32 [2][CT][ROWW]
     off += 2 * 4 * int64_t(CT) * s.ROWW;
     s.total = align_up(off, 128);
     return s;
 }
 
-// Row blocks per instance: the first stage (state 0, no input link), then 8-state
+// Row blocks per instance: the first stage (state 0, no input link), then RT-state
 // blocks of states 1 .. Nmax-1 for each input candidate, the blocks with the most cut
 // points first.
-__host__ __device__ inline int lay_blocks(const Geo &g, int CT) { return 1 + lay_plan(g, CT).NIB * CT; }
+__host__ __device__ inline int lay_blocks(const Geo &g, int CT, int RT) { return 1 + lay_plan(g, CT, RT).NIB * CT; }
 
 // Row (p, i, c) of the 32-bit copy of the DP values: d = 1 .. Dx at [d - 1].
 __device__ __forceinline__ uint32_t *dp32_row(const PassArgs &a, int b, int p, int i, int c) {
@@ -143,25 +145,25 @@ __global__ void __launch_bounds__(256) sweep_layer1_kernel(PassArgs a) {
     if (__syncthreads_or(sat) && threadIdx.x == 0) atomicOr(&ph->lay_sat, 1);
 }
 
-// Position p >= 2 for every instance on the layered words.  blockIdx.x = instance *
-// blocks + row block.
-template <int CT>
+// Position p >= 2 for every instance whose words take tag mode TW (0 rank, 1 width).
+// blockIdx.x = instance * blocks + row block.
+template <int CT, int RT, int TW>
 __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, int p) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait();
     pdl_trigger();
     const Geo &g = a.g;
-    const LayPlan lp = lay_plan(g, CT);
+    const LayPlan lp = lay_plan(g, CT, RT);
     const int NB = 1 + lp.NIB * CT;
     const int b = blockIdx.x / NB, blk = blockIdx.x % NB;
     PrepHdr *ph = prep_hdr(a, b);
     if (ph->status != NEST_SOLVED || p > ph->P) return;   // uniform over the CTA
     const LayWords w = lay_words(ph);
-    if (lay_leaves(ph)) return;   // the streaming sweep solves it
+    if (lay_leaves(ph) || w.mode != TW) return;   // the streaming sweep or the other mode's launch
     const int L = ph->L, C = ph->C, K = ph->K, Du = ph->Du;
     const bool first = blk == 0;
     const int c = first ? 0 : (blk - 1) % CT;
-    const int i0 = first ? 0 : 1 + ((blk - 1) / CT) * kLRows;
+    const int i0 = first ? 0 : 1 + ((blk - 1) / CT) * RT;
     if ((!first && c >= C) || i0 >= L) return;
     const unsigned char *pb = reinterpret_cast<const unsigned char *>(ph);
     const Inst s = load_inst(a, ph, b);
@@ -169,8 +171,8 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
 
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + lp.mbar);
     int64_t *Xs = reinterpret_cast<int64_t *>(smem + lp.X);   // [Nmax + 1][CT]
-    int *rk = reinterpret_cast<int *>(smem + lp.rk);          // [CT][16]
-    int *dec = reinterpret_cast<int *>(smem + lp.dec);        // [Emax]
+    int *rk = reinterpret_cast<int *>(smem + lp.rk);          // [CT][16] slot of (m, c') in A
+    int *dec = reinterpret_cast<int *>(smem + lp.dec);        // [Emax]: (m << 4) | c'
     uint32_t *As = reinterpret_cast<uint32_t *>(smem + lp.A);
     uint32_t *Bs = reinterpret_cast<uint32_t *>(smem + lp.B);
 
@@ -183,15 +185,15 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
         lim[c2] = ml < 0 || mlimc < 0 ? -1 : (ml < mlimc ? ml : mlimc);
     }
     // the states of the block, and whether each has a cell at position p
-    bool act[kLRows];
+    bool act[RT];
 #pragma unroll
-    for (int r = 0; r < kLRows; r++) {
+    for (int r = 0; r < RT; r++) {
         const int i = i0 + r;
         act[r] = (first ? r == 0 : i < L) && p <= layers_of(pb, a, ph, i) && mlimc >= 0;
     }
     bool any = false;
 #pragma unroll
-    for (int r = 0; r < kLRows; r++) any |= act[r];
+    for (int r = 0; r < RT; r++) any |= act[r];
     const int jlo = i0 + 1;
     const int jhi = ph->graph ? L - 1 : (L - p + 1 < L - 1 ? L - p + 1 : L - 1);
 
@@ -230,8 +232,8 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
     while (mwarp + 1 < K && (1 << (mwarp + 1)) <= dmax_w - (p - 1)) mwarp++;
 
     // A words of cut point j: thread q takes (r, m) = (q / K, q % K) for q = tid + k NT
-    constexpr int kPre = (kLRows * 16 + 31) / 32;
-    const int npair = kLRows * K;
+    constexpr int kPre = (RT * 16 + 31) / 32;
+    const int npair = RT * K;
     uint64_t pre[kPre];
     auto fetch = [&](int j) {
 #pragma unroll
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
         }
     };
     auto build = [&](int j, int buf) {
-        uint32_t *Ab = As + buf * lp.Emax * kLRows;
+        uint32_t *Ab = As + buf * lp.Emax * RT;
 #pragma unroll
         for (int k = 0; k < kPre; k++) {
             const int q = tid + k * NT;
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                 if (e < 0) continue;
                 const int64_t v = base + Xs[int64_t(j) * CT + c2];
                 const uint32_t vv = v > int64_t(w.vmax) ? w.vmax + 1 : uint32_t(v);   // saturated
-                Ab[e * kLRows + r] = base < 0 ? ~0u : (vv << w.tb) | uint32_t(e);
+                Ab[e * RT + r] = base < 0 ? ~0u : (vv << w.tb) | uint32_t(TW ? m : e);
             }
         }
     };
@@ -276,24 +278,24 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                          &mbar[buf]);
     };
 
-    // the running best word and cut point of each of the thread's 8 x 4 cells
-    uint32_t rw[kLRows][kLCols], rj[kLRows][kLCols];
+    // the running best word and argument of each of the thread's RT x 4 cells (rank
+    // tags: the cut point; width tags: (j << 4) | c')
+    uint32_t rw[RT][kLCols], rj[RT][kLCols];
 #pragma unroll
-    for (int r = 0; r < kLRows; r++)
+    for (int r = 0; r < RT; r++)
 #pragma unroll
         for (int k = 0; k < kLCols; k++) {
             rw[r][k] = ~0u;
             rj[r][k] = 0;
         }
-    uint32_t phase[2] = {0, 0};
-    bool pending[2] = {false, false};
+    uint32_t phase = 0, pending = 0;   // bit q: mbarrier q's parity, a copy on it in flight
     bool aborted = false;
     const int t = tid;   // columns d = 4t + 1 .. 4t + 4
 
     if (any && jlo <= jhi) {
         if (tid == 0) {
             issue(jlo, 0);
-            pending[0] = true;
+            pending = 1;
         }
         fetch(jlo);
         build(jlo, 0);
@@ -304,27 +306,43 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
             if (more) {
                 if (tid == 0) {
                     issue(j + 1, buf ^ 1);
-                    pending[buf ^ 1] = true;
+                    pending |= 1u << (buf ^ 1);
                 }
                 fetch(j + 1);
             }
-            const bool ok = !aborted && mbar_wait(&mbar[buf], phase[buf], spin);
+            const bool ok = !aborted && mbar_wait(&mbar[buf], (phase >> buf) & 1, spin);
             if (ok) {
-                phase[buf] ^= 1;
-                if (tid == 0) pending[buf] = false;
-                uint32_t cw[kLRows][kLCols];
+                phase ^= 1u << buf;
+                pending &= ~(1u << buf);
+                uint32_t cw[RT][kLCols];   // best over the pairs (m, c') of this cut point
+                uint32_t jw[TW ? RT : 1][kLCols], jc[TW ? RT : 1][kLCols];
 #pragma unroll
-                for (int r = 0; r < kLRows; r++)
+                for (int r = 0; r < RT; r++)
 #pragma unroll
                     for (int k = 0; k < kLCols; k++) cw[r][k] = ~0u;
-                const uint4 *Ab = reinterpret_cast<const uint4 *>(As + buf * lp.Emax * kLRows);
-                auto relax = [&](uint4 B, int e) {
-                    const uint32_t te = uint32_t(e);
-                    const uint32_t bb[4] = {B.x | te, B.y | te, B.z | te, B.w | te};
-                    const uint4 a0 = Ab[2 * e], a1 = Ab[2 * e + 1];
-                    const uint32_t aa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                if constexpr (TW) {
 #pragma unroll
-                    for (int r = 0; r < kLRows; r++)
+                    for (int r = 0; r < RT; r++)
+#pragma unroll
+                        for (int k = 0; k < kLCols; k++) {
+                            jw[r][k] = ~0u;
+                            jc[r][k] = 0;
+                        }
+                }
+                const uint32_t *Ab = As + buf * lp.Emax * RT;
+                auto relax = [&](uint4 B, int e, uint32_t tag) {
+                    const uint32_t bb[4] = {B.x | tag, B.y | tag, B.z | tag, B.w | tag};
+                    uint32_t aa[RT];
+#pragma unroll
+                    for (int h = 0; h < RT / 4; h++) {
+                        const uint4 a4 = reinterpret_cast<const uint4 *>(Ab + e * RT)[h];
+                        aa[4 * h] = a4.x;
+                        aa[4 * h + 1] = a4.y;
+                        aa[4 * h + 2] = a4.z;
+                        aa[4 * h + 3] = a4.w;
+                    }
+#pragma unroll
+                    for (int r = 0; r < RT; r++)
 #pragma unroll
                         for (int k = 0; k < kLCols; k++) cw[r][k] = min(cw[r][k], max(aa[r], bb[k]));
                 };
@@ -336,20 +354,35 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                     const int *rkc = rk + c2 * 16;
                     const uint4 U0 = *reinterpret_cast<const uint4 *>(row + 4 * t);       // B[4t+1 .. 4t+4]
                     const uint4 U1 = *reinterpret_cast<const uint4 *>(row + 4 * t - 4);   // B[4t-3 .. 4t]
-                    relax(make_uint4(U1.w, U0.x, U0.y, U0.z), rkc[0]);                    // 2^0
-                    if (mm >= 1) relax(make_uint4(U1.z, U1.w, U0.x, U0.y), rkc[1]);       // 2^1
-                    if (mm >= 2) relax(U1, rkc[2]);                                       // 2^2
+                    relax(make_uint4(U1.w, U0.x, U0.y, U0.z), rkc[0], TW ? 0u : uint32_t(rkc[0]));   // 2^0
+                    if (mm >= 1) relax(make_uint4(U1.z, U1.w, U0.x, U0.y), rkc[1], TW ? 1u : uint32_t(rkc[1]));
+                    if (mm >= 2) relax(U1, rkc[2], TW ? 2u : uint32_t(rkc[2]));                      // 2^2
                     for (int m = 3; m <= mm; m++)
-                        relax(*reinterpret_cast<const uint4 *>(row + 4 * t - (1 << m)), rkc[m]);
+                        relax(*reinterpret_cast<const uint4 *>(row + 4 * t - (1 << m)), rkc[m],
+                              TW ? uint32_t(m) : uint32_t(rkc[m]));
+                    if constexpr (TW) {
+                        // this candidate's best (v, m) replaces the cut point's only when
+                        // strictly smaller: equal ones keep the smaller c'
+#pragma unroll
+                        for (int r = 0; r < RT; r++)
+#pragma unroll
+                            for (int k = 0; k < kLCols; k++) {
+                                const bool take = cw[r][k] < jw[r][k];
+                                jw[r][k] = take ? cw[r][k] : jw[r][k];
+                                jc[r][k] = take ? uint32_t(c2) : jc[r][k];
+                                cw[r][k] = ~0u;
+                            }
+                    }
                 }
                 // a later cut point wins only with a strictly smaller value
 #pragma unroll
-                for (int r = 0; r < kLRows; r++)
+                for (int r = 0; r < RT; r++)
 #pragma unroll
                     for (int k = 0; k < kLCols; k++) {
-                        const bool take = cw[r][k] < (rw[r][k] & w.nmask);
-                        rw[r][k] = take ? cw[r][k] : rw[r][k];
-                        rj[r][k] = take ? uint32_t(j) : rj[r][k];
+                        const uint32_t cand = TW ? jw[TW ? r : 0][k] : cw[r][k];
+                        const bool take = cand < (rw[r][k] & w.nmask);
+                        rw[r][k] = take ? cand : rw[r][k];
+                        rj[r][k] = take ? (TW ? uint32_t(j) << 4 | jc[TW ? r : 0][k] : uint32_t(j)) : rj[r][k];
                     }
             }
             if (more) build(j + 1, buf ^ 1);
@@ -360,7 +393,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
     // the cells: canonical tables and the 32-bit row for position p + 1
     bool sat = false;
 #pragma unroll
-    for (int r = 0; r < kLRows; r++) {
+    for (int r = 0; r < RT; r++) {
         const int i = i0 + r;
         if (first ? r != 0 : i >= L) continue;
         uint32_t wd[kLCols];
@@ -372,9 +405,11 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
             sat |= v == w.vmax + 1 && d <= Du;
             wd[k] = fin && d <= Du ? (rw[r][k] & w.nmask) : w.nmask;
             if (d <= Du) {
-                const uint64_t key = fin ? (uint64_t(v) << 24) | (uint64_t(rj[r][k]) << 8) |
-                                               uint64_t(dec[rw[r][k] & ~w.nmask])
-                                         : kInf;
+                const uint32_t tag = rw[r][k] & ~w.nmask;
+                // (j << 8) | (m << 4) | c'
+                const uint32_t arg = TW ? (rj[r][k] >> 4) << 8 | tag << 4 | (rj[r][k] & 15)
+                                        : rj[r][k] << 8 | uint32_t(dec[tag]);
+                const uint64_t key = fin ? (uint64_t(v) << 24) | uint64_t(arg) : kInf;
                 write_cell(s, g.Dpad, p, i, c, d, key);
             }
         }
@@ -389,26 +424,35 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
     if (tid == 0) {
         // drain copies still in flight (only after a wait gave up)
         for (int q = 0; q < 2; q++)
-            if (pending[q]) mbar_wait(&mbar[q], phase[q], kDefaultSpin);
+            if ((pending >> q) & 1) mbar_wait(&mbar[q], (phase >> q) & 1, kDefaultSpin);
         if (aborted) ph->status = NEST_TIMED_OUT;
     }
 }
 
-template <int CT>
-int launch_layer_ct(const PassArgs &a, void *stream, int p) {
-    const LayPlan lp = lay_plan(a.g, CT);
+template <int CT, int RT, int TW>
+int launch_layer_mode(const PassArgs &a, void *stream, int p) {
+    const LayPlan lp = lay_plan(a.g, CT, RT);
     const size_t smem = size_t(lp.total);
-    if (int rc = cuda_status(cudaFuncSetAttribute(sweep_layer_kernel<CT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  int(smem)),
+    if (int rc = cuda_status(cudaFuncSetAttribute(sweep_layer_kernel<CT, RT, TW>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
                              "layered sweep smem attribute"))
         return rc;
-    const dim3 grid(unsigned(int64_t(a.n) * lay_blocks(a.g, CT)));
-    return launch_kernel(sweep_layer_kernel<CT>, grid, dim3(unsigned(lp.NT)), smem, stream, 1, "layered sweep launch", a, p);
+    const dim3 grid(unsigned(int64_t(a.n) * lay_blocks(a.g, CT, RT)));
+    return launch_kernel(sweep_layer_kernel<CT, RT, TW>, grid, dim3(unsigned(lp.NT)), smem, stream, 1,
+                         "layered sweep launch", a, p);
+}
+
+// Position p: the rank-tag launch (8 states per thread), then the width-tag launch (4
+// states per thread); each leaves the other's instances alone.
+template <int CT>
+int launch_layer_ct(const PassArgs &a, void *stream, int p) {
+    if (int rc = launch_layer_mode<CT, 8, 0>(a, stream, p)) return rc;
+    return launch_layer_mode<CT, 4, 1>(a, stream, p);
 }
 
 }  // namespace
 
-int64_t layered_smem_bytes(const Geo &g) { return lay_plan(g, ct_of(g.Cmax)).total; }
+int64_t layered_smem_bytes(const Geo &g) { return lay_plan(g, ct_of(g.Cmax), 8).total; }
 
 int launch_layered(const PassArgs &a, void *stream) {
     const Geo &g = a.g;

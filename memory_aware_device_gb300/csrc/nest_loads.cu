@@ -25,14 +25,19 @@
 // invariant divisors (Granlund & Montgomery, see nest_divide.cuh).  pmax comes
 // from a float estimate corrected by exact integer comparisons.
 //
-// GB300 mapping: a CTA copies the instance's derived tables (the prep block) into
-// shared memory in one coalesced pass and handles `ppc` stages (pairs); `spt`
-// threads per stage run over its strategies.  A thread computes the width-free
-// terms of one (stage, strategy) once and then its K width words, folding each into
-// a shared bucket[pair][m][pmax] with an atomic minimum on (tau << 16) | s (taken
-// only when it improves the bucket).  A suffix minimum over pmax gives the
-// per-position loads.  The (stage, width, strategy) words themselves go to memory
-// only when NEST_KEEP_COSTS asks for them.
+// GB300 mapping: one CTA per (instance, state i) copies the instance's derived tables
+// (the prep block) into shared memory in one coalesced pass and takes the stages (i, j)
+// for every j > i, a chunk of them at a time.  An item is one (stage, dense group): the
+// strategies that share (t, cp) share the dense collective prices and those that also
+// share e every expert one, so the thread of an item prices, per width, the dense
+// gradient collectives once, the expert ones and the three amortised syncs once per e,
+// and then evaluates each member's ZeRO stage and recompute choice with adds, selects
+// and the memory test (unrolled when a group holds the whole (z, r) grid).  Each
+// member's word is folded
+// into a shared bucket[stage][m][pmax] with an atomic minimum on (tau << 16) | s (taken
+// only when it improves the bucket); a suffix minimum over pmax gives the per-position
+// loads.  The (stage, width, strategy) words themselves go to memory only when
+// NEST_KEEP_COSTS asks for them.
 #include <cuda_runtime.h>
 
 #include "nest_stages.cuh"
@@ -42,41 +47,99 @@ namespace nest {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBucketBytes = 64 * 1024;   // shared buckets per CTA, at most
+constexpr int kBucketBytes = 48 * 1024;   // shared buckets per CTA, at most
 
-__global__ void __launch_bounds__(kThreads) loads_kernel(PassArgs a, int spt, int ppc) {
-    extern __shared__ __align__(16) unsigned char smem[];   // prep block, buckets, one word
+__global__ void __launch_bounds__(kThreads) loads_kernel(PassArgs a, int pj_max) {
+    extern __shared__ __align__(16) unsigned char smem[];   // prep block, buckets
+    __shared__ uint32_t bmax_s;
     pdl_wait();
     pdl_trigger();
-    const int b = blockIdx.y;
+    const int i = blockIdx.x, b = blockIdx.y;
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(a.ws + a.w.prep + int64_t(b) * a.w.prep_stride);
         uint4 *dst = reinterpret_cast<uint4 *>(smem);
         for (int q = threadIdx.x; q < int(a.pl.bytes / 16); q += blockDim.x) dst[q] = src[q];
     }
+    if (threadIdx.x == 0) bmax_s = 0;
     __syncthreads();
-    if (reinterpret_cast<const PrepHdr *>(smem)->status != NEST_SOLVED) return;   // uniform over the CTA
+    const PrepHdr *ph = reinterpret_cast<const PrepHdr *>(smem);
+    if (ph->status != NEST_SOLVED || i >= ph->L) return;   // uniform over the CTA
+    const Geo &g = a.g;
+    const int L = ph->L, K = ph->K, P = ph->P, ngd = ph->ngd;
+    const int rowp = g.Pcap + 1;
     uint64_t *bucket = reinterpret_cast<uint64_t *>(smem + a.pl.bytes);
-    uint32_t *bmax = reinterpret_cast<uint32_t *>(bucket + int64_t(ppc) * a.g.Kmax * (a.g.Pcap + 1));
-    loads_slice(a, b, smem, int64_t(blockIdx.x) * ppc, ppc, spt, bucket, bmax);
+    const int npair = L - i;   // stages (i, j), j = i + 1 .. L
+    int PJ = kThreads / ngd;
+    PJ = PJ < 1 ? 1 : PJ > pj_max ? pj_max : PJ;
+    uint64_t *out = reinterpret_cast<uint64_t *>(a.ws + a.w.loads) + int64_t(b) * a.w.loads_stride;
+    const int64_t pos_stride = int64_t(g.NP) * g.Kpad;
+    uint32_t tmax = 0;   // largest finite tau written, saturated at 2^31 - 1
+    for (int c0 = 0; c0 < npair; c0 += PJ) {
+        const int nj = PJ < npair - c0 ? PJ : npair - c0;
+        for (int q = threadIdx.x; q < nj * g.Kmax * rowp; q += blockDim.x) bucket[q] = kInf;
+        __syncthreads();
+        for (int it = threadIdx.x; it < nj * ngd; it += blockDim.x) {
+            const int jj = it / ngd, gd = it % ngd;
+            const int j = i + 1 + c0 + jj;
+            const int64_t pair = row_offset(i, L) + c0 + jj;
+            uint64_t *bk = bucket + jj * g.Kmax * rowp;
+            auto fold = [&](int m, int s, uint64_t w) {   // into bucket[m][pmax]
+                const int pm = w == kInf ? 0 : int(w & 0xFF);
+                if (pm == 0) return;
+                const uint64_t key = ((w >> 8) << 16) | uint64_t(s);
+                uint64_t *slot = bk + m * rowp + pm;
+                if (key < *slot) atomicMin(reinterpret_cast<unsigned long long *>(slot), key);
+            };
+            if (a.keep_costs) {
+                uint64_t *cout = reinterpret_cast<uint64_t *>(a.ws + a.w.cost) + int64_t(b) * a.w.cost_stride +
+                                 pair * g.Kmax * g.Spad;
+                dense_group_words<true>(ph, smem, a.pl, g, i, j, gd, [&](int m, int s, uint64_t w) {
+                    cout[int64_t(m) * g.Spad + s] = w;
+                    fold(m, s, w);
+                });
+            } else {
+                dense_group_words<false>(ph, smem, a.pl, g, i, j, gd, fold);
+            }
+        }
+        __syncthreads();
+        // suffix minimum over pmax: position p takes the strategies with pmax >= p
+        for (int r = threadIdx.x; r < nj * K; r += blockDim.x) {
+            const int jj = r / K, m = r % K;
+            const int64_t pr = row_offset(i, L) + c0 + jj;
+            const uint64_t *bq = bucket + (jj * g.Kmax + m) * rowp;
+            uint64_t cur = kInf;
+            for (int p = P; p >= 1; p--) {
+                cur = bq[p] < cur ? bq[p] : cur;
+                out[int64_t(p - 1) * pos_stride + pr * g.Kpad + m] = cur;
+                if (cur != kInf) {
+                    const uint64_t tau = cur >> 16;
+                    const uint32_t t32 = tau < 0x7FFFFFFFu ? uint32_t(tau) : 0x7FFFFFFFu;
+                    tmax = t32 > tmax ? t32 : tmax;
+                }
+            }
+        }
+        __syncthreads();   // the buckets are reused
+    }
+    // one atomic per CTA: the sweeps keep 32-bit words when every value is small
+    tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
+    if ((threadIdx.x & 31) == 0 && tmax) atomicMax(&bmax_s, tmax);
+    __syncthreads();
+    if (threadIdx.x == 0 && bmax_s) atomicMax(&prep_hdr(a, b)->maxload32, bmax_s);
 }
 
 }  // namespace
 
 int launch_loads(const PassArgs &a, void *stream) {
-    // spt threads per stage over its strategies, ppc stages per CTA (bounded by the
-    // shared buckets)
-    const int spt = a.g.Smax < kThreads ? a.g.Smax : kThreads;
+    // stages per chunk bounded by the shared buckets
     const int per_pair = a.g.Kmax * (a.g.Pcap + 1) * 8;
-    int ppc = kThreads / spt;
-    if (ppc * per_pair > kBucketBytes) ppc = kBucketBytes / per_pair > 0 ? kBucketBytes / per_pair : 1;
-    const int threads = (ppc * spt + 31) / 32 * 32;
-    const size_t smem = size_t(a.pl.bytes) + size_t(ppc) * per_pair + 16;
+    int pj_max = kBucketBytes / per_pair;
+    pj_max = pj_max < 1 ? 1 : pj_max > kThreads ? kThreads : pj_max;
+    const size_t smem = size_t(a.pl.bytes) + size_t(pj_max) * per_pair;
     if (int rc = cuda_status(cudaFuncSetAttribute(loads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
                              "loads smem attribute"))
         return rc;
-    const dim3 grid(unsigned((int64_t(a.g.NP) + ppc - 1) / ppc), unsigned(a.n));
-    return launch_kernel(loads_kernel, grid, dim3(unsigned(threads)), smem, stream, 1, "loads launch", a, spt, ppc);
+    const dim3 grid(unsigned(a.g.Nmax), unsigned(a.n));
+    return launch_kernel(loads_kernel, grid, dim3(kThreads), smem, stream, 1, "loads launch", a, pj_max);
 }
 
 }  // namespace nest

@@ -328,6 +328,37 @@ static __device__ __noinline__ void prep_instance(const PassArgs &a, int b, unsi
                 uint32_t(x[3]) << 12 | uint32_t(x[4]) << 14;
     }
     __syncthreads();
+    // the strategies sorted by (t, cp, e, z, r, s), and the groups of equal (t, cp, e): the
+    // stage-loads pass prices the collectives of a group once per width and then each
+    // member's ZeRO stage and recompute choice
+    {
+        uint32_t *ss = reinterpret_cast<uint32_t *>(pb + a.pl.ssort);
+        uint32_t *sg = reinterpret_cast<uint32_t *>(pb + a.pl.sgrp);
+        auto key = [&](int s) {
+            const uint32_t c = sp[s];
+            return uint64_t((c & 0xFFF) << 3 | (c >> 12 & 3) << 1 | (c >> 14 & 1)) << 12 | uint64_t(s);
+        };
+        for (int s = threadIdx.x; s < h.S; s += blockDim.x) {
+            const uint64_t ks = key(s);
+            int rank = 0;
+            for (int t = 0; t < h.S; t++) rank += key(t) < ks;
+            ss[rank] = sp[s] | uint32_t(s) << 16;
+        }
+        __syncthreads();
+        uint32_t *sd = reinterpret_cast<uint32_t *>(pb + a.pl.sgd);
+        if (threadIdx.x == 0) {
+            int n = 0, nd = 0;
+            for (int q = 0; q < h.S; q++) {
+                if (q == 0 || (ss[q] & 0xFF) != (ss[q - 1] & 0xFF)) sd[nd++] = uint32_t(n);   // new (t, cp)
+                if (q == 0 || (ss[q] & 0xFFF) != (ss[q - 1] & 0xFFF)) sg[n++] = uint32_t(q);  // new (t, cp, e)
+            }
+            sg[n] = uint32_t(h.S);
+            sd[nd] = uint32_t(n);
+            ph->ngrp = n;
+            ph->ngd = nd;
+        }
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
         ph->L = E;
         ph->maxX32 = xmax;
@@ -385,181 +416,157 @@ __device__ __forceinline__ void mask_sums(const int64_t *pfx, const int64_t *aws
     }
 }
 
-// The K width words (tau << 8) | pmax of the stage from state i to state j under
-// strategy s, handed to emit(m, word); all ones where the strategy does not apply at
-// that width, and for a graph instance when state j is not inside state i.
-template <typename Emit>
-__device__ __forceinline__ void stage_words(const PrepHdr *ph, const unsigned char *pb, const PrepLayout &pl,
-                                            const Geo &g, int i, int j, int s, Emit emit) {
-    const int K = ph->K, lu = ph->lu;
-    const uint32_t code = reinterpret_cast<const uint32_t *>(pb + pl.strat)[s];
-    const int lt = code & 15, lcp = (code >> 4) & 15, le = (code >> 8) & 15;
-    const int z = (code >> 12) & 3, r = (code >> 14) & 1;
+// The stage sums of the stage from state i to state j: false when it is no stage (for a
+// graph instance, state j not inside state i).
+__device__ __forceinline__ bool pair_sums(const PrepHdr *ph, const unsigned char *pb, const PrepLayout &pl,
+                                          const Geo &g, int i, int j, StageSums &u) {
     const int64_t *pfx = reinterpret_cast<const int64_t *>(pb + pl.pfx);
     const int64_t *awst = reinterpret_cast<const int64_t *>(pb + pl.awst);
-    const int64_t ld = g.Lmax + 1;
-    // valid for some width iff t cp e <= the widest stage, and e > 1 only over MoE layers
-    const int lmin = lt + lcp + le - lu;  // smallest m that admits the strategy
-    StageSums u;
     if (ph->graph) {
         const uint64_t *um = reinterpret_cast<const uint64_t *>(pb + pl.umask);
         const uint64_t Di = um[i], Dj = um[j];
-        if ((Dj & ~Di) || lmin > K - 1) {
-            for (int m = 0; m < K; m++) emit(m, kInf);
-            return;
-        }
+        if (Dj & ~Di) return false;
         mask_sums(pfx, awst, g, Di & ~Dj, u);
-        if (le > 0 && u.v[kNm] == 0) {
-            for (int m = 0; m < K; m++) emit(m, kInf);
-            return;
-        }
-    } else {
-        u.v[kNm] = pfx[kNm * ld + j] - pfx[kNm * ld + i];
-        if (lmin > K - 1 || (le > 0 && u.v[kNm] == 0)) {
-            for (int m = 0; m < K; m++) emit(m, kInf);
-            return;
-        }
-        for (int q = 0; q < kNm; q++) u.v[q] = pfx[q * ld + j] - pfx[q * ld + i];
-        u.nL = j - i;
-        u.awmax = r ? aw_max(awst, g, i, j) : 0;
+        return true;
+    }
+    const int64_t ld = g.Lmax + 1;
+    for (int q = 0; q < kNumPfx; q++) u.v[q] = pfx[q * ld + j] - pfx[q * ld + i];
+    u.nL = j - i;
+    u.awmax = aw_max(awst, g, i, j);
+    return true;
+}
+
+// pmax of one strategy (§3.3): the largest position p <= P whose stash still fits,
+// 1F1B (p - 1 stashed microbatches) or GPipe (all ceil(M / q) of a replica's).
+// rem = budget - static >= 0; full = (P - 1) * stash, inv ~ 1 / stash.
+__device__ __forceinline__ int fit_positions(const PrepHdr *ph, int64_t rem, int64_t st, int64_t full, float inv,
+                                             int lq) {
+    const int P = ph->P;
+    if (ph->schedule == 1) {
+        // GPipe: ceil(M / q) stashed microbatches; exact 128-bit product
+        const uint64_t inflight = uint64_t((ph->M + (int64_t(1) << lq) - 1) >> lq);
+        const uint64_t lo = uint64_t(st) * inflight, hi = __umul64hi(uint64_t(st), inflight);
+        return hi == 0 && lo <= uint64_t(rem) ? P : 0;
+    }
+    if (rem >= full) return P;   // also st == 0
+    // (P - 1) st > rem: the quotient is below 31; a float estimate, corrected exactly
+    int p = 1 + int(float(rem) * inv);
+    p = p > P ? P : p < 1 ? 1 : p;
+    if (int64_t(p - 1) * st > rem) p--;
+    else if (p < P && int64_t(p) * st <= rem) p++;
+    return p;
+}
+
+// The width words (tau << 8) | pmax of stage (i, j) for every strategy of dense group
+// gd (equal t, cp), handed to emit(m, s, word) for every width m; all ones where a
+// strategy does not apply to a width.  A dense group is a run of strategy groups (equal
+// t, cp, e) whose members differ in the ZeRO stage z and recompute r.  Per width the
+// collectives are priced once: the dense ones once per dense group, the expert ones
+// once per strategy group.  With S1 = coll(1, q) + coll(1, q / e) and
+// S2 = coll(2, q) + coll(2, q / e) over the dense and expert gradient bytes, the
+// gradient sync is S2 for z = 0 (AllReduce), 2 S1 for z = 1, 2 (ReduceScatter +
+// AllGather) and S1 for z = 3 (ReduceScatter); the ZeRO-3 weight gathers (two
+// AllGathers of the shards per layer, count 2 nL and volume 2 W) cost exactly S2: the
+// same latency steps (cnt phi) and the same bytes per device (phi V).
+template <bool kAll, typename Emit>
+__device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsigned char *pb, const PrepLayout &pl,
+                                                  const Geo &g, int i, int j, int gd, Emit emit) {
+    // kAll: also hand over the all-ones words of strategies that do not apply (only the
+    // kept stage-cost tensor wants them; the per-position loads skip them anyway)
+    const int K = ph->K, lu = ph->lu;
+    const uint32_t *ss = reinterpret_cast<const uint32_t *>(pb + pl.ssort);
+    const uint32_t *sg = reinterpret_cast<const uint32_t *>(pb + pl.sgrp);
+    const uint32_t *sd = reinterpret_cast<const uint32_t *>(pb + pl.sgd);
+    const int g0 = int(sd[gd]), g1 = int(sd[gd + 1]);   // its strategy groups
+    const int q0 = int(sg[g0]), q1 = int(sg[g1]);       // its strategies
+    const uint32_t c0 = ss[q0];
+    const int lt = c0 & 15, lcp = (c0 >> 4) & 15;
+    const int ltc = lt + lcp;
+    StageSums u;
+    const bool stage = pair_sums(ph, pb, pl, g, i, j, u);
+    if (!stage || ltc - lu > K - 1) {
+        if (kAll)
+            for (int m = 0; m < K; m++)
+                for (int q = q0; q < q1; q++) emit(m, int(ss[q] >> 16), kInf);
+        return;
     }
     const int64_t Fl = u.v[kFl], Pd = u.v[kPd], Pe = u.v[kPe], Ao = u.v[kAo], Aw = u.v[kAw], A2 = u.v[kA2];
     const int64_t nM = u.v[kNm], nL = u.nL;
     const Net net{ph};
-
-    // width-independent terms: groups inside one replica
-    const int64_t comp = int64_t(divide_up(uint64_t(up_shift(Fl * (3 + r), lt + lcp)), uint64_t(ph->R), ph->Rdiv));
-    const int64_t rep = comp + net.coll(2, lt, ph->tier_log[lt], 4 * up_shift(Ao, lcp), 4 * nL) +
-                        net.coll(1, lcp, ph->tier_log[lt + lcp], 4 * up_shift(Ao, lt), 4 * nL) +
-                        net.coll(1, le, ph->tier_log[lt + lcp + le], 4 * up_shift(A2, lt + lcp), 4 * nM);
-    const int64_t Wd = up_shift(Pd, lt), We = up_shift(Pe, lt + le);
-    int64_t act, stash;
-    if (r) {
-        act = up_shift(u.awmax, lt + lcp);
-        stash = up_shift(reinterpret_cast<const int64_t *>(pb + pl.ain)[i], lt + lcp);
-    } else {
-        act = up_shift(Aw, lt + lcp);
-        stash = act;
-    }
+    // width-independent terms of the dense group: compute per recompute choice, the TP and
+    // CP collectives inside one replica, weights, activations and stash
+    const int64_t tpcp = net.coll(2, lt, ph->tier_log[lt], 4 * up_shift(Ao, lcp), 4 * nL) +
+                         net.coll(1, lcp, ph->tier_log[ltc], 4 * up_shift(Ao, lt), 4 * nL);
+    const int64_t cmp0 = int64_t(divide_up(uint64_t(up_shift(Fl * 3, ltc)), uint64_t(ph->R), ph->Rdiv)) + tpcp;
+    const int64_t cmp1 = int64_t(divide_up(uint64_t(up_shift(Fl * 4, ltc)), uint64_t(ph->R), ph->Rdiv)) + tpcp;
+    const int64_t Wd = up_shift(Pd, lt);
+    const int64_t act0 = up_shift(Aw, ltc), act1 = up_shift(u.awmax, ltc);
+    const int64_t st0 = act0, st1 = up_shift(reinterpret_cast<const int64_t *>(pb + pl.ain)[i], ltc);
+    const float inv0 = st0 > 0 ? 1.0f / float(st0) : 0.0f, inv1 = st1 > 0 ? 1.0f / float(st1) : 0.0f;
+    const int64_t full0 = int64_t(ph->P - 1) * st0, full1 = int64_t(ph->P - 1) * st1;
     const int64_t opt = ph->opt, budget = ph->budget, M = ph->M;
-    const int P = ph->P;
-    const float inv_stash = stash > 0 ? 1.0f / float(stash) : 0.0f;
-    const int64_t mult = z == 0 ? 1 : (z < 3 ? 2 : 1);
-    const int64_t phi_s = z == 0 ? 2 : 1;
+    const int64_t owd = opt * Wd;
     for (int m = 0; m < K; m++) {
-        uint64_t word = kInf;
-        if (m >= lmin) {
-            const int lq = lu + m - lt - lcp, lqe = lq - le;
-            const int tk = ph->tier_log[lu + m];
-            const int64_t z3 =
-                z == 3 ? net.coll(1, lq, tk, 2 * Wd, 2 * nL) + net.coll(1, lqe, tk, 2 * We, 2 * nM) : 0;
-            const int64_t sync = mult * (net.coll(phi_s, lq, tk, Wd, nL) + net.coll(phi_s, lqe, tk, We, nM));
-            const int64_t tau = up_shift(rep + z3, lq) + int64_t(divide_up(uint64_t(sync), uint64_t(M), ph->Mdiv));
-            if (tau < kCap) {
-                const int64_t sh = up_shift(Wd, lq) + up_shift(We, lqe);
-                const int64_t w = z == 3 ? sh : Wd + We;
-                const int64_t gr = z >= 2 ? sh : Wd + We;
-                const int64_t o = z >= 1 ? up_shift(opt * Wd, lq) + up_shift(opt * We, lqe) : opt * (Wd + We);
-                const int64_t stat = w + gr + o + act;
-                int pmax;
-                if (stat > budget) {
-                    pmax = 0;
-                } else if (ph->schedule == 1) {
-                    // GPipe: ceil(M / q) stashed microbatches; exact 128-bit product
-                    const uint64_t inflight = uint64_t((M + (int64_t(1) << lq) - 1) >> lq);
-                    const uint64_t lo = uint64_t(stash) * inflight, hi = __umul64hi(uint64_t(stash), inflight);
-                    pmax = hi == 0 && lo <= uint64_t(budget - stat) ? P : 0;
-                } else if (stash == 0) {
-                    pmax = P;
-                } else {
-                    // largest p <= P with (p - 1) stash <= budget - stat
-                    const int64_t rem = budget - stat;
-                    int p = 1 + int(fminf(float(rem) * inv_stash, 64.0f));
-                    p = p > P ? P : p;
-                    while (p > 1 && int64_t(p - 1) * stash > rem) p--;
-                    while (p < P && int64_t(p) * stash <= rem) p++;
-                    pmax = p;
+        const int lq = lu + m - ltc;
+        if (lq < 0) {
+            if (kAll)
+                for (int q = q0; q < q1; q++) emit(m, int(ss[q] >> 16), kInf);
+            continue;
+        }
+        const int tk = ph->tier_log[lu + m];
+        const int64_t D1 = net.coll(1, lq, tk, Wd, nL), D2 = net.coll(2, lq, tk, Wd, nL);
+        const int64_t wdq = up_shift(Wd, lq), owdq = up_shift(owd, lq);
+        for (int gi = g0; gi < g1; gi++) {
+            const int qa = int(sg[gi]), qb = int(sg[gi + 1]);
+            const int le = (ss[qa] >> 8) & 15;
+            const int lqe = lq - le;
+            if (lqe < 0 || (le > 0 && nM == 0)) {
+                if (kAll)
+                    for (int q = qa; q < qb; q++) emit(m, int(ss[q] >> 16), kInf);
+                continue;
+            }
+            // the strategy group's expert degree: its weights, AllToAlls and expert sync
+            const int64_t We = up_shift(Pe, lt + le);
+            const int64_t ep = net.coll(1, le, ph->tier_log[ltc + le], 4 * up_shift(A2, ltc), 4 * nM);
+            const int64_t S1 = D1 + net.coll(1, lqe, tk, We, nM);
+            const int64_t S2 = D2 + net.coll(2, lqe, tk, We, nM);
+            const int64_t dM0 = int64_t(divide_up(uint64_t(S2), uint64_t(M), ph->Mdiv));       // z = 0
+            const int64_t dM12 = int64_t(divide_up(uint64_t(2 * S1), uint64_t(M), ph->Mdiv));  // z = 1, 2
+            const int64_t dM3 = int64_t(divide_up(uint64_t(S1), uint64_t(M), ph->Mdiv));       // z = 3
+            const int64_t full = Wd + We;
+            const int64_t sh = wdq + up_shift(We, lqe);
+            const int64_t osh = owdq + up_shift(opt * We, lqe);
+            const int64_t sz0 = 2 * full + opt * full, sz1 = 2 * full + osh, sz2 = full + sh + osh, sz3 = 2 * sh + osh;
+            const int64_t r0 = cmp0 + ep, r1 = cmp1 + ep;
+            const int64_t t00 = up_shift(r0, lq), t10 = up_shift(r1, lq);            // z < 3
+            const int64_t t03 = up_shift(r0 + S2, lq), t13 = up_shift(r1 + S2, lq);  // z = 3
+            // one member: its word from its (z, r)
+            auto member = [&](int q, int z, int r) {
+                const int s = int(ss[q] >> 16);
+                const int64_t tau = (z == 3 ? (r ? t13 : t03) : (r ? t10 : t00)) + (z == 0 ? dM0 : z == 3 ? dM3 : dM12);
+                uint64_t word = kInf;
+                if (tau < kCap) {
+                    const int64_t stat = (z == 0 ? sz0 : z == 1 ? sz1 : z == 2 ? sz2 : sz3) + (r ? act1 : act0);
+                    const int pmax = stat > budget ? 0
+                                                   : fit_positions(ph, budget - stat, r ? st1 : st0, r ? full1 : full0,
+                                                                   r ? inv1 : inv0, lq);
+                    word = (uint64_t(tau) << 8) | uint64_t(pmax);
                 }
-                word = (uint64_t(tau) << 8) | uint64_t(pmax);
-            }
-        }
-        emit(m, word);
-    }
-}
-
-// The per-position loads of stages pair0 .. pair0 + ppc - 1 of instance b, from a
-// copy of its prep block in shared memory (`smem`, status solved), with `bucket`
-// ([ppc][Kmax][Pcap + 1] uint64) and one word `bmax` of shared scratch.  spt threads
-// per stage run over its strategies (ppc * spt <= blockDim.x).  Every thread of the
-// block calls it.
-static __device__ __noinline__ void loads_slice(const PassArgs &a, int b, const unsigned char *smem, int64_t pair0, int ppc,
-                                         int spt, uint64_t *bucket, uint32_t *bmax_s) {
-    const Geo &g = a.g;
-    const PrepLayout &pl = a.pl;
-    const PrepHdr *ph = reinterpret_cast<const PrepHdr *>(smem);
-    const int L = ph->L, S = ph->S, K = ph->K, P = ph->P;
-    const int64_t npairs = int64_t(L) * (L + 1) / 2;
-    if (pair0 >= npairs) return;             // uniform over the CTA
-    const int rowp = g.Pcap + 1;
-    for (int q = threadIdx.x; q < ppc * g.Kmax * rowp; q += blockDim.x) bucket[q] = kInf;
-    __syncthreads();
-
-    const int lp = threadIdx.x / spt, s0 = threadIdx.x % spt;
-    const int64_t pair = pair0 + lp;
-    if (lp < ppc && pair < npairs) {
-        // invert pair = row_offset(i) + (j - i - 1)
-        int i = int((2.0f * L + 1.0f - sqrtf((2.0f * L + 1.0f) * (2.0f * L + 1.0f) - 8.0f * float(pair))) * 0.5f);
-        if (i < 0) i = 0;
-        if (i > L - 1) i = L - 1;
-        while (i > 0 && row_offset(i, L) > pair) i--;
-        while (i < L - 1 && row_offset(i + 1, L) <= pair) i++;
-        const int j = i + 1 + int(pair - row_offset(i, L));
-        uint64_t *bk = bucket + lp * g.Kmax * rowp;
-        uint64_t *cout = a.keep_costs ? reinterpret_cast<uint64_t *>(a.ws + a.w.cost) + int64_t(b) * a.w.cost_stride +
-                                            pair * g.Kmax * g.Spad
-                                      : nullptr;
-        for (int s = s0; s < S; s += spt) {
-            stage_words(ph, smem, pl, g, i, j, s, [&](int m, uint64_t w) {
-                if (cout) cout[int64_t(m) * g.Spad + s] = w;
-                const int pm = w == kInf ? 0 : int(w & 0xFF);
-                if (pm == 0) return;
-                const uint64_t key = ((w >> 8) << 16) | uint64_t(s);
-                uint64_t *slot = bk + m * rowp + pm;
-                if (key < *slot) atomicMin(reinterpret_cast<unsigned long long *>(slot), key);
-            });
-        }
-    }
-    __syncthreads();
-    // suffix minimum over pmax: position p takes the strategies with pmax >= p
-    uint64_t *out = reinterpret_cast<uint64_t *>(a.ws + a.w.loads) + int64_t(b) * a.w.loads_stride;
-    const int64_t pos_stride = int64_t(g.NP) * g.Kpad;
-    uint32_t tmax = 0;   // largest finite tau written, saturated at 2^31 - 1
-    for (int r = threadIdx.x; r < ppc * K; r += blockDim.x) {
-        const int q = r / K, m = r % K;
-        const int64_t pr = pair0 + q;
-        if (pr >= npairs) continue;
-        const uint64_t *bq = bucket + (q * g.Kmax + m) * rowp;
-        uint64_t cur = kInf;
-        for (int p = P; p >= 1; p--) {
-            cur = bq[p] < cur ? bq[p] : cur;
-            out[int64_t(p - 1) * pos_stride + pr * g.Kpad + m] = cur;
-            if (cur != kInf) {
-                const uint64_t tau = cur >> 16;
-                const uint32_t t32 = tau < 0x7FFFFFFFu ? uint32_t(tau) : 0x7FFFFFFFu;
-                tmax = t32 > tmax ? t32 : tmax;
+                emit(m, s, word);
+            };
+            // the whole (z, r) grid in order (eight members): unrolled, every select folds
+            bool grid = qb - qa == 8;
+            if (grid)
+                for (int k = 0; k < 8; k++) grid &= ((ss[qa + k] >> 12) & 7) == uint32_t(k >> 1 | (k & 1) << 2);
+            if (grid) {
+#pragma unroll
+                for (int k = 0; k < 8; k++) member(qa + k, k >> 1, k & 1);
+            } else {
+                for (int q = qa; q < qb; q++) member(q, (ss[q] >> 12) & 3, (ss[q] >> 14) & 1);
             }
         }
     }
-    // one atomic per CTA: the sweep keeps 32-bit words when every value is small
-    if (threadIdx.x == 0) *bmax_s = 0;
-    __syncthreads();
-    tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
-    if ((threadIdx.x & 31) == 0 && tmax) atomicMax(bmax_s, tmax);
-    __syncthreads();
-    if (threadIdx.x == 0 && *bmax_s) atomicMax(&prep_hdr(a, b)->maxload32, *bmax_s);
-    __syncthreads();   // the buckets and bmax may be reused
 }
-
 
 // The final batch-time loop and the plan of instance b, by one whole warp; `walk`
 // is 64 ints of shared scratch for the warp (stage q -> (i | j << 8 | m << 16 |

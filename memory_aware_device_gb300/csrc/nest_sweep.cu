@@ -319,6 +319,14 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
     auto accept = [&](const Pick &r) {
         return r.best > 0 && (variant == 1 || r.shape.resident_waves == 1 || r.ctas >= int64_t(sms));
     };
+    // the library's choice between a resident shape in several waves and the layered
+    // sweep: over enough states the layered launches are throughput-bound and win
+    // (measured on GB300: 256 instances of 48 states, resident in waves 6.4 ms, layered
+    // 4.9 ms); below that each of their launches is bound by the serial cut points of
+    // its longest CTA (16 instances of 32 states: resident 0.16 ms, layered 1.7 ms)
+    auto prefer_layered = [&](const SweepShape &sh) {
+        return variant == 0 && sh.resident_waves >= 3 && g.Nmax >= 40 && layered() == NEST_OK;
+    };
     out.split = 0;
     out.wide = {};
     if (variant != 2 && g.Cmax <= 4) {
@@ -339,6 +347,7 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
                 }
                 if (ok) {
                     const SweepShape &ns = narrow.shape;
+                    if (prefer_layered(ns)) return NEST_OK;
                     out = {ns.cluster, ns.jsplit, ns.jc, ns.threads, ns.resident, ns.resident_waves, 1, ws};
                     if (std::getenv("NEST_DEBUG"))
                         std::fprintf(stderr,
@@ -352,6 +361,7 @@ int sweep_configure(const Geo &g, int n, int cluster_opt, int jsplit_opt, int va
         }
         if (accept(both)) {
             const SweepShape &p = both.shape;
+            if (prefer_layered(p)) return NEST_OK;
             out = {p.cluster, p.jsplit, p.jc, p.threads, p.resident, p.resident_waves, 0, {}};
             if (std::getenv("NEST_DEBUG"))
                 std::fprintf(stderr, "nest: sweep resident, cluster %d jsplit %d threads %d\n", p.cluster, p.jsplit,

@@ -138,30 +138,40 @@ __device__ __forceinline__ uint32_t cluster_map(const void *local, uint32_t rank
 
 // The 32-bit words of an instance on the layered sweep (nest_layered.cu): a value v is
 // held as (v << tb) | tag; values 0 .. vmax are exact, vmax + 1 ("sat") stands for any
-// larger finite value, and all value bits set for no value.
+// larger finite value, and all value bits set for no value.  Two tag modes:
+//  - rank (mode 0): the tag is the rank of (m, c') among a row block's admissible pairs,
+//    so one minimum orders a cut point's candidates by (v, m, c');
+//  - width (mode 1): the tag is the width index m alone (fewer tag bits, more value
+//    bits), and the next-link candidate c' is resolved by a compare per candidate.
+// An instance takes the rank mode when its value bound (largest load plus two link
+// costs, a bound of every value of its DP) fits those words, else the width mode.
 struct LayWords {
     bool ok;         // the instance takes the layered sweep
-    bool fits;       // its value bound (largest load plus two link costs) is at most vmax,
-                     // so no word saturates
+    bool fits;       // its value bound is at most vmax, so no word saturates
+    int mode;        // 0 = rank tags, 1 = width tags
     int tb;          // tag bits
     uint32_t nmask;  // value bits of a word
     uint32_t vmax;   // largest exact value
 };
 
-// tb = log2 of the number of (m, c') pairs a row block can admit (at most those of the
-// first stage, which has no input link: every width up to the next link's tier).
 __device__ __forceinline__ LayWords lay_words(const PrepHdr *ph) {
+    // rank tags: at most the pairs of the first stage, which has no input link (every
+    // width up to each next-link candidate's tier)
     int E = 0;
     for (int c = 0; c < ph->C && c < 16; c++)
         if (ph->mlim[c] >= 0) E += (ph->mlim[c] < ph->K - 1 ? ph->mlim[c] : ph->K - 1) + 1;
-    int tb = 1;
-    while ((1 << tb) < E) tb++;
+    int tr = 1;
+    while ((1 << tr) < E) tr++;
+    int tw = 1;   // width tags: m = 0 .. K - 1
+    while ((1 << tw) < ph->K) tw++;
+    const uint64_t bound = uint64_t(ph->maxload32) + 2 * uint64_t(ph->maxX32);
     LayWords w;
-    w.tb = tb;
-    w.nmask = ~((1u << tb) - 1u);
-    w.vmax = (1u << (32 - tb)) - 3u;
+    w.mode = bound <= uint64_t((1u << (32 - tr)) - 3u) ? 0 : 1;
+    w.tb = w.mode == 0 ? tr : tw;
+    w.nmask = ~((1u << w.tb) - 1u);
+    w.vmax = (1u << (32 - w.tb)) - 3u;
     w.ok = ph->C <= 4;
-    w.fits = uint64_t(ph->maxload32) + 2 * uint64_t(ph->maxX32) <= uint64_t(w.vmax);
+    w.fits = bound <= uint64_t(w.vmax);
     return w;
 }
 

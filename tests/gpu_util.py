@@ -155,9 +155,10 @@ def same_graph_result(g, o):
     return g["status"] != 0 or g["layers"] == [int(st[i]) & ~int(st[j]) for i, j, *_ in o["plan"]]
 
 
-def layered_tag_bits(inst):
-    """Tag bits of the layered sweep's 32-bit words for an instance: log2 of the (m, c')
-    pairs its first stage admits (every width up to each next-link candidate's tier)."""
+def layered_words(inst):
+    """The layered sweep's 32-bit words for an instance, as (mode, tag bits, vmax): rank
+    tags (mode 0, log2 of the (m, c') pairs its first stage admits) when the value bound
+    is at most their largest exact value, else width tags (mode 1, log2 of the widths)."""
     Du = inst.D // inst.unit
     K = Du.bit_length()
     E = 0
@@ -166,14 +167,20 @@ def layered_tag_bits(inst):
         ml = max((m for m in range(16) if 2 * (int(inst.unit) << m) <= G), default=-1)
         if ml >= 0:
             E += min(ml, K - 1) + 1
-    tb = 1
-    while (1 << tb) < E:
-        tb += 1
-    return tb
+    tr = 1
+    while (1 << tr) < E:
+        tr += 1
+    tw = 1
+    while (1 << tw) < K:
+        tw += 1
+    vb = value_bound(inst)
+    mode = 0 if vb <= 2**(32 - tr) - 3 else 1
+    tb = tr if mode == 0 else tw
+    return mode, tb, 2**(32 - tb) - 3
 
 
-def layered_words(inst):
-    """Whether the layered sweep holds the instance on its 32-bit words: at most four
-    candidates and a value bound of at most 2^(32 - tb) - 2."""
-    tb = layered_tag_bits(inst)
-    return len(inst.cand) <= 4 and value_bound(inst) <= 2**(32 - tb) - 2
+def layered_fits(inst):
+    """Whether no word of the layered sweep can saturate for the instance (at most four
+    candidates and a value bound within its mode's exact values)."""
+    _, _, vmax = layered_words(inst)
+    return len(inst.cand) <= 4 and value_bound(inst) <= vmax

@@ -1,9 +1,10 @@
-"""GPU parity of the layered DP sweep (one launch per pipeline position, 32-bit tagged
-words) against the CPU oracle, bit for bit: every DP key, the per-position loads, the
-stage-cost words and the results, on every workload, random tiny instances, layer
-DAGs, edge cases, and batches that mix instances on its words with instances left to
-the 64-bit streaming sweep (values beyond the words).  Nest §4 Eq. 3 is layered in the
-stage count: position p reads only position p - 1."""
+"""GPU parity of the layered DP sweep (one launch per pipeline position and tag mode,
+32-bit tagged words) against the CPU oracle, bit for bit: every DP key, the
+per-position loads, the stage-cost words and the results, on every workload, random
+tiny instances, layer DAGs, edge cases, and batches that mix instances on rank tags,
+on width tags, and instances left to the 64-bit streaming sweep (values beyond the
+words).  Nest §4 Eq. 3 is layered in the stage count: position p reads only position
+p - 1."""
 import numpy as np
 import pytest
 
@@ -47,24 +48,27 @@ def test_layered_launch_description():
     dims = nest.make_dims(synth.config_batch(5, B=4))
     d = nest.describe_launch(dims, nest.options(variant=LAYERED))
     assert d["sweep_variant"] == LAYERED
-    # prep, stage loads, position 1, positions 2 .. 16, the streaming launch, backtrack
-    assert d["kernels_per_chunk"] == 2 + 16 + 1 + 1
+    # prep, stage loads, position 1, two launches (tag modes) for each of positions
+    # 2 .. 16, the streaming launch, backtrack
+    assert d["kernels_per_chunk"] == 2 + 1 + 2 * 15 + 1 + 1
 
 
 def test_layered_workload1():
     inst = synth.config_instance(1, 0)
-    assert G.layered_words(inst)
+    assert G.layered_fits(inst)
     check_batch([inst], tables=(0,))
 
 
 def test_layered_workload2():
     insts = synth.config_batch(2)
-    assert all(G.layered_words(x) for x in insts)
+    assert all(G.layered_words(x)[0] == 0 and G.layered_fits(x) for x in insts)
     check_batch(insts, tables=(0, 7, 15))
 
 
 def test_layered_workload3():
+    # the deep dense workload's values need 29 bits: width tags
     insts = synth.config_batch(3, B=8)
+    assert G.layered_words(insts[0])[0] == 1
     check_batch(insts, tables=(0, 5))
 
 
@@ -76,7 +80,7 @@ def test_layered_workload4():
 def test_layered_workload5_tables():
     # instance 2 has the largest values of the first instances (its value bound ~2^26.4)
     insts = synth.config_batch(5, B=3)
-    assert all(G.layered_words(x) for x in insts)
+    assert all(G.layered_words(x)[0] == 0 and G.layered_fits(x) for x in insts)
     check_batch(insts, tables=(0, 2))
 
 
@@ -92,28 +96,46 @@ def test_layered_random_tiny(part):
             check_tables(s, b, insts[b])
 
 
-def test_layered_and_streaming_in_one_solve():
-    # flops scaled so that some values pass 2^(32 - tb) - 2: those instances take the
-    # 64-bit streaming launch of the same solve, the others the layered words
+def test_layered_modes_and_streaming_in_one_solve():
+    # flops scaled so that the value bounds spread over rank tags, width tags and beyond
+    # the words (those instances saturate and take the 64-bit streaming launch of the
+    # same solve)
     base = synth.config_batch(2, B=6)
     factors = (1, 3, 6, 12, 40, 200)
     insts = [G.scaled(x, f) for x, f in zip(base, factors)]
-    fits = [G.layered_words(x) for x in insts]
-    assert any(fits) and not all(fits), fits
+    modes = [G.layered_words(x)[0] for x in insts]
+    fits = [G.layered_fits(x) for x in insts]
+    assert 0 in modes and 1 in modes and not all(fits), (modes, fits)
     check_batch(insts, tables=range(len(insts)))
 
 
-def test_layered_values_at_the_word_limit():
-    # values just below and just above the largest value the tagged words hold
+def test_layered_values_at_the_word_limits():
+    # value bounds just below and above the largest exact value of the rank tags, and
+    # just below and above that of the width tags
     x = synth.config_instance(2, 3)
-    tb = G.layered_tag_bits(x)
-    lim = 2**(32 - tb) - 2
     vb = G.value_bound(x)
-    lo = max(1, int(lim * 0.97) // vb)
-    hi = lim // vb + 1
-    insts = [G.scaled(x, lo), G.scaled(x, hi)]
-    assert G.layered_words(insts[0]) and not G.layered_words(insts[1])
-    check_batch(insts, tables=(0, 1))
+    _, tr, vr = G.layered_words(x)
+    insts = [G.scaled(x, max(1, int(vr * 0.97) // vb)), G.scaled(x, vr // vb + 1)]
+    _, tw, vw = G.layered_words(insts[1])
+    insts += [G.scaled(x, max(1, int(vw * 0.97) // vb)), G.scaled(x, vw // vb + 1)]
+    modes = [G.layered_words(y)[0] for y in insts]
+    fits = [G.layered_fits(y) for y in insts]
+    assert modes == [0, 1, 1, 1] and fits == [True, True, True, False], (modes, fits)
+    check_batch(insts, tables=range(4))
+
+
+@pytest.mark.parametrize("part", range(2))
+def test_layered_width_tags_random_tiny(part):
+    # flops scaled by 2^12: most tiny instances leave the rank tags
+    insts = [G.scaled(synth.random_tiny(9000 * part + k, Lmax=7, Dmax=16), 1 << 12) for k in range(300)]
+    assert sum(G.layered_words(x)[0] == 1 for x in insts) > 50
+    s, res = G.run(insts, Pcap=6, variant=LAYERED)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), (b, res[b], oracle[b])
+    for b in range(0, 300, 41):
+        if oracle[b]["status"] != 2:
+            check_tables(s, b, insts[b])
 
 
 def test_layered_graphs():
