@@ -147,12 +147,12 @@ def test_cost_tensor_sizes_match_workload_table():
 
 def test_describe_launch_without_a_device():
     # no GPU here: no resident shape can be sized, so the shape falls back to the layered
-    # sweep (position 1, one launch per later position, the streaming launch for the
-    # instances beyond its words), followed by the backtrack
+    # sweep (position 1, a launch per tag mode for each later position, the streaming
+    # launch for the instances beyond its words), followed by the backtrack
     dims = nest.make_dims(synth.config_batch(2, B=4))
     d = nest.describe_launch(dims)
     assert d["chunks"] == 1 and d["sweep_variant"] in (1, 2, 3)
-    per = {1: 3 + d["sweep_split"], 2: 4 + d["sweep_split"], 3: 2 + dims.Pcap + 1 + 1}
+    per = {1: 3 + d["sweep_split"], 2: 4 + d["sweep_split"], 3: 2 + 1 + 2 * (dims.Pcap - 1) + 1 + 1}
     assert d["kernels_per_chunk"] == per[d["sweep_variant"]]
     for v in (2, 3):
         assert nest.describe_launch(dims, nest.options(variant=v))["sweep_variant"] == v
