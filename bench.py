@@ -1,12 +1,13 @@
 """Benchmark of the Nest placement DP on GB300: DP relaxations/s and solves/s.
 
-One step = one nest_solve of a whole batch: prep, stage-cost build, strategy
-reduction, DP sweep and backtrack, inputs resident in HBM.  The default workload
-is the 32-layer dense transformer (hidden 4096) on 64 devices in three tiers,
-16 instances.  `value` counts the min-max transitions (j, m, c') of the
-recurrence per second; `solves_per_s` counts instances.
+One step = one nest_solve of a whole batch: prep, stage loads (cost build and
+strategy reduction), DP sweep and backtrack, inputs resident in HBM.  The default
+workload is the large sweep stress batch: 1024 instances of 128 mixed dense / MoE
+layers (hidden 4096, 8192 or 16384) on 4096 devices in four tiers, 672 strategies.
+`value` counts the min-max transitions (j, m, c') of the recurrence whose successor
+cell can hold a value, per second; `solves_per_s` counts instances.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 5] [--impl ours|reference]
 
 Under torchrun (N > 1) every rank solves its own batch (different seeds): the
 work is partitioned, so there is no collective on the data path (weak scaling);
@@ -120,6 +121,25 @@ def _count(x, with_strategies: bool) -> int:
     return tot
 
 
+_COUNTS = {}
+
+
+def _structure(x, with_strategies: bool):
+    """What the work counts depend on: instances of one workload share it."""
+    key = (int(x.L), int(x.D), int(x.unit), int(x.Pmax), tuple(int(x.tierG[int(c)]) for c in x.cand),
+           None if getattr(x, "succ", None) is None else tuple(int(v) for v in x.succ))
+    if with_strategies:
+        key += (tuple(map(tuple, np.asarray(x.strat).tolist())), tuple(int(v) for v in x.moe))
+    return key
+
+
+def _count_cached(x, with_strategies: bool) -> int:
+    key = (with_strategies,) + _structure(x, with_strategies)
+    if key not in _COUNTS:
+        _COUNTS[key] = _count(x, with_strategies)
+    return _COUNTS[key]
+
+
 def relaxations(x) -> int:
     """Min-max transitions (j, m, c') of the recurrence for one instance whose
     successor cell can hold a value: every cell (i, d, p, c) times its cut points j
@@ -127,7 +147,7 @@ def relaxations(x) -> int:
     allowed by the link tier, and next-link candidates c' allowed for that width.
     Transitions into successor cells that are empty by construction (too few layers
     or device units left for the remaining p - 1 stages) are not counted."""
-    return _count(x, False)
+    return _count_cached(x, False)
 
 
 def relaxations_with_strategies(x) -> int:
@@ -270,29 +290,43 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(instances, relax_total, seconds=12.0):
-    """The oracle as it stands, one instance per host thread, on all host cores."""
+def cpu_baseline(instances, seconds=12.0):
+    """The oracle as it stands, one instance per host thread on all host cores, over a
+    bounded sample of the batch: rounds of one instance per core (cycling through the
+    batch) until `seconds` have passed, at least one round."""
     from oracle import oracle as O
     from concurrent.futures import ThreadPoolExecutor
     O.lib()
     cores = os.cpu_count() or 1
+    n = min(cores, len(instances))
     t0 = time.perf_counter()
-    passes = 0
+    done, relax, rounds = 0, 0, 0
     with ThreadPoolExecutor(max_workers=cores) as ex:
         while True:
-            list(ex.map(oracle_solve, instances))
-            passes += 1
+            batch = [instances[(done + q) % len(instances)] for q in range(n)]
+            list(ex.map(oracle_solve, batch))
+            done += n
+            rounds += 1
+            relax += sum(relaxations(x) for x in batch)
             if time.perf_counter() - t0 >= seconds:
                 break
     dt = time.perf_counter() - t0
-    return {"value": passes * relax_total / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{passes} pass(es) over the {len(instances)}-instance batch, {dt:.1f} s",
-            "solves_per_s": passes * len(instances) / dt}
+    return {"value": relax / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} instance solves ({rounds} round(s) of {n} in parallel, cycling through the "
+                      f"{len(instances)}-instance batch), {dt:.1f} s",
+            "solves_per_s": done / dt}
 
 
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def bench_config(workload, instances, chunk, relax_total, words, ws):
+    """The `config` of the JSON line, the same for both arms."""
+    return {"workload": workload, "batch_per_gpu": len(instances), "chunk": chunk,
+            "relaxations_per_batch": relax_total, "cost_words_per_batch": words,
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)", "parallelism": f"replicas{ws}"}
 
 
 def run_reference(args, workload, instances, relax_total):
@@ -320,11 +354,14 @@ def run_reference(args, workload, instances, relax_total):
                 done_relax += sum(per[q] for q in idx)
     total = sum(times)
     value = done_relax / total
+    chunk = args.chunk if 0 < args.chunk < len(instances) else len(instances)
+    words = sum(cost_words(x) for x in instances)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
-            "data": "synthetic", "config": {"workload": workload, "batch": len(instances),
-                                            "reference": "CPU oracle (plain C), one instance per host thread"},
+            "data": "synthetic", "config": bench_config(workload, instances, chunk, relax_total, words, ws),
+            "reference": "CPU oracle (plain C), one instance per host thread; each step solves one instance "
+                         "per host core, cycling through the batch",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{n} instance(s) per step over {args.steps} steps"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -353,9 +390,9 @@ def job_totals(local_units: float, local_ms: float, dist=None, device=None):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 15 s of work)")
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--sweep-variant", type=int, default=0, choices=[0, 1, 2, 3],
                     help="DP sweep variant: 0 = the library's choice, 1 = resident, 2 = streaming, "
@@ -381,6 +418,10 @@ def main():
                     help="joint microbatch-size search: every problem solved with 1, 2, 4 and 8 samples "
                          "per microbatch, the best variant selected on the GPU")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = {1: 2000, 2: 2000, 3: 500, 4: 500, 5: 20}[args.workload]
+    if args.warmup is None:
+        args.warmup = 3 if args.workload == 5 else 20
     if args.warmup < 3:
         args.warmup = 3
 
@@ -509,14 +550,16 @@ def main():
     torch.cuda.synchronize(dev)
     dom_ms = kernel_ms(opts)[dom] if graph is None else wk[dom]
     clk = clocks.stop()
-    # per-kernel breakdown from a separate pass with events at every kernel boundary
-    bd = [make_opt() for _ in range(min(args.steps, 100))]
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    # per-kernel breakdown from a separate pass with events at every kernel boundary (a
+    # second or two of steps)
+    nbd = min(args.steps, 100, max(3, int(1500.0 / max(statistics.mean(step_ms), 1e-3))))
+    bd = [make_opt() for _ in range(nbd)]
     for o in bd:
         flush.zero_()
         step(o[0])
     torch.cuda.synchronize(dev)
     kms = kernel_ms(bd)
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     job_relax, total_ms = job_totals(relax_total, sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     value = job_relax / (ms_per_step * 1e-3)
@@ -526,6 +569,9 @@ def main():
 
     # end to end through the host-buffer entry point: H2D records, solve, D2H results
     e2e_steps = args.e2e_steps or min(args.steps, 500)
+    if group == 1:   # the device path's workspace is not needed any more
+        solver.workspace = None
+        torch.cuda.empty_cache()
     wsh = torch.empty(nest.workspace_size(dims, args.chunk, host=True), dtype=torch.uint8, device=dev)
     rec_pin = torch.from_numpy(records.ravel().copy()).pin_memory()
     costs_pin = torch.empty(B, dtype=torch.int64).pin_memory()
@@ -551,7 +597,7 @@ def main():
         costs_pin.copy_(solver.costs, non_blocking=True)
         plans_pin.copy_(solver.plans, non_blocking=True)
         stream.synchronize()
-    for _ in range(args.warmup):
+    for _ in range(min(args.warmup, 3)):
         host_step()
     if dist is not None:
         dist.barrier()
@@ -601,26 +647,28 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": stored_traffic(dom, workload),
                 "kernel": dom, "peak_source": f"{peaks['source']} hbm_gbs"}
-    # the stage-loads kernel (cost build + strategy reduction) against HBM: the bytes of
-    # the per-position loads table it must write, over its time in the breakdown pass
-    loads_bytes_all = sum(8 * x.Pmax * state_pairs(x) * (x.D // x.unit).bit_length() for x in instances)
-    roof_loads = {"bound": "hbm", "kernel": "stage_loads", "achieved": loads_bytes_all / (kms["stage_loads"] * 1e-3) / 1e9,
+    # the stage-loads kernel (cost build + strategy reduction) against HBM, on the cost
+    # builder's algorithmic bytes: 8 bytes per (stage, width, strategy) cost word written.
+    # The fused kernel reduces the words in shared memory instead of writing them (and of
+    # reading them back for the strategy reduction); its bound is integer arithmetic
+    k1_bytes = 8 * words
+    roof_loads = {"bound": "hbm", "kernel": "stage_loads", "achieved": k1_bytes / (kms["stage_loads"] * 1e-3) / 1e9,
                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                  "frac": loads_bytes_all / (kms["stage_loads"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "frac": k1_bytes / (kms["stage_loads"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
                   "traffic": stored_traffic("stage_loads", workload),
-                  "note": "integer-ALU bound: exact 64-bit collective prices, about 430 integer instructions "
-                          "per (stage, width, strategy) word (ncu: 9.5 M warp instructions for 709 K words)"}
+                  "cost_words_per_s": words / (kms["stage_loads"] * 1e-3),
+                  "note": "achieved = 8 B per cost word (the cost tensor the fused kernel never writes) over "
+                          "its time; integer-ALU bound: exact 64-bit collective prices, shared per strategy "
+                          "group"}
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(instances, relax_total, args.cpu_seconds)
+        cpu = cpu_baseline(instances, args.cpu_seconds)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
-                "config": {"workload": workload, "batch_per_gpu": B, "chunk": chunk,
-                           "relaxations_per_batch": relax_total, "cost_words_per_batch": words,
-                           "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
-                           "parallelism": f"replicas{ws}", "launch": plan},
+                "config": bench_config(workload, instances, chunk, relax_total, words, ws),
+                "launch": plan,
                 "solves_per_s": solves,
                 "relaxations_jmsc_per_s": job_relax / relax_total * relax_s_total / (ms_per_step * 1e-3),
                 "relaxations_jmsc_note": "the (j, m, s, c') count of the recurrence with the strategy axis, "
