@@ -83,19 +83,19 @@ __global__ void __launch_bounds__(kThreads) loads_kernel(PassArgs a, int pj_max)
             const int j = i + 1 + c0 + jj;
             const int64_t pair = row_offset(i, L) + c0 + jj;
             uint64_t *bk = bucket + jj * g.Kmax * rowp;
-            auto fold = [&](int m, int s, uint64_t w) {   // into bucket[m][pmax]
-                const int pm = w == kInf ? 0 : int(w & 0xFF);
-                if (pm == 0) return;
-                const uint64_t key = ((w >> 8) << 16) | uint64_t(s);
+            auto fold = [&](int m, int s, int64_t tau, int pm) {   // into bucket[m][pmax]
+                if (pm == 0) return;   // also a strategy that does not apply (tau < 0)
+                const uint64_t key = (uint64_t(tau) << 16) | uint64_t(s);
                 uint64_t *slot = bk + m * rowp + pm;
                 if (key < *slot) atomicMin(reinterpret_cast<unsigned long long *>(slot), key);
             };
             if (a.keep_costs) {
                 uint64_t *cout = reinterpret_cast<uint64_t *>(a.ws + a.w.cost) + int64_t(b) * a.w.cost_stride +
                                  pair * g.Kmax * g.Spad;
-                dense_group_words<true>(ph, smem, a.pl, g, i, j, gd, [&](int m, int s, uint64_t w) {
-                    cout[int64_t(m) * g.Spad + s] = w;
-                    fold(m, s, w);
+                dense_group_words<true>(ph, smem, a.pl, g, i, j, gd, [&](int m, int s, int64_t tau, int pm) {
+                    // the stage-cost word (tau << 8) | pmax, all ones where the strategy does not apply
+                    cout[int64_t(m) * g.Spad + s] = tau < 0 ? kInf : (uint64_t(tau) << 8) | uint64_t(pm);
+                    fold(m, s, tau, pm);
                 });
             } else {
                 dense_group_words<false>(ph, smem, a.pl, g, i, j, gd, fold);

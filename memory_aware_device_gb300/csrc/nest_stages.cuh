@@ -457,9 +457,9 @@ __device__ __forceinline__ int fit_positions(const PrepHdr *ph, int64_t rem, int
     return p;
 }
 
-// The width words (tau << 8) | pmax of stage (i, j) for every strategy of dense group
-// gd (equal t, cp), handed to emit(m, s, word) for every width m; all ones where a
-// strategy does not apply to a width.  A dense group is a run of strategy groups (equal
+// The stage time tau and the fitting positions pmax of stage (i, j) for every strategy
+// of dense group gd (equal t, cp), handed to emit(m, s, tau, pmax) for every width m;
+// tau = -1 where a strategy does not apply to a width or reaches the cap.  A dense group is a run of strategy groups (equal
 // t, cp, e) whose members differ in the ZeRO stage z and recompute r.  Per width the
 // collectives are priced once: the dense ones once per dense group, the expert ones
 // once per strategy group.  With S1 = coll(1, q) + coll(1, q / e) and
@@ -471,8 +471,8 @@ __device__ __forceinline__ int fit_positions(const PrepHdr *ph, int64_t rem, int
 template <bool kAll, typename Emit>
 __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsigned char *pb, const PrepLayout &pl,
                                                   const Geo &g, int i, int j, int gd, Emit emit) {
-    // kAll: also hand over the all-ones words of strategies that do not apply (only the
-    // kept stage-cost tensor wants them; the per-position loads skip them anyway)
+    // kAll: also hand over the strategies that do not apply (only the kept stage-cost
+    // tensor wants them; the per-position loads skip them anyway)
     const int K = ph->K, lu = ph->lu;
     const uint32_t *ss = reinterpret_cast<const uint32_t *>(pb + pl.ssort);
     const uint32_t *sg = reinterpret_cast<const uint32_t *>(pb + pl.sgrp);
@@ -487,7 +487,7 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
     if (!stage || ltc - lu > K - 1) {
         if (kAll)
             for (int m = 0; m < K; m++)
-                for (int q = q0; q < q1; q++) emit(m, int(ss[q] >> 16), kInf);
+                for (int q = q0; q < q1; q++) emit(m, int(ss[q] >> 16), int64_t(-1), 0);
         return;
     }
     const int64_t Fl = u.v[kFl], Pd = u.v[kPd], Pe = u.v[kPe], Ao = u.v[kAo], Aw = u.v[kAw], A2 = u.v[kA2];
@@ -506,11 +506,20 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
     const int64_t full0 = int64_t(ph->P - 1) * st0, full1 = int64_t(ph->P - 1) * st1;
     const int64_t opt = ph->opt, budget = ph->budget, M = ph->M;
     const int64_t owd = opt * Wd;
+    // strategy groups holding the whole (z, r) grid in order (eight members): their
+    // members are evaluated unrolled, every select folded
+    uint32_t grids = 0;
+    for (int gi = g0; gi < g1 && gi - g0 < 32; gi++) {
+        const int qa = int(sg[gi]), qb = int(sg[gi + 1]);
+        bool grid = qb - qa == 8;
+        for (int k = 0; k < 8 && grid; k++) grid = ((ss[qa + k] >> 12) & 7) == uint32_t(k >> 1 | (k & 1) << 2);
+        grids |= uint32_t(grid) << (gi - g0);
+    }
     for (int m = 0; m < K; m++) {
         const int lq = lu + m - ltc;
         if (lq < 0) {
             if (kAll)
-                for (int q = q0; q < q1; q++) emit(m, int(ss[q] >> 16), kInf);
+                for (int q = q0; q < q1; q++) emit(m, int(ss[q] >> 16), int64_t(-1), 0);
             continue;
         }
         const int tk = ph->tier_log[lu + m];
@@ -522,7 +531,7 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
             const int lqe = lq - le;
             if (lqe < 0 || (le > 0 && nM == 0)) {
                 if (kAll)
-                    for (int q = qa; q < qb; q++) emit(m, int(ss[q] >> 16), kInf);
+                    for (int q = qa; q < qb; q++) emit(m, int(ss[q] >> 16), int64_t(-1), 0);
                 continue;
             }
             // the strategy group's expert degree: its weights, AllToAlls and expert sync
@@ -530,9 +539,12 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
             const int64_t ep = net.coll(1, le, ph->tier_log[ltc + le], 4 * up_shift(A2, ltc), 4 * nM);
             const int64_t S1 = D1 + net.coll(1, lqe, tk, We, nM);
             const int64_t S2 = D2 + net.coll(2, lqe, tk, We, nM);
+            // the syncs amortised over M: ceil(S2 / M), and from S1 = qM + rm both
+            // ceil(S1 / M) = q + (rm > 0) and ceil(2 S1 / M) = 2q + ceil(2 rm / M)
             const int64_t dM0 = int64_t(divide_up(uint64_t(S2), uint64_t(M), ph->Mdiv));       // z = 0
-            const int64_t dM12 = int64_t(divide_up(uint64_t(2 * S1), uint64_t(M), ph->Mdiv));  // z = 1, 2
-            const int64_t dM3 = int64_t(divide_up(uint64_t(S1), uint64_t(M), ph->Mdiv));       // z = 3
+            const int64_t q1M = int64_t(divide(uint64_t(S1), ph->Mdiv)), rm = S1 - q1M * M;
+            const int64_t dM3 = q1M + (rm > 0);                                                  // z = 3
+            const int64_t dM12 = 2 * q1M + (2 * rm > M ? 2 : rm > 0 ? 1 : 0);                 // z = 1, 2
             const int64_t full = Wd + We;
             const int64_t sh = wdq + up_shift(We, lqe);
             const int64_t osh = owdq + up_shift(opt * We, lqe);
@@ -540,25 +552,21 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
             const int64_t r0 = cmp0 + ep, r1 = cmp1 + ep;
             const int64_t t00 = up_shift(r0, lq), t10 = up_shift(r1, lq);            // z < 3
             const int64_t t03 = up_shift(r0 + S2, lq), t13 = up_shift(r1 + S2, lq);  // z = 3
-            // one member: its word from its (z, r)
+            // one member: its time and fitting positions from its (z, r)
             auto member = [&](int q, int z, int r) {
                 const int s = int(ss[q] >> 16);
                 const int64_t tau = (z == 3 ? (r ? t13 : t03) : (r ? t10 : t00)) + (z == 0 ? dM0 : z == 3 ? dM3 : dM12);
-                uint64_t word = kInf;
-                if (tau < kCap) {
-                    const int64_t stat = (z == 0 ? sz0 : z == 1 ? sz1 : z == 2 ? sz2 : sz3) + (r ? act1 : act0);
-                    const int pmax = stat > budget ? 0
-                                                   : fit_positions(ph, budget - stat, r ? st1 : st0, r ? full1 : full0,
-                                                                   r ? inv1 : inv0, lq);
-                    word = (uint64_t(tau) << 8) | uint64_t(pmax);
+                if (tau >= kCap) {
+                    if (kAll) emit(m, s, int64_t(-1), 0);
+                    return;
                 }
-                emit(m, s, word);
+                const int64_t stat = (z == 0 ? sz0 : z == 1 ? sz1 : z == 2 ? sz2 : sz3) + (r ? act1 : act0);
+                const int pmax = stat > budget ? 0
+                                               : fit_positions(ph, budget - stat, r ? st1 : st0, r ? full1 : full0,
+                                                               r ? inv1 : inv0, lq);
+                emit(m, s, tau, pmax);
             };
-            // the whole (z, r) grid in order (eight members): unrolled, every select folds
-            bool grid = qb - qa == 8;
-            if (grid)
-                for (int k = 0; k < 8; k++) grid &= ((ss[qa + k] >> 12) & 7) == uint32_t(k >> 1 | (k & 1) << 2);
-            if (grid) {
+            if (gi - g0 < 32 && (grids >> (gi - g0)) & 1) {
 #pragma unroll
                 for (int k = 0; k < 8; k++) member(qa + k, k >> 1, k & 1);
             } else {
