@@ -150,16 +150,19 @@ __global__ void __launch_bounds__(256) sweep_layer1_kernel(PassArgs a) {
 template <int CT, int RT, int TW>
 __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, int p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    pdl_wait();
-    pdl_trigger();
     const Geo &g = a.g;
     const LayPlan lp = lay_plan(g, CT, RT);
     const int NB = 1 + lp.NIB * CT;
     const int b = blockIdx.x / NB, blk = blockIdx.x % NB;
     PrepHdr *ph = prep_hdr(a, b);
-    if (ph->status != NEST_SOLVED || p > ph->P) return;   // uniform over the CTA
+    // the instance's tag mode comes from the prep and stage-loads tables, which are
+    // complete by now (every launch of this sweep waits for its predecessor before it
+    // lets its own dependents start): the other mode's CTAs leave at once
+    if (ph->status != NEST_SOLVED || p > ph->P || lay_words(ph).mode != TW) return;
+    pdl_wait();
+    pdl_trigger();
     const LayWords w = lay_words(ph);
-    if (lay_leaves(ph) || w.mode != TW) return;   // the streaming sweep or the other mode's launch
+    if (lay_leaves(ph)) return;   // the streaming sweep solves it (a flag the previous launch may set)
     const int L = ph->L, C = ph->C, K = ph->K, Du = ph->Du;
     const bool first = blk == 0;
     const int c = first ? 0 : (blk - 1) % CT;

@@ -382,6 +382,24 @@ struct Net {
         const int64_t steps = cnt * phi * ((int64_t(1) << ln) - 1) * ph->lat[tr];
         return steps + int64_t(divide_up(uint64_t(per_device) * 1000, uint64_t(ph->bw[tr]), ph->bwdiv[tr]));
     }
+    // coll(1, ...) and coll(2, ...) of the same group, tier and bytes with one division:
+    // the phi = 2 bytes per device are 2 x1 - b with x1 = V - floor(V / n) and
+    // b = bit (ln - 1) of V, so with x1 * 1000 = q bw + r their ceiling over bw is
+    // 2q + ceil(y / bw), y = 2r - 1000 b, and -bw <= -1000 <= y < 2 bw (bw >= 1000).
+    __device__ __forceinline__ void coll12(int ln, int tr, int64_t V, int64_t cnt, int64_t &c1, int64_t &c2) const {
+        if (ln == 0 || V == 0) {
+            c1 = c2 = 0;
+            return;
+        }
+        const int64_t x1 = V - (V >> ln);
+        const int64_t steps = cnt * ((int64_t(1) << ln) - 1) * ph->lat[tr];
+        const int64_t bw = ph->bw[tr];
+        const int64_t q = int64_t(divide(uint64_t(x1) * 1000, ph->bwdiv[tr]));
+        const int64_t r = x1 * 1000 - q * bw;
+        const int64_t y = 2 * r - 1000 * ((V >> (ln - 1)) & 1);
+        c1 = steps + q + (r > 0);
+        c2 = 2 * steps + 2 * q + (y > bw ? 2 : y > 0 ? 1 : y > -bw ? 0 : -1);
+    }
 };
 
 // Largest aw over layers [x, y), x < y, from the sparse table.
@@ -439,10 +457,9 @@ __device__ __forceinline__ bool pair_sums(const PrepHdr *ph, const unsigned char
 // pmax of one strategy (§3.3): the largest position p <= P whose stash still fits,
 // 1F1B (p - 1 stashed microbatches) or GPipe (all ceil(M / q) of a replica's).
 // rem = budget - static >= 0; full = (P - 1) * stash, inv ~ 1 / stash.
-__device__ __forceinline__ int fit_positions(const PrepHdr *ph, int64_t rem, int64_t st, int64_t full, float inv,
-                                             int lq) {
-    const int P = ph->P;
-    if (ph->schedule == 1) {
+__device__ __forceinline__ int fit_positions(const PrepHdr *ph, bool gpipe, int P, int64_t rem, int64_t st,
+                                             int64_t full, float inv, int lq) {
+    if (gpipe) {
         // GPipe: ceil(M / q) stashed microbatches; exact 128-bit product
         const uint64_t inflight = uint64_t((ph->M + (int64_t(1) << lq) - 1) >> lq);
         const uint64_t lo = uint64_t(st) * inflight, hi = __umul64hi(uint64_t(st), inflight);
@@ -505,7 +522,15 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
     const float inv0 = st0 > 0 ? 1.0f / float(st0) : 0.0f, inv1 = st1 > 0 ? 1.0f / float(st1) : 0.0f;
     const int64_t full0 = int64_t(ph->P - 1) * st0, full1 = int64_t(ph->P - 1) * st1;
     const int64_t opt = ph->opt, budget = ph->budget, M = ph->M;
+    const int P = ph->P;
+    const bool gpipe = ph->schedule == 1;
     const int64_t owd = opt * Wd;
+    // the expert AllToAlls of each strategy group (they do not depend on the width)
+    int64_t epv[16];
+    for (int gi = g0; gi < g1 && gi - g0 < 16; gi++) {
+        const int le = (ss[sg[gi]] >> 8) & 15;
+        epv[gi - g0] = net.coll(1, le, ph->tier_log[ltc + le], 4 * up_shift(A2, ltc), 4 * nM);
+    }
     // strategy groups holding the whole (z, r) grid in order (eight members): their
     // members are evaluated unrolled, every select folded
     uint32_t grids = 0;
@@ -523,7 +548,8 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
             continue;
         }
         const int tk = ph->tier_log[lu + m];
-        const int64_t D1 = net.coll(1, lq, tk, Wd, nL), D2 = net.coll(2, lq, tk, Wd, nL);
+        int64_t D1, D2;
+        net.coll12(lq, tk, Wd, nL, D1, D2);
         const int64_t wdq = up_shift(Wd, lq), owdq = up_shift(owd, lq);
         for (int gi = g0; gi < g1; gi++) {
             const int qa = int(sg[gi]), qb = int(sg[gi + 1]);
@@ -536,9 +562,11 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
             }
             // the strategy group's expert degree: its weights, AllToAlls and expert sync
             const int64_t We = up_shift(Pe, lt + le);
-            const int64_t ep = net.coll(1, le, ph->tier_log[ltc + le], 4 * up_shift(A2, ltc), 4 * nM);
-            const int64_t S1 = D1 + net.coll(1, lqe, tk, We, nM);
-            const int64_t S2 = D2 + net.coll(2, lqe, tk, We, nM);
+            const int64_t ep = gi - g0 < 16 ? epv[gi - g0]
+                                            : net.coll(1, le, ph->tier_log[ltc + le], 4 * up_shift(A2, ltc), 4 * nM);
+            int64_t E1, E2;
+            net.coll12(lqe, tk, We, nM, E1, E2);
+            const int64_t S1 = D1 + E1, S2 = D2 + E2;
             // the syncs amortised over M: ceil(S2 / M), and from S1 = qM + rm both
             // ceil(S1 / M) = q + (rm > 0) and ceil(2 S1 / M) = 2q + ceil(2 rm / M)
             const int64_t dM0 = int64_t(divide_up(uint64_t(S2), uint64_t(M), ph->Mdiv));       // z = 0
@@ -562,8 +590,8 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
                 }
                 const int64_t stat = (z == 0 ? sz0 : z == 1 ? sz1 : z == 2 ? sz2 : sz3) + (r ? act1 : act0);
                 const int pmax = stat > budget ? 0
-                                               : fit_positions(ph, budget - stat, r ? st1 : st0, r ? full1 : full0,
-                                                               r ? inv1 : inv0, lq);
+                                               : fit_positions(ph, gpipe, P, budget - stat, r ? st1 : st0,
+                                                               r ? full1 : full0, r ? inv1 : inv0, lq);
                 emit(m, s, tau, pmax);
             };
             if (gi - g0 < 32 && (grids >> (gi - g0)) & 1) {

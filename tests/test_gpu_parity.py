@@ -297,6 +297,24 @@ def test_random_tiny_batches(part, variant, factor):
             check_tables(s, b, insts[b])
 
 
+def test_lowest_bandwidth_tiers():
+    # every tier at the smallest allowed bandwidth (1000 bytes/us): every ring transfer's
+    # bytes divide exactly, so the rounding cases of the collective prices (shared
+    # between the AllReduce and the AllGather of a group) all occur
+    insts = []
+    for k in range(200):
+        x = synth.random_tiny(41000 + k, Lmax=7, Dmax=16)
+        x.tierBw = np.full(len(x.tierBw), 1000, dtype=np.int64) + (k % 2) * np.arange(len(x.tierBw))
+        insts.append(x)
+    s, res = G.run(insts, Pcap=6)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), (b, res[b], oracle[b])
+    for b in range(0, 200, 13):
+        if oracle[b]["status"] != 2:
+            check_tables(s, b, insts[b])
+
+
 def test_ragged_chunks_and_mixed_shapes():
     """Instances of different sizes in one batch, processed in ragged chunks."""
     insts = synth.config_batch(2, B=5) + synth.config_batch(1) + \
