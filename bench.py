@@ -219,9 +219,12 @@ def measured_relax_peak(wide: int = 0):
 
 def relax_peak_mode(instances, plan) -> int:
     """Which relaxation peak the sweep's roofline divides by, as the microbenchmark's mode:
-    2 = tagged 32-bit words (batches of at most two link candidates: one max and one min
-    per candidate and cell), 0 = plain 32-bit words (max, compare, two selects), 1 = 64-bit
-    words (a streaming sweep runs on those)."""
+    2 = tagged 32-bit words (the layered sweep, and resident batches of at most two link
+    candidates: one max and one min per candidate and cell), 0 = plain 32-bit words (max,
+    compare, two selects), 1 = 64-bit words (a streaming sweep runs on those).  A batch
+    whose instances take different words (a split resident sweep, or instances whose
+    values need 64-bit words) is reported against the peak of its fastest words, an upper
+    bound of the batch's effective peak: the fraction is then a lower bound."""
     if plan.get("sweep_variant") == 3:
         return 2   # layered: tagged 32-bit words, one max and one min per pair and cell
     if plan.get("sweep_variant") == 2:

@@ -295,13 +295,17 @@ int nest_select_best(const int64_t *costs, int32_t B, int32_t group, int32_t *be
  * memory is a fixed array of NEST_STATIC_SCRATCH_BYTES inside the library, held by
  * every GPU that loads the library until the process exits.  The call allocates
  * nothing and frees nothing.  Returns NEST_E_WORKSPACE when the batch (or chunk,
- * opt->chunk) needs more scratch than that - nest_workspace_size() tells how much -
- * and otherwise what nest_solve returns.  The first call made with a device current
- * looks up the array's device address for that device; make that first call before
- * any stream capture.  All calls share the array and it keeps the last call's
- * contents (nothing in it needs clearing: the solve writes every scratch word before
- * reading it); calls whose work overlaps on the GPU race on it, so the caller must
- * serialise them (one stream, or an event between them). */
+ * opt->chunk) needs more scratch than that - nest_workspace_size() tells how much -,
+ * NEST_E_INVALID with NEST_KEEP_COSTS (the stage-cost tensor would land in the array,
+ * out of the caller's reach), and otherwise what nest_solve returns.  A call made
+ * outside a stream capture looks up the array's device address for the current device
+ * (so a device reset does not leave a stale address behind); a call made while its
+ * stream is being captured reuses the address of the last such lookup on that device,
+ * so make one call before capturing (else NEST_E_INVALID).  All calls share the array
+ * and it keeps the last call's contents (nothing in it needs clearing: the solve
+ * writes every scratch word before reading it); calls whose work overlaps on the GPU
+ * race on it, so the caller must serialise them (one stream, or an event between
+ * them). */
 #define NEST_STATIC_SCRATCH_BYTES (64u << 20)
 int nest_solve_static(const nest_dims *dims, const void *records, int64_t *costs_out, void *plans_out,
                       void *stream, const nest_options *opt);
