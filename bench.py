@@ -38,7 +38,7 @@ UNIT = "relaxations/s"
 KERNELS = ("prep", "stage_loads", "dp_sweep", "backtrack")
 NEV = len(KERNELS) + 1   # events per chunk
 KERNEL_SRC = {"prep": ("nest_prep.cu",), "stage_loads": ("nest_loads.cu",),
-              "dp_sweep": ("nest_sweep.cu", "nest_sweep_res_a.cu", "nest_sweep_res_b.cu"),
+              "dp_sweep": ("nest_sweep.cu", "nest_sweep_res_a.cu", "nest_sweep_res_b.cu", "nest_layered.cu"),
               "backtrack": ("nest_backtrack.cu",)}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -371,11 +371,13 @@ def run_reference(args, workload, instances, relax_total):
     print(json.dumps(line), flush=True)
 
 
-def rank_instances(workload_id: int, rank: int):
+def rank_instances(workload_id: int, rank: int, batch: int = 0):
     """The batch one rank solves: its own B instances (seeds 1000 w + rank B + b), so
-    ranks share nothing and need no exchange (the tiny workload is one fixed instance)."""
+    ranks share nothing and need no exchange (the tiny workload is one fixed instance);
+    `batch` > 0 takes the first `batch` of them."""
     B = synth.CONFIG_BATCH[workload_id]
-    return synth.config_batch(workload_id, B=B, first=rank * B if workload_id != 1 else 0)
+    n = min(batch, B) if batch > 0 else B
+    return synth.config_batch(workload_id, B=n, first=rank * B if workload_id != 1 else 0)
 
 
 def job_totals(local_units: float, local_ms: float, dist=None, device=None):
@@ -396,6 +398,9 @@ def main():
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 15 s of work)")
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--batch", type=int, default=0,
+                    help="solve only the first N instances of the workload (0 = its whole batch); for "
+                         "profiling captures on a small case")
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--sweep-variant", type=int, default=0, choices=[0, 1, 2, 3],
                     help="DP sweep variant: 0 = the library's choice, 1 = resident, 2 = streaming, "
@@ -430,8 +435,8 @@ def main():
 
     rank, local_rank, ws = dist_env()
     workload = f"{synth.CONFIG_NAMES[args.workload]}"
-    B = synth.CONFIG_BATCH[args.workload]
-    instances = rank_instances(args.workload, rank)
+    instances = rank_instances(args.workload, rank, args.batch)
+    B = len(instances)
     if args.topology == "torus":
         if args.workload != 2:
             raise SystemExit("--topology torus applies to workload 2 (64 devices)")
