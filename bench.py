@@ -317,7 +317,8 @@ def cpu_baseline(instances, seconds=12.0):
     return {"value": relax / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{done} instance solves ({rounds} round(s) of {n} in parallel, cycling through the "
                       f"{len(instances)}-instance batch), {dt:.1f} s",
-            "solves_per_s": done / dt}
+            "solves_per_s": done / dt,
+            "core_s_per_instance": dt * n / done}
 
 
 def dist_env():
