@@ -162,7 +162,12 @@ typedef struct {
     int32_t sweep_variant;  /* 0 = auto; 1 = rows resident in shared memory (NEST_E_LIMITS
                                if they do not fit, or with sweep_cluster 1 when Pcap > 1:
                                rows go to the next position's CTA, which must be another
-                               one); 2 = rows streamed from global memory */
+                               one); 2 = rows streamed from global memory (64-bit words);
+                               3 = layered: one launch per pipeline position over every
+                               instance, 32-bit tagged words (NEST_E_LIMITS beyond four
+                               candidates; instances whose values the words cannot hold
+                               are solved again by a streaming launch of the same call).
+                               The choice changes no result. */
     int64_t spin_limit;     /* polls before a device wait gives up (each poll suspends for at
                                most 20 us): 0 = default (2^16, about a second); a negative
                                value makes every wait give up at once, which exercises the
@@ -193,7 +198,8 @@ size_t nest_plan_bytes(const nest_dims *dims);
 /* Device workspace bytes that nest_solve needs for passes of `chunk` instances
  * (chunk <= 0 means dims->B).  0 when dims break the limits.  The workspace holds,
  * per instance of a chunk, the derived per-instance tables, the per-position
- * strategy loads, and the DP value and argument tables. */
+ * strategy loads, the DP value and argument tables and a 32-bit copy of the values
+ * (read by the layered sweep). */
 size_t nest_workspace_size(const nest_dims *dims, int32_t chunk);
 
 /* The same plus room for the stage-cost tensor cost[pair(i, j)][m][s] (8 bytes per
@@ -259,8 +265,10 @@ int nest_workspace_layout(const nest_dims *dims, int32_t chunk, nest_ws_layout *
  * Returns NEST_OK, NEST_E_INVALID (null pointer, bad option) or NEST_E_LIMITS. */
 typedef struct {
     int32_t chunks;             /* passes through the kernels */
-    int32_t kernels_per_chunk;  /* launches per pass: prep, stage loads, sweep (1 or 2), backtrack */
-    int32_t sweep_variant;      /* 1 = rows resident in shared memory, 2 = streamed from global memory */
+    int32_t kernels_per_chunk;  /* launches per pass: prep, stage loads, the sweep (1 or 2 resident
+                                   or streaming launches; layered: 1 + 2 (Pcap - 1) + 1), backtrack */
+    int32_t sweep_variant;      /* 1 = rows resident in shared memory, 2 = streamed from global
+                                   memory, 3 = layered (one launch per position and tag mode) */
     int32_t sweep_cluster;      /* CTAs per instance */
     int32_t sweep_jsplit;       /* threads per DP cell */
     int32_t sweep_threads;      /* threads per CTA */
