@@ -562,6 +562,16 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
             }
             // the strategy group's expert degree: its weights, AllToAlls and expert sync
             const int64_t We = up_shift(Pe, lt + le);
+            const int64_t full = Wd + We;
+            const int64_t sh = wdq + up_shift(We, lqe);
+            const int64_t osh = owdq + up_shift(opt * We, lqe);
+            const int64_t sz0 = 2 * full + opt * full, sz1 = 2 * full + osh, sz2 = full + sh + osh, sz3 = 2 * sh + osh;
+            // Memory shrinks as the ZeRO stage grows (sz0 >= sz1 >= sz2 >= sz3: each of
+            // weights, gradients and optimizer states is at most its unsharded size), so
+            // when even ZeRO-3 with the smaller activation exceeds the budget, no member
+            // fits the first position and none reaches a per-position load: the group
+            // is not priced (only the kept cost tensor wants its words)
+            if (!kAll && sz3 + (act0 < act1 ? act0 : act1) > budget) continue;
             const int64_t ep = gi - g0 < 16 ? epv[gi - g0]
                                             : net.coll(1, le, ph->tier_log[ltc + le], 4 * up_shift(A2, ltc), 4 * nM);
             int64_t E1, E2;
@@ -573,10 +583,6 @@ __device__ __forceinline__ void dense_group_words(const PrepHdr *ph, const unsig
             const int64_t q1M = int64_t(divide(uint64_t(S1), ph->Mdiv)), rm = S1 - q1M * M;
             const int64_t dM3 = q1M + (rm > 0);                                                  // z = 3
             const int64_t dM12 = 2 * q1M + (2 * rm > M ? 2 : rm > 0 ? 1 : 0);                 // z = 1, 2
-            const int64_t full = Wd + We;
-            const int64_t sh = wdq + up_shift(We, lqe);
-            const int64_t osh = owdq + up_shift(opt * We, lqe);
-            const int64_t sz0 = 2 * full + opt * full, sz1 = 2 * full + osh, sz2 = full + sh + osh, sz3 = 2 * sh + osh;
             const int64_t r0 = cmp0 + ep, r1 = cmp1 + ep;
             const int64_t t00 = up_shift(r0, lq), t10 = up_shift(r1, lq);            // z < 3
             const int64_t t03 = up_shift(r0 + S2, lq), t13 = up_shift(r1 + S2, lq);  // z = 3
