@@ -55,7 +55,7 @@ struct LayPlan {
     int ROWW;    // words per shared row
     int Emax;    // (m, c') pairs per row block, at most
     int NIB;     // row blocks of 8 states per candidate (states 1 .. Nmax-1)
-    int64_t mbar, X, rk, dec, A, B, total;
+    int64_t mbar, X, rk, dec, fin, A, B, total;
 };
 
 __host__ __device__ inline LayPlan lay_plan(const Geo &g, int CT, int RT) {
@@ -75,6 +75,8 @@ __host__ __device__ inline LayPlan lay_plan(const Geo &g, int CT, int RT) {
     off += 4 * 16 * CT;
     s.dec = off;                         // int32 [Emax]: (m << 4) | c'
     off = align_up(off + 4 * int64_t(s.Emax), 16);
+    s.fin = off;                         // uint8 [2][16][8]: per buffer and width, byte r = row r has a load
+    off += 2 * 16 * 8;
     s.A = off;                           // uint32 [2][Emax][RT]
     off += 2 * 4 * int64_t(s.Emax) * RT;
     s.B = off;                           // uint32 [2][CT][ROWW]
@@ -178,6 +180,9 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
     int *dec = reinterpret_cast<int *>(smem + lp.dec);        // [Emax]: (m << 4) | c'
     uint32_t *As = reinterpret_cast<uint32_t *>(smem + lp.A);
     uint32_t *Bs = reinterpret_cast<uint32_t *>(smem + lp.B);
+    // per buffer and width m: a word whose byte r is set when row r has a finite load at
+    // this cut point; a width with none relaxes nothing (max(no value, B) = no value)
+    uint64_t *finw = reinterpret_cast<uint64_t *>(smem + lp.fin);
 
     // the widths a row block admits with each next-link candidate
     const int mlimc = first ? K - 1 : (ph->mlim[c] < K - 1 ? ph->mlim[c] : K - 1);
@@ -222,6 +227,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
         }
         // every shared row starts as caps (no value); the copies fill d = 1 .. Dx
         for (int e = tid; e < 2 * CT * lp.ROWW; e += NT) Bs[e] = w.nmask;
+        for (int e = tid; e < 2 * 16; e += NT) finw[e] = 0;   // bytes of rows >= RT stay 0
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
@@ -258,6 +264,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
             if (q >= npair) continue;
             const int r = q / K, m = q % K, i = i0 + r;
             const int64_t base = pre[k] == kInf ? -1 : int64_t(pre[k] >> 16) + Xs[int64_t(i) * CT + c];
+            reinterpret_cast<unsigned char *>(finw + buf * 16 + m)[r] = base < 0 ? 0 : 1;
 #pragma unroll
             for (int c2 = 0; c2 < CT; c2++) {
                 const int e = rk[c2 * 16 + m];
@@ -333,6 +340,9 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                         }
                 }
                 const uint32_t *Ab = As + buf * lp.Emax * RT;
+                // the widths with a finite load in some row at this cut point
+                uint32_t fmask = 0;
+                for (int m = 0; m < K; m++) fmask |= uint32_t(finw[buf * 16 + m] != 0) << m;
                 auto relax = [&](uint4 B, int e, uint32_t tag) {
                     const uint32_t bb[4] = {B.x | tag, B.y | tag, B.z | tag, B.w | tag};
                     uint32_t aa[RT];
@@ -357,12 +367,14 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                     const int *rkc = rk + c2 * 16;
                     const uint4 U0 = *reinterpret_cast<const uint4 *>(row + 4 * t);       // B[4t+1 .. 4t+4]
                     const uint4 U1 = *reinterpret_cast<const uint4 *>(row + 4 * t - 4);   // B[4t-3 .. 4t]
-                    relax(make_uint4(U1.w, U0.x, U0.y, U0.z), rkc[0], TW ? 0u : uint32_t(rkc[0]));   // 2^0
-                    if (mm >= 1) relax(make_uint4(U1.z, U1.w, U0.x, U0.y), rkc[1], TW ? 1u : uint32_t(rkc[1]));
-                    if (mm >= 2) relax(U1, rkc[2], TW ? 2u : uint32_t(rkc[2]));                      // 2^2
+                    if (fmask & 1) relax(make_uint4(U1.w, U0.x, U0.y, U0.z), rkc[0], TW ? 0u : uint32_t(rkc[0]));   // 2^0
+                    if (mm >= 1 && (fmask & 2))
+                        relax(make_uint4(U1.z, U1.w, U0.x, U0.y), rkc[1], TW ? 1u : uint32_t(rkc[1]));
+                    if (mm >= 2 && (fmask & 4)) relax(U1, rkc[2], TW ? 2u : uint32_t(rkc[2]));   // 2^2
                     for (int m = 3; m <= mm; m++)
-                        relax(*reinterpret_cast<const uint4 *>(row + 4 * t - (1 << m)), rkc[m],
-                              TW ? uint32_t(m) : uint32_t(rkc[m]));
+                        if ((fmask >> m) & 1)
+                            relax(*reinterpret_cast<const uint4 *>(row + 4 * t - (1 << m)), rkc[m],
+                                  TW ? uint32_t(m) : uint32_t(rkc[m]));
                     if constexpr (TW) {
                         // this candidate's best (v, m) replaces the cut point's only when
                         // strictly smaller: equal ones keep the smaller c'
