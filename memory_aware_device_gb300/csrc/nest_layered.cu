@@ -359,6 +359,8 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
 #pragma unroll
                         for (int k = 0; k < kLCols; k++) cw[r][k] = min(cw[r][k], max(aa[r], bb[k]));
                 };
+                // a cut point whose stages fit no strategy at this position gives nothing
+                if (fmask != 0) {
 #pragma unroll
                 for (int c2 = 0; c2 < CT; c2++) {
                     const int mm = lim[c2] < mwarp ? lim[c2] : mwarp;
@@ -399,6 +401,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                         rw[r][k] = take ? cand : rw[r][k];
                         rj[r][k] = take ? (TW ? uint32_t(j) << 4 | jc[TW ? r : 0][k] : uint32_t(j)) : rj[r][k];
                     }
+                }
             }
             if (more) build(j + 1, buf ^ 1);
             aborted = __syncthreads_or(!ok) != 0;
