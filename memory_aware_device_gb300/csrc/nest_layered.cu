@@ -75,8 +75,8 @@ __host__ __device__ inline LayPlan lay_plan(const Geo &g, int CT, int RT) {
     off += 4 * 16 * CT;
     s.dec = off;                         // int32 [Emax]: (m << 4) | c'
     off = align_up(off + 4 * int64_t(s.Emax), 16);
-    s.fin = off;                         // uint8 [2][16][8]: per buffer and width, byte r = row r has a load
-    off += 2 * 16 * 8;
+    s.fin = off;                         // uint32 [3]: per cut point (in turn), the widths with a load
+    off += 16;
     s.A = off;                           // uint32 [2][Emax][RT]
     off += 2 * 4 * int64_t(s.Emax) * RT;
     s.B = off;                           // uint32 [2][CT][ROWW]
@@ -180,9 +180,11 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
     int *dec = reinterpret_cast<int *>(smem + lp.dec);        // [Emax]: (m << 4) | c'
     uint32_t *As = reinterpret_cast<uint32_t *>(smem + lp.A);
     uint32_t *Bs = reinterpret_cast<uint32_t *>(smem + lp.B);
-    // per buffer and width m: a word whose byte r is set when row r has a finite load at
-    // this cut point; a width with none relaxes nothing (max(no value, B) = no value)
-    uint64_t *finw = reinterpret_cast<uint64_t *>(smem + lp.fin);
+    // per cut point, a mask of the widths m for which some row has a finite load; a width
+    // with none relaxes nothing (max(no value, B) = no value).  Three words in turn: the
+    // one built for cut point j + 1, the one read for j, and the one read for j - 1, which
+    // is cleared while j is relaxed (no barrier separates a clear from the next build)
+    uint32_t *fmw = reinterpret_cast<uint32_t *>(smem + lp.fin);
 
     // the widths a row block admits with each next-link candidate
     const int mlimc = first ? K - 1 : (ph->mlim[c] < K - 1 ? ph->mlim[c] : K - 1);
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
         }
         // every shared row starts as caps (no value); the copies fill d = 1 .. Dx
         for (int e = tid; e < 2 * CT * lp.ROWW; e += NT) Bs[e] = w.nmask;
-        for (int e = tid; e < 2 * 16; e += NT) finw[e] = 0;   // bytes of rows >= RT stay 0
+        if (tid < 3) fmw[tid] = 0;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
@@ -256,15 +258,16 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
             }
         }
     };
-    auto build = [&](int j, int buf) {
+    auto build = [&](int j, int buf, int slot) {   // every thread calls it
         uint32_t *Ab = As + buf * lp.Emax * RT;
+        uint32_t bits = 0;   // widths with a finite load in one of this thread's rows
 #pragma unroll
         for (int k = 0; k < kPre; k++) {
             const int q = tid + k * NT;
             if (q >= npair) continue;
             const int r = q / K, m = q % K, i = i0 + r;
             const int64_t base = pre[k] == kInf ? -1 : int64_t(pre[k] >> 16) + Xs[int64_t(i) * CT + c];
-            reinterpret_cast<unsigned char *>(finw + buf * 16 + m)[r] = base < 0 ? 0 : 1;
+            bits |= base < 0 ? 0u : 1u << m;
 #pragma unroll
             for (int c2 = 0; c2 < CT; c2++) {
                 const int e = rk[c2 * 16 + m];
@@ -274,6 +277,8 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                 Ab[e * RT + r] = base < 0 ? ~0u : (vv << w.tb) | uint32_t(TW ? m : e);
             }
         }
+        bits = __reduce_or_sync(0xFFFFFFFFu, bits);
+        if ((tid & 31) == 0 && bits) atomicOr(&fmw[slot], bits);
     };
     auto issue = [&](int j, int buf) {   // thread 0: the B rows (j, c') of position p - 1
         uint32_t bytes = 0;
@@ -308,10 +313,13 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
             pending = 1;
         }
         fetch(jlo);
-        build(jlo, 0);
+        build(jlo, 0, 0);
         __syncthreads();
+        int slot = 0;   // mask word of cut point j: (j - jlo) mod 3
         for (int j = jlo; j <= jhi; j++) {
             const int buf = (j - jlo) & 1;
+            const int slot1 = slot == 2 ? 0 : slot + 1, slot2 = slot1 == 2 ? 0 : slot1 + 1;
+            if (tid == 0) fmw[slot2] = 0;   // last read for cut point j - 1, next built for j + 2
             const bool more = j < jhi && !aborted;
             if (more) {
                 if (tid == 0) {
@@ -341,8 +349,7 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                 }
                 const uint32_t *Ab = As + buf * lp.Emax * RT;
                 // the widths with a finite load in some row at this cut point
-                uint32_t fmask = 0;
-                for (int m = 0; m < K; m++) fmask |= uint32_t(finw[buf * 16 + m] != 0) << m;
+                const uint32_t fmask = fmw[slot];
                 auto relax = [&](uint4 B, int e, uint32_t tag) {
                     const uint32_t bb[4] = {B.x | tag, B.y | tag, B.z | tag, B.w | tag};
                     uint32_t aa[RT];
@@ -403,8 +410,9 @@ __global__ void __launch_bounds__(kLMaxThreads) sweep_layer_kernel(PassArgs a, i
                     }
                 }
             }
-            if (more) build(j + 1, buf ^ 1);
+            if (more) build(j + 1, buf ^ 1, slot1);
             aborted = __syncthreads_or(!ok) != 0;
+            slot = slot1;
         }
     }
 
