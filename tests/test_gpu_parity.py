@@ -264,23 +264,58 @@ def workload5():
     return insts, gold, tables, last0
 
 
-@pytest.mark.parametrize("variant", [0, 2])
-def test_workload5_full_size_all_instances(workload5, variant):
+@pytest.mark.parametrize("variant,keep_costs", [(0, True), (2, True), (0, False)])
+def test_workload5_full_size_all_instances(workload5, variant, keep_costs):
     """All 1024 instances solved in chunks of 152 (the library's sweep choice, and the
     streaming variant): every status, t_batch, bottleneck and plan against the oracle's
-    stored results, and every table (stage-cost words, per-position loads, DP keys) of
-    two instances against the oracle."""
+    stored results, and every table (stage-cost words when kept, per-position loads, DP
+    keys) of two instances against the oracle.  Without the kept cost tensor the stage
+    loads take the path that never prices strategy groups fitting no position, which is
+    the one solves take by default."""
     insts, gold, tables, last0 = workload5
-    s, res = G.run(insts, chunk=152, variant=variant)
+    s, res = G.run(insts, chunk=152, variant=variant, keep_costs=keep_costs)
     for b in range(1024):
         _, st, t, v, plan = gold[b]
         assert (res[b]["status"], res[b]["t_batch"]) == (st, t), (b, res[b])
         if st == 0:
             assert res[b]["bottleneck"] == v and res[b]["plan"] == plan, (b, res[b])
     for b, (cost, loads, keys) in tables.items():
-        np.testing.assert_array_equal(G.cost_table(s, b - last0, insts[b]), cost)
+        if keep_costs:
+            np.testing.assert_array_equal(G.cost_table(s, b - last0, insts[b]), cost)
         np.testing.assert_array_equal(G.loads_table(s, b - last0, insts[b]), loads)
         np.testing.assert_array_equal(G.dp_keys(s, b - last0, insts[b]), keys)
+
+
+@pytest.mark.parametrize("cfg,B", [(2, 16), (3, 4), (4, 12)])
+def test_loads_without_kept_costs(cfg, B):
+    """The stage loads solves take by default (no kept cost tensor: strategy groups that
+    fit no position are never priced): results, per-position loads and DP keys against
+    the oracle."""
+    insts = synth.config_batch(cfg, B=B)
+    s, res = G.run(insts, keep_costs=False)
+    oracle = G.oracle_many(insts)
+    for b in range(B):
+        assert G.same_result(res[b], oracle[b]), (b, res[b], oracle[b])
+    for b in (0, B - 1):
+        np.testing.assert_array_equal(G.loads_table(s, b, insts[b]), O.loads(insts[b]))
+        o = O.solve(insts[b], want_dp=True)
+        np.testing.assert_array_equal(G.dp_keys(s, b, insts[b]), G.oracle_dp_keys(insts[b], o["dp"]))
+
+
+def test_loads_without_kept_costs_tight_budgets():
+    # budgets from generous to an eighth: more and more strategy groups fit no position
+    insts = []
+    for k in range(240):
+        x = synth.random_tiny(52000 + k, Lmax=7, Dmax=16)
+        x.budget = int(x.budget) // (1 + k % 8)
+        insts.append(x)
+    s, res = G.run(insts, Pcap=6, keep_costs=False)
+    oracle = G.oracle_many(insts)
+    for b in range(len(insts)):
+        assert G.same_result(res[b], oracle[b]), (b, res[b], oracle[b])
+    for b in range(0, 240, 23):
+        if oracle[b]["status"] != 2:
+            np.testing.assert_array_equal(G.loads_table(s, b, insts[b]), O.loads(insts[b]))
 
 
 @pytest.mark.parametrize("part,variant,factor", [(0, 0, 1), (1, 1, 1), (2, 2, 1), (3, 1, 1), (4, 1, 1 << 20)])
