@@ -29,6 +29,10 @@
 //    increasing order and one replaces the cut point's best only when strictly smaller.
 //    Across cut points (visited in increasing j) a later one wins only with a strictly
 //    smaller value, so each cell keeps its best word and its cut point (and c').
+//  - a width whose stage fits no strategy at this position in any row of the block has
+//    no finite A word and can only give no value: the A-word build records the widths
+//    that have one (a mask per cut point), and the whole CTA skips the others, as the
+//    recurrence itself skips transitions without a load.
 // Values up to vmax = 2^(32 - tb) - 3 are exact.  A larger finite value saturates to
 // vmax + 1: it can neither win nor tie against an exact value, so every cell whose
 // optimum is at most vmax still gets its exact key, and a cell whose optimum is
