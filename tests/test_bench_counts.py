@@ -81,3 +81,32 @@ def test_relax_peak_mode():
     assert bench.relax_peak_mode(torus, resident) == 0
     assert bench.relax_peak_mode(dense, streaming) == 1
     assert bench.relax_peak_mode(dense + torus, resident) == 0
+
+
+def test_reference_arm_line():
+    # the reference arm (the oracle on the host cores) prints one JSON line with the
+    # GPU arm's metric, unit and config, and no host-device traffic
+    import json
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--workload", "2", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=300, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert (line["metric"], line["unit"]) == (bench.METRIC, bench.UNIT)
+    assert (line["steps"], line["warmup"], line["n_gpus"]) == (3, 3, 1)
+    batch = synth.config_batch(2)
+    words = sum(bench.cost_words(x) for x in batch)
+    assert line["config"] == bench.bench_config("dense-32L-h4096-64dev", batch, len(batch),
+                                                57229968, words, 1)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"] > 0
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT,
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # under torchrun only rank 0 runs it; the other ranks exit 0 without output
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--workload", "2", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=300, cwd=root, env=env)
+    assert out.returncode == 0 and out.stdout.strip() == "", (out.stdout, out.stderr[-2000:])
