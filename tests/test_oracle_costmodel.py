@@ -338,3 +338,31 @@ def test_context_and_expert_groups_together():
     b = O.terms(inst, 0, 1, 3, 1)   # k = 8: t cp = 4, q = 2, e = 2
     assert b["cpc"] == 4 * ring_gather(2, A // 2, 300, 2 * 10**6)
     assert b["ep"] == 4 * ring_gather(2, V // 4, 5000, 10**6)
+
+
+def test_peak_memory_is_the_sum_of_its_parts():
+    """Nest §3.3: Mem(S, p) = 2 weights + optimizer states + activations + (p - 1)
+    stashed microbatches.  One layer on k = 2 devices with t = 2 (so q = 1, no ZeRO
+    sharding): every part is halved by the tensor split.  The budget is set to the
+    p-th position's total and one byte below it, so pmax must be p and p - 1."""
+    P, A, f, t = 8 * 10**6, 3 * 10**6, 6, 2
+    for p in range(1, 7):
+        total = (2 + f) * P // t + A // t + (p - 1) * (A // t)
+        for budget, want in ((total, p), (total - 1, p - 1)):
+            inst = make(pd=P, aw=A, opt=f, strat=((t, 1, 1, 0, 0),), D=2, G=(2,),
+                        Pmax=8, M=8, budget=budget)
+            assert O.terms(inst, 0, 1, 1, 0)["pmax"] == want, (p, budget)
+
+
+def test_peak_memory_with_recompute():
+    """With activation recompute a stage keeps one layer's activations at a time (the
+    largest) and stashes only its input (the output of the layer before it): stage
+    [1, 3) of a three-layer chain, t = 2 on two devices."""
+    Pd, aw, ao, f, t = (2 * 10**6, 6 * 10**6, 4 * 10**6), (2 * 10**6, 5 * 10**6, 9 * 10**6), \
+        (7 * 10**6, 10**6, 3 * 10**6), 6, 2
+    for p in range(1, 7):
+        total = (2 + f) * (Pd[1] + Pd[2]) // t + max(aw[1], aw[2]) // t + (p - 1) * (ao[0] // t)
+        for budget, want in ((total, p), (total - 1, p - 1)):
+            inst = make(L=3, pd=Pd, aw=aw, ao=ao, opt=f, strat=((t, 1, 1, 0, 1),), D=2,
+                        G=(2,), Pmax=8, M=8, budget=budget)
+            assert O.terms(inst, 1, 3, 1, 0)["pmax"] == want, (p, budget)
