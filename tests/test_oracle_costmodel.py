@@ -366,3 +366,29 @@ def test_peak_memory_with_recompute():
             inst = make(L=3, pd=Pd, aw=aw, ao=ao, opt=f, strat=((t, 1, 1, 0, 1),), D=2,
                         G=(2,), Pmax=8, M=8, budget=budget)
             assert O.terms(inst, 1, 3, 1, 0)["pmax"] == want, (p, budget)
+
+
+def test_context_parallel_splits_compute_and_activations():
+    """Context parallelism splits the sequence over its cp devices: each computes a
+    cp-th of the layer's flops and holds a cp-th of its activations and stash
+    (Nest §3.1 context parallelism; §3.3 memory).  One layer, t = 1, cp = 4 on four
+    devices (q = 1), no activation traffic, so no CP collective."""
+    F_, A, cp = 4 * 10**6, 8 * 10**6, 4
+    strat = ((1, cp, 1, 0, 0),)
+    inst = make(fl=F_, aw=A, strat=strat, D=4, G=(4,))
+    t = O.terms(inst, 0, 1, 2, 0)
+    assert t["comp"] == 3 * F_ // cp and t["cpc"] == 0 and t["tau"] == t["comp"]
+    for p in range(1, 6):
+        total = A // cp + (p - 1) * (A // cp)
+        for budget, want in ((total, p), (total - 1, p - 1)):
+            inst = make(fl=F_, aw=A, strat=strat, D=4, G=(4,), Pmax=8, M=8, budget=budget)
+            assert O.terms(inst, 0, 1, 2, 0)["pmax"] == want, (p, budget)
+
+
+def test_expert_alltoall_counts_moe_layers_only():
+    """The dispatch and combine AllToAlls are issued by the MoE layers alone: a stage of
+    one dense and one MoE layer pays the latency steps of one MoE layer (GShard)."""
+    n, V, alpha, beta = 8, 16 * 10**6, 200, 4 * 10**6
+    inst = make(L=2, a2a=(0, V), moe=(0, 1), G=(8,), bw=(beta,), lat=(alpha,), strat=((1, 1, 8, 0, 0),))
+    t = O.terms(inst, 0, 2, 3, 0)
+    assert t["ep"] == 4 * ring_gather(n, V, alpha, beta)

@@ -136,3 +136,51 @@ def test_one_unit_means_one_stage():
         r = O.solve(inst)
         if r["status"] == 0:
             assert len(r["plan"]) == 1 and r["plan"][0][2] == inst.unit
+
+
+def test_batch_time_ties_go_to_fewer_stages():
+    """Two plans with the same batch time: one stage on both devices (6 compute + 3
+    amortised gradient AllReduce, times M = 2) and a two-stage pipeline of one device
+    each (6, times M + 1 = 3): 18 ns both.  The tie goes to fewer stages."""
+    import brute
+    inst = make(L=2, fl=(2, 2), pd=(3, 3), D=2, G=(2,), bw=(1000,), lat=(0,), Pmax=2, M=2)
+    plans = sorted((t, P, v) for t, P, v, _ in brute.enumerate_plans(inst, O.cost_tensor(inst), O.links(inst)))
+    assert plans[:2] == [(18, 1, 9), (18, 2, 6)]
+    r = O.solve(inst)
+    assert (r["t_batch"], r["bottleneck"], len(r["plan"])) == (18, 9, 1)
+    assert r["plan"][0][:3] == (0, 2, 2)
+
+
+@pytest.mark.parametrize("heavy", [0, 1])
+def test_stage_times_at_the_cap_are_infeasible(heavy):
+    """Stage times (load plus link costs) of 2^40 - 1 ns or more are infeasible.  Two
+    layers whose activations fit one at a time but not together, so the only plans
+    are two one-device stages; the heavy layer's compute plus the 3 ns link lands on
+    the cap exactly, or one below it."""
+    CAP = (1 << 40) - 1
+    for link, ok in ((3, False), (2, True)):
+        fl = [0, 0]
+        fl[heavy] = (CAP - 3) // 3        # compute 3 fl = 2^40 - 4
+        inst = make(L=2, fl=fl, ao=(link, 0), aw=(1, 2), D=2, G=(2,), bw=(1000,), lat=(0,),
+                    Pmax=2, M=2, budget=2, opt=0)
+        assert O.terms(inst, 0, 2, 0, 0)["pmax"] == 0          # both layers: 3 bytes > 2
+        r = O.solve(inst)
+        if ok:
+            assert r["status"] == 0 and r["bottleneck"] == CAP - 3 + link
+            assert r["t_batch"] == (CAP - 3 + link) * 3 and len(r["plan"]) == 2
+        else:
+            assert r["status"] == 1
+            if heavy:   # the last stage's own cell holds no value at the cap either
+                dp = O.solve(inst, want_dp=True)["dp"]
+                assert (dp[1] == O.INF).all()
+
+
+def test_a_stage_load_at_the_cap_is_infeasible():
+    """A one-stage plan whose compute alone is 2^40 - 1 ns has no feasible load; one
+    flop less per pass gives 2^40 - 4 ns, which is feasible."""
+    CAP = (1 << 40) - 1
+    for fl, ok in ((CAP // 3, False), (CAP // 3 - 1, True)):
+        inst = make(fl=fl, D=1, G=(1,))
+        assert (O.cost_tensor(inst)[0, 0, 0] == O.INF) != ok
+        r = O.solve(inst)
+        assert (r["status"], r["t_batch"]) == ((0, CAP - 3) if ok else (1, -1))
